@@ -1,0 +1,410 @@
+"""Benchmark of libfattn's hot path on GB300.
+
+One step = one exact attention forward over the 2 x 16 x 4096 x 128 causal
+bf16 workload (fa_forward) + one paged decode over the 64-sequence x 32-head
+x head 128 workload with contexts uniform in [1, 4096] (fa_paged_decode):
+every row of the hot path.  Inputs are seeded synthetic draws, resident in
+device memory before timing starts.  Each kernel launch is bracketed by CUDA
+events on the stream it runs on; L2 is flushed (a 512 MiB write) before each
+launch, outside the events.
+
+Printed JSON line (rank 0):
+  value          forward TFLOP/s, FLOPs = 4*B*H*N^2*d/2 (causal)
+  decode         decode GB/s over the algorithmic bytes (K/V of every context
+                 token, q, block table entries read, out)
+  roofline       the forward (dominant kernel) against the measured bf16 peak
+  e2e            the same metrics through the C ABI with pinned host buffers,
+                 host<->device copies inside the timed region
+  cpu_baseline   the float64 CPU oracle on the host cores, on a sample
+--impl reference times that oracle alone (the reference arm of this build).
+Multi-GPU (torchrun): each rank runs an independent replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FWD = dict(B=2, H=16, N=4096, d=128, causal=True, seed=3)
+DEC = dict(num_seqs=64, num_heads=32, head_size=128, block_size=16, max_ctx=4096, seed=5)
+L2_FLUSH_BYTES = 512 << 20
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "fwd attention TFLOPS & % of BF16 tensor peak; paged-decode HBM GB/s"
+
+
+def fwd_flops(B, H, N, d, causal, **_):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock, power and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# The GPU arm
+
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_11_gb300 as fa
+    from exact_attention_11_gb300 import _build, inputs
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+    fa.load()
+
+    stream = torch.cuda.Stream(dev)
+    sptr = stream.cuda_stream
+    B, H, N, d, causal = FWD["B"], FWD["H"], FWD["N"], FWD["d"], FWD["causal"]
+    # Each rank draws its own replica (weak scaling): seed offset by rank.
+    q, k, v = (t.to(dev) for t in inputs.forward_inputs(B, H, N, d, torch.bfloat16,
+                                                         seed=FWD["seed"] + 1000 * rank))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    di = inputs.decode_inputs(DEC["num_seqs"], DEC["num_heads"], DEC["head_size"],
+                              DEC["block_size"], DEC["max_ctx"], seed=DEC["seed"] + 1000 * rank,
+                              device=dev)
+    out = torch.empty_like(di.q)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    scale = d ** -0.5
+
+    def run_fwd():
+        fa.fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                      B, H, N, d, scale, causal, sptr)
+
+    S, Hd, D = di.q.shape
+
+    def run_dec():
+        fa.fa_paged_decode(di.q.data_ptr(), di.k_cache.data_ptr(), di.v_cache.data_ptr(),
+                           di.block_tables.data_ptr(), di.context_lens.data_ptr(),
+                           out.data_ptr(), S, Hd, D, di.block_size, di.max_blocks, di.scale, sptr)
+
+    flops = fwd_flops(**FWD)
+    ctx = di.context_lens.to(torch.int64)
+    n_blk = int(((ctx + di.block_size - 1) // di.block_size).sum())
+    dec_bytes = (di.kv_bytes_read() + di.q.numel() * 2 + out.numel() * 2 + n_blk * 4
+                 + S * 4)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            run_fwd()
+            flush.zero_()
+            run_dec()
+    stream.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the load
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.zero_()
+            evs[i][0].record(stream)
+            run_fwd()
+            evs[i][1].record(stream)
+            flush.zero_()
+            evs[i][2].record(stream)
+            run_dec()
+            evs[i][3].record(stream)
+    stream.synchronize()
+    wall = time.perf_counter() - t0
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    dec_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K
+    status = fa.fa_device_status()
+
+    # End to end through the C ABI with pinned host buffers.
+    hq, hk, hv = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3))
+    for h, t in zip((hq, hk, hv), (q, k, v)):
+        h.copy_(t)
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    hdq = torch.empty(di.q.shape, dtype=di.q.dtype, pin_memory=True)
+    hdq.copy_(di.q)
+    hbt = torch.empty(di.block_tables.shape, dtype=torch.int32, pin_memory=True)
+    hbt.copy_(di.block_tables)
+    hcl = torch.empty(di.context_lens.shape, dtype=torch.int32, pin_memory=True)
+    hcl.copy_(di.context_lens)
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dbt, dcl, ddq = (torch.empty_like(di.block_tables), torch.empty_like(di.context_lens),
+                     torch.empty_like(di.q))
+    ke = max(3, min(K, 50))
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(ke)]
+    with torch.cuda.stream(stream):
+        for i in range(ke + 2):
+            rec = i >= 2
+            if rec:
+                e2e_ev[i - 2][0].record(stream)
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            fa.fa_forward(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o.data_ptr(),
+                          lse.data_ptr(), B, H, N, d, scale, causal, sptr)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+            if rec:
+                e2e_ev[i - 2][1].record(stream)
+            ddq.copy_(hdq, non_blocking=True)
+            dbt.copy_(hbt, non_blocking=True)
+            dcl.copy_(hcl, non_blocking=True)
+            fa.fa_paged_decode(ddq.data_ptr(), di.k_cache.data_ptr(), di.v_cache.data_ptr(),
+                               dbt.data_ptr(), dcl.data_ptr(), out.data_ptr(), S, Hd, D,
+                               di.block_size, di.max_blocks, di.scale, sptr)
+            hout.copy_(out, non_blocking=True)
+            if rec:
+                e2e_ev[i - 2][2].record(stream)
+    stream.synchronize()
+    e2e_fwd_ms = sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / ke
+    e2e_dec_ms = sum(e[1].elapsed_time(e[2]) for e in e2e_ev) / ke
+    h2d = 3 * q.numel() * 2 + di.q.numel() * 2 + di.block_tables.numel() * 4 + S * 4
+    d2h = o.numel() * 2 + lse.numel() * 4 + out.numel() * 2
+
+    if ws > 1:
+        t = torch.tensor([fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall], device=dev,
+                         dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall = t.tolist()
+        st = torch.tensor([status], device=dev, dtype=torch.int32)
+        dist.all_reduce(st, op=dist.ReduceOp.MIN)
+        status = int(st.item())
+
+    peaks, peak_kind = read_peaks()
+    tflops = ws * flops / (fwd_ms * 1e-3) / 1e12
+    per_gpu_tflops = flops / (fwd_ms * 1e-3) / 1e12
+    gbs = ws * dec_bytes / (dec_ms * 1e-3) / 1e9
+    per_gpu_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    peak_t = peaks["bf16_tflops"]
+    peak_h = peaks["hbm_gbs"]
+    result = {
+        "metric": METRIC,
+        "value": round(tflops, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(fwd_ms + dec_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) inputs; no dataset)",
+        "config": {
+            "workload": "fa_forward bf16 B=2 H=16 N=4096 d=128 causal + fa_paged_decode bf16 "
+                        "64 seqs x 32 heads x head 128, block 16, ctx U[1,4096]",
+            "fwd": {k_: v_ for k_, v_ in FWD.items() if k_ != "seed"},
+            "decode": {k_: v_ for k_, v_ in DEC.items() if k_ != "seed"},
+            "decode_sum_ctx": int(ctx.sum()),
+            "l2": "flushed (512 MiB write) before every timed launch",
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+        },
+        "fwd_ms": round(fwd_ms, 4),
+        "fwd_frac_of_bf16_peak": round(per_gpu_tflops / peak_t, 4),
+        "decode": {
+            "value": round(gbs, 1), "unit": "GB/s", "ms": round(dec_ms, 4),
+            "bytes_per_launch": dec_bytes,
+            "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1), "peak": peak_h,
+                         "unit": "GB/s", "frac": round(per_gpu_gbs / peak_h, 4),
+                         "traffic": None, "peak_kind": peak_kind},
+        },
+        "roofline": {"bound": "tensor", "achieved": round(per_gpu_tflops, 2), "peak": peak_t,
+                     "unit": "TFLOP/s", "frac": round(per_gpu_tflops / peak_t, 4),
+                     "traffic": None, "peak_kind": f"{peak_kind} bf16 burst",
+                     "kernel": "fwd_bf16_tc_kernel<128>", "flops_per_launch": flops},
+        "e2e": {"value": round(ws * flops / (e2e_fwd_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "decode_gbs": round(ws * dec_bytes / (e2e_dec_ms * 1e-3) / 1e9, 1),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "KV cache resident (serving state); q, K, V, q_decode, block table, "
+                        "context lens copied in and O, LSE, out copied back every step"},
+        "gpu_launches": 2 * K,
+        "clocks": clk,
+        "device_status": status,
+        "wall_s": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if ws > 1:
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+# ---------------------------------------------------------------------------
+# The float64 CPU oracle, timed on the host cores
+
+def _oracle_sample(target_s: float):
+    """Times the oracle forward on whole causal heads of the benchmark's
+    forward workload until about target_s seconds have passed."""
+    import torch
+
+    import oracle
+    from exact_attention_11_gb300 import inputs
+    oracle.build()
+    B, H, N, d = FWD["B"], FWD["H"], FWD["N"], FWD["d"]
+    q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=FWD["seed"])
+    q, k, v = (t.double().numpy() for t in (q, k, v))
+    per_head = fwd_flops(1, 1, N, d, True)
+    cores = oracle.max_threads()
+    heads, t_total = 0, 0.0
+    while heads < B * H:
+        b, h = divmod(heads, H)
+        t0 = time.perf_counter()
+        oracle.attention_forward(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1],
+                                 d ** -0.5, True)
+        t_total += time.perf_counter() - t0
+        heads += 1
+        if t_total >= target_s:
+            break
+    return heads, t_total, per_head * heads / t_total / 1e12, cores
+
+
+def cpu_baseline(target_s: float):
+    heads, secs, tflops, cores = _oracle_sample(target_s)
+    return {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{heads} of the 32 causal heads (N=4096, d=128) of the forward workload, "
+                      f"float64, {secs:.1f} s"}
+
+
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    per_step = []
+    for _ in range(args.warmup):
+        _oracle_sample(0.0)
+    vals, heads_tot, secs_tot, cores = [], 0, 0.0, 1
+    for _ in range(args.steps):
+        heads, secs, tflops, cores = _oracle_sample(args.ref_step_seconds)
+        vals.append(tflops)
+        heads_tot += heads
+        secs_tot += secs
+        per_step.append(secs)
+    value = fwd_flops(1, 1, FWD["N"], FWD["d"], True) * heads_tot / secs_tot / 1e12
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs_tot / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) inputs; no dataset)",
+        "config": {"workload": "fa_forward bf16 B=2 H=16 N=4096 d=128 causal (oracle: whole "
+                               "causal heads per step)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{heads_tot} causal heads over {args.steps} steps"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="approximate CPU time for the oracle baseline sample")
+    ap.add_argument("--ref-step-seconds", type=float, default=0.5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300":
+        ap.error("--warmup must be >= 3")
+    res = reference_arm(args) if args.impl == "reference" else gpu_arm(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,169 @@
+"""Python binding of libfattn: exact attention forward and paged decode on GB300.
+
+The C ABI (``include/fattn.h``) is reached through ctypes.  The functions
+``fa_forward``, ``fa_forward_fp32`` and ``fa_paged_decode`` take the same
+arguments as their C counterparts (device pointers as ints, sizes, a stream
+handle) and only marshal them; every step of the computation runs in the CUDA
+kernels of ``libfattn.so``.  ``forward`` and ``paged_decode`` are torch
+conveniences that allocate the outputs and pass the tensors' device pointers.
+
+There is no fallback: if ``libfattn.so`` is missing, cannot be loaded, or the
+device is not an sm_103 GPU, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = ["fa_forward", "fa_forward_fp32", "fa_paged_decode", "fa_status_string",
+           "fa_device_status", "fa_release", "forward", "paged_decode", "FattnError",
+           "library_path", "load"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libfattn.so")
+_lock = threading.Lock()
+_lib = None
+
+FA_OK = 0
+STATUS_NAMES = {0: "FA_OK", -1: "FA_ERR_INVALID_ARG", -2: "FA_ERR_UNSUPPORTED",
+                -3: "FA_ERR_ALIGNMENT", -4: "FA_ERR_CUDA", -5: "FA_ERR_TIMEOUT",
+                -6: "FA_ERR_NO_MEMORY", -7: "FA_ERR_NO_DEVICE"}
+
+
+class FattnError(RuntimeError):
+    def __init__(self, func: str, status: int):
+        self.status = status
+        super().__init__(f"{func} failed: {STATUS_NAMES.get(status, status)} "
+                         f"({fa_status_string(status)})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+_vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+EXPORTS = {
+    "fa_forward": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "fa_forward_fp32": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "fa_paged_decode": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_status_string": ([_i], ctypes.c_char_p),
+    "fa_device_status": ([], _i),
+    "fa_release": ([], None),
+    "fa_version": ([], _i),
+}
+
+
+def load():
+    """Loads libfattn.so (raising if it is absent) and declares its exports."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"libfattn.so not found at {_LIB_PATH}; build it with "
+                "`python -m exact_attention_11_gb300._build` (needs nvcc)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (args, res) in EXPORTS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(name: str, rc: int) -> int:
+    if rc != FA_OK:
+        raise FattnError(name, rc)
+    return rc
+
+
+# ---------------------------------------------------------------- raw C ABI
+def fa_forward(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
+    return _check("fa_forward", load().fa_forward(q, k, v, o, lse, B, H, N, d, scale,
+                                                  int(causal), stream))
+
+
+def fa_forward_fp32(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
+    return _check("fa_forward_fp32", load().fa_forward_fp32(q, k, v, o, lse, B, H, N, d, scale,
+                                                            int(causal), stream))
+
+
+def fa_paged_decode(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, num_heads,
+                    head_size, block_size, max_num_blocks_per_seq, scale, stream) -> int:
+    return _check("fa_paged_decode", load().fa_paged_decode(
+        q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, num_heads, head_size,
+        block_size, max_num_blocks_per_seq, scale, stream))
+
+
+def fa_status_string(status: int) -> str:
+    try:
+        return load().fa_status_string(status).decode()
+    except Exception:  # library missing: still give a name
+        return STATUS_NAMES.get(status, "unknown")
+
+
+def fa_device_status() -> int:
+    return load().fa_device_status()
+
+
+def fa_release() -> None:
+    load().fa_release()
+
+
+# ---------------------------------------------------------------- torch helpers
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(t):
+    import torch
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def forward(q, k, v, scale=None, causal=False, out=None, lse=None, want_lse=True):
+    """Exact attention on [B,H,N,d] CUDA tensors (bf16 or fp32, contiguous).
+
+    Returns (O, LSE) with O in the input dtype and LSE fp32 [B,H,N] (None when
+    ``want_lse`` is False).  Runs on the current torch stream."""
+    import torch
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B,H,N,d] shape")
+    if not (q.is_cuda and q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous CUDA tensors")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q, k, v must all be bf16 or all fp32")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fn = fa_forward if q.dtype == torch.bfloat16 else fa_forward_fp32
+    fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, float(scale), bool(causal),
+       _stream(q))
+    return out, lse
+
+
+def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale=None, out=None):
+    """Single-query paged decode on CUDA tensors in the layouts of fattn.h."""
+    import torch
+    S, H, D = q.shape
+    nb, Hk, Dx, bs, x = k_cache.shape
+    if Hk != H or Dx * x != D or tuple(v_cache.shape) != (nb, H, D, bs):
+        raise ValueError("inconsistent cache shapes")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    for t in (q, k_cache, v_cache, block_tables, context_lens):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("all decode inputs must be contiguous CUDA tensors")
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    fa_paged_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                    _ptr(context_lens), _ptr(out), S, H, D, bs, block_tables.shape[1],
+                    float(scale), _stream(q))
+    return out

@@ -1,0 +1,237 @@
+// api.cu -- the C ABI of libfattn (declared in include/fattn.h): argument
+// validation, TMA tensor-map encoding, the per-device state the library
+// owns, and kernel launches.  Every public function returns a status code;
+// nothing here aborts or asserts.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fattn.h"
+#include "kernels.h"
+
+namespace {
+
+using fattn::launch_fwd_bf16;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  int *status = nullptr;          // device-side latched status word
+  float *decode_ws = nullptr;     // split-K partials
+  size_t decode_ws_bytes = 0;
+  int *decode_counters = nullptr; // one int per (sequence, head), kept at zero
+  size_t decode_counter_count = 0;
+  int checked = 0;                // 1: sm_103 verified, -1: unsupported
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Resolves the current device and makes sure its state exists.
+int current_device(int *dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_NO_DEVICE;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_NO_DEVICE;
+  DeviceState &st = g_dev[dev];
+  if (st.checked == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA_ERR_NO_DEVICE;
+    st.checked = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (st.checked < 0) return FA_ERR_NO_DEVICE;
+  if (st.status == nullptr) {
+    if (cudaMalloc(&st.status, sizeof(int)) != cudaSuccess) return FA_ERR_NO_MEMORY;
+    if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  *dev_out = dev;
+  return FA_OK;
+}
+
+int get_encoder() {
+  if (g_encode) return FA_OK;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return FA_ERR_CUDA;
+  g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  return FA_OK;
+}
+
+// 3-D bf16 view {d, N, BH} of a [BH, N, d] tensor; boxes of 64 x 128 x 1
+// (one 128-byte row segment per box row) with the 128-byte swizzle.  Rows
+// past N read as zero.
+int encode_qkv_map(CUtensorMap *m, const void *base, int BH, int N, int d) {
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+int check_forward_args(const void *q, const void *k, const void *v, const void *o,
+                       const void *lse, int B, int H, int N, int d, float scale) {
+  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_ALIGNMENT;
+  // Grid and tensor-map limits: B*H and the tile count index 32-bit grids.
+  const long long BH = (long long)B * H;
+  if (BH > 0x7fffffffLL / 2 || (long long)N > 0x7fffffffLL / 2) return FA_ERR_UNSUPPORTED;
+  if (BH * ((N + 127) / 128) > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 10000; }
+
+const char *fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported size";
+    case FA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device-side wait timed out";
+    case FA_ERR_NO_MEMORY: return "out of device memory";
+    case FA_ERR_NO_DEVICE: return "no usable sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+int fa_forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+               int N, int d, float scale, int causal, fa_stream_t stream) {
+  int rc = check_forward_args(q, k, v, o, lse, B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  const int BH = B * H;
+  if (BH == 0 || N == 0) return FA_OK;
+  int dev = 0;
+  CUtensorMap tq, tk, tv;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if ((rc = current_device(&dev)) != FA_OK) return rc;
+    if ((rc = get_encoder()) != FA_OK) return rc;
+  }
+  if ((rc = encode_qkv_map(&tq, q, BH, N, d)) != FA_OK) return rc;
+  if ((rc = encode_qkv_map(&tk, k, BH, N, d)) != FA_OK) return rc;
+  if ((rc = encode_qkv_map(&tv, v, BH, N, d)) != FA_OK) return rc;
+  return cuda_status(launch_fwd_bf16(tq, tk, tv, o, lse, BH, N, d, scale, causal ? 1 : 0,
+                                     g_dev[dev].status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_forward_fp32(const float *q, const float *k, const float *v, float *o, float *lse, int B,
+                    int H, int N, int d, float scale, int causal, fa_stream_t stream) {
+  int rc = check_forward_args(q, k, v, o, lse, B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  const int BH = B * H;
+  if (BH == 0 || N == 0) return FA_OK;
+  if (BH > 0x7fffffff || (N + 31) / 32 > 65535) return FA_ERR_UNSUPPORTED;
+  int dev = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if ((rc = current_device(&dev)) != FA_OK) return rc;
+  }
+  return cuda_status(fattn::launch_fwd_f32(q, k, v, o, lse, BH, N, d, scale, causal ? 1 : 0,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_paged_decode(const void *q, const void *k_cache, const void *v_cache,
+                    const int *block_tables, const int *context_lens, void *out, int num_seqs,
+                    int num_heads, int head_size, int block_size, int max_num_blocks_per_seq,
+                    float scale, fa_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return FA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || num_heads <= 0 || max_num_blocks_per_seq <= 0) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (head_size != fattn::kDecodeHeadSize || block_size != fattn::kDecodeBlockSize)
+    return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return FA_ERR_ALIGNMENT;
+  if (num_heads > 65535 || num_seqs > 65535) return FA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return FA_OK;
+  const int max_parts = fattn::decode_max_parts(max_num_blocks_per_seq);
+  const size_t ws_bytes = fattn::decode_workspace_bytes(num_seqs, num_heads, max_parts);
+  const size_t n_counters = (size_t)num_seqs * num_heads;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float *ws = nullptr;
+  int *counters = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0, rc;
+    if ((rc = current_device(&dev)) != FA_OK) return rc;
+    DeviceState &st = g_dev[dev];
+    if (st.decode_ws_bytes < ws_bytes) {
+      if (st.decode_ws) cudaFree(st.decode_ws);  // synchronises: no launch still uses it
+      st.decode_ws = nullptr;
+      st.decode_ws_bytes = 0;
+      if (cudaMalloc(&st.decode_ws, ws_bytes) != cudaSuccess) return FA_ERR_NO_MEMORY;
+      st.decode_ws_bytes = ws_bytes;
+    }
+    if (st.decode_counter_count < n_counters) {
+      if (st.decode_counters) cudaFree(st.decode_counters);
+      st.decode_counters = nullptr;
+      st.decode_counter_count = 0;
+      if (cudaMalloc(&st.decode_counters, n_counters * sizeof(int)) != cudaSuccess)
+        return FA_ERR_NO_MEMORY;
+      if (cudaMemset(st.decode_counters, 0, n_counters * sizeof(int)) != cudaSuccess)
+        return FA_ERR_CUDA;
+      st.decode_counter_count = n_counters;
+    }
+    ws = st.decode_ws;
+    counters = st.decode_counters;
+  }
+  return cuda_status(fattn::launch_paged_decode(q, k_cache, v_cache, block_tables, context_lens,
+                                                out, num_seqs, num_heads, max_num_blocks_per_seq,
+                                                scale, ws, counters, s));
+}
+
+int fa_device_status(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0, rc;
+  if ((rc = current_device(&dev)) != FA_OK) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, g_dev[dev].status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (h != 0 && cudaMemset(g_dev[dev].status, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  return h;
+}
+
+void fa_release(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+  DeviceState &st = g_dev[dev];
+  if (st.decode_ws) cudaFree(st.decode_ws);
+  if (st.decode_counters) cudaFree(st.decode_counters);
+  if (st.status) cudaFree(st.status);
+  st = DeviceState{};
+}
+
+}  // extern "C"

@@ -1,0 +1,35 @@
+// kernels.h -- launchers shared between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+
+namespace fattn {
+
+constexpr int kDecodeHeadSize = 128;
+constexpr int kDecodeBlockSize = 16;
+constexpr int kDecodePartitionTokens = 512;
+
+cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,
+                           int BH, int N, int d, float scale, int causal, cudaStream_t stream);
+
+// q, k, v tensor maps: 3-D views {d, N, B*H} of the bf16 inputs, 64 x 128 x 1
+// boxes with the 128-byte swizzle.
+cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            void *o, float *lse, int BH, int N, int d, float scale, int causal,
+                            int *dev_status, cudaStream_t stream);
+
+int decode_max_parts(int max_num_blocks_per_seq);
+// Split-K workspace: per (sequence, head, partition) an unnormalised output
+// row and its (max, sum) pair, in fp32.  `counters` holds one int per
+// (sequence, head); it must be all zero before the first launch and every
+// launch leaves it all zero again.
+size_t decode_workspace_bytes(int num_seqs, int num_heads, int max_parts);
+cudaError_t launch_paged_decode(const void *q, const void *k_cache, const void *v_cache,
+                                const int *block_tables, const int *context_lens, void *out,
+                                int num_seqs, int num_heads, int max_blocks, float scale,
+                                float *workspace, int *counters, cudaStream_t stream);
+
+}  // namespace fattn

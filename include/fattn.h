@@ -1,0 +1,143 @@
+/*
+ * fattn.h -- C ABI of libfattn: exact scaled-dot-product attention on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Every call takes plain device pointers and sizes, enqueues its kernels on
+ * `stream` and returns without synchronising.  Nothing here depends on any
+ * framework's tensor types.  Unless a call says otherwise:
+ *
+ *  - All tensor arguments are DEVICE pointers owned by the caller, dense and
+ *    C-contiguous (row-major) in the layout stated for them, and must stay
+ *    valid until the enqueued work has finished.
+ *  - bf16 means IEEE-style bfloat16 (1 sign, 8 exponent, 7 mantissa bits),
+ *    passed as `void *`.
+ *  - The return value is an fa_status_t.  Argument errors are detected on the
+ *    host before anything is enqueued and return a negative code; no call
+ *    ever aborts the process or asserts.  A kernel launch failure returns
+ *    FA_ERR_CUDA.  Errors that only the device can see (a pipeline wait that
+ *    exceeded its time limit) are latched in a per-device status word that
+ *    fa_device_status() reads.
+ *  - NaN or Inf inputs are not checked for; they propagate per IEEE rules.
+ *
+ * The library owns only small per-device state (the split-K workspace of the
+ * paged decode, its counters, and cached launch attributes); fa_release()
+ * frees it.  Calls on one device from several host threads are safe; calls
+ * whose work overlaps on the GPU may share that workspace only if they are
+ * ordered on one stream.
+ */
+#ifndef FATTN_H_
+#define FATTN_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = -1,  /* null pointer, negative size, inconsistent sizes */
+    FA_ERR_UNSUPPORTED = -2,  /* a size the kernels are not built for (e.g. d) */
+    FA_ERR_ALIGNMENT = -3,    /* a pointer not 16-byte aligned */
+    FA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed */
+    FA_ERR_TIMEOUT = -5,      /* a device-side wait exceeded its limit */
+    FA_ERR_NO_MEMORY = -6,    /* the library could not allocate its workspace */
+    FA_ERR_NO_DEVICE = -7     /* no usable sm_103 device is current */
+} fa_status_t;
+
+/*
+ * fa_forward -- exact attention forward, bf16 in / bf16 out, fp32 LSE.
+ *
+ * Computes, for every batch b < B, head h < H and query row i < N,
+ *     O[b,h,i,:] = sum_j softmax_j(scale * Q[b,h,i,:] . K[b,h,j,:]) V[b,h,j,:]
+ *     lse[b,h,i] = ln sum_j exp(scale * Q[b,h,i,:] . K[b,h,j,:])
+ * over the visible keys j: all j < N, or j <= i when causal != 0 (the
+ * causal mask fused in the kernel, as in section 11.3 of "FlashAttention:
+ * GPU 메모리 계층을 활용한 어텐션 최적화 분석", youngju.dev).  The row is
+ * evaluated tile by tile with the online-softmax running max and running sum
+ * of "Flash Attention" (suniverse77.github.io, section "Online Softmax",
+ * eqs. (2)-(4)), so the N x N score matrix never reaches device memory.
+ *
+ *   q, k, v  bf16 [B, H, N, d], read only.
+ *   o        bf16 [B, H, N, d], written (rounded to nearest even).
+ *   lse      fp32 [B, H, N] natural-log log-sum-exp of the scaled scores,
+ *            written; may be NULL when the caller does not need it.
+ *   d        head dimension: 64 or 128 (else FA_ERR_UNSUPPORTED).
+ *   scale    multiplier applied to every score before the softmax (usually
+ *            1/sqrt(d)); must be finite and > 0.
+ *   causal   0 or non-zero.
+ * Products are accumulated in fp32 on the tensor cores; the softmax weights
+ * are rounded to bf16 before they multiply V.  B*H or N equal to 0 is a
+ * no-op that returns FA_OK.  q, k, v, o, lse must be 16-byte aligned.
+ */
+int fa_forward(const void *q, const void *k, const void *v, void *o, float *lse,
+               int B, int H, int N, int d, float scale, int causal,
+               fa_stream_t stream);
+
+/*
+ * fa_forward_fp32 -- the same operation and contract as fa_forward with fp32
+ * q, k, v and o (every product and sum in fp32 on the CUDA cores, no reduced
+ * precision anywhere).  d is 64 or 128.
+ */
+int fa_forward_fp32(const float *q, const float *k, const float *v, float *o, float *lse,
+                    int B, int H, int N, int d, float scale, int causal,
+                    fa_stream_t stream);
+
+/*
+ * fa_paged_decode -- single-query attention over a paged KV cache.
+ *
+ * One query token per sequence attends to all context_lens[s] tokens of its
+ * sequence, whose keys and values live in fixed-size cache blocks found
+ * through the block table ("PagedAttention", data-sketchers.com, sections
+ * "Inputs", "Concepts", "Key" and "Value").  Token t of sequence s is stored
+ * in physical block pb = block_tables[s * max_num_blocks_per_seq +
+ * t / block_size] at offset t % block_size; with x = 8 (bf16 elements in 16
+ * bytes), element c of its key is k_cache[pb][h][c / x][t % block_size][c % x]
+ * and element c of its value is v_cache[pb][h][c][t % block_size].
+ *
+ *   q             bf16 [num_seqs, num_heads, head_size], read only.
+ *   k_cache       bf16 [num_blocks, num_heads, head_size/8, block_size, 8].
+ *   v_cache       bf16 [num_blocks, num_heads, head_size, block_size].
+ *   block_tables  int32 [num_seqs, max_num_blocks_per_seq]; entries past the
+ *                 sequence's last used block are never read.  Entries that
+ *                 are read must be valid block numbers (not checked: the
+ *                 caller owns the cache and knows num_blocks).
+ *   context_lens  int32 [num_seqs], each in [0, max_num_blocks_per_seq *
+ *                 block_size] (not checked on the device).  A sequence with
+ *                 context 0 gets an all-zero output row.
+ *   out           bf16 [num_seqs, num_heads, head_size], written.
+ *   head_size     128;  block_size 16 (else FA_ERR_UNSUPPORTED).
+ *   scale         score multiplier, finite and > 0.
+ * num_kv_heads equals num_heads.  Long contexts are split into partitions
+ * of 512 tokens whose partial (max, sum, output) triples are merged with the
+ * output update of eq. (4) of the "Flash Attention" page; the partials live
+ * in a workspace the library owns and grows on first use for a given size
+ * (cudaMallocAsync on `stream`).  num_seqs == 0 is a no-op.
+ */
+int fa_paged_decode(const void *q, const void *k_cache, const void *v_cache,
+                    const int *block_tables, const int *context_lens, void *out,
+                    int num_seqs, int num_heads, int head_size, int block_size,
+                    int max_num_blocks_per_seq, float scale, fa_stream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *fa_status_string(int status);
+
+/*
+ * Reads and clears the current device's latched device-side status
+ * (FA_OK or FA_ERR_TIMEOUT).  Synchronises the device first.
+ */
+int fa_device_status(void);
+
+/* Frees the library-owned per-device state on the current device.  The
+ * caller must ensure no enqueued libfattn work is still running. */
+void fa_release(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FATTN_H_ */

@@ -1,0 +1,94 @@
+"""The C ABI library builds, loads and exports every symbol fattn.h declares,
+and rejects bad arguments on the host (no compute call needs a GPU here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_11_gb300 as fa
+from exact_attention_11_gb300 import _build
+
+HEADER = os.path.join(_build.INCLUDE, "fattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return fa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fa_forward", "fa_forward_fp32", "fa_paged_decode", "fa_status_string",
+              "fa_device_status", "fa_release", "fa_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in fattn.h but not exported"
+        assert name in fa.EXPORTS, f"{name} has no Python binding"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.fa_version() == 10000
+    assert fa.fa_status_string(0) == "ok"
+    for code in range(-7, 0):
+        assert fa.fa_status_string(code) != "unknown status"
+
+
+NULL = None
+P = 4096  # a 16-byte-aligned fake address: never dereferenced on these paths
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((NULL, P, P, P, NULL, 1, 1, 64, 64, 0.125, 0), -1),      # null q
+    ((P, P, P, P, NULL, -1, 1, 64, 64, 0.125, 0), -1),        # negative B
+    ((P, P, P, P, NULL, 1, 1, 64, 96, 0.125, 0), -2),         # d not 64/128
+    ((P, P, P, P, NULL, 1, 1, 64, 64, 0.0, 0), -1),           # scale 0
+    ((P, P, P, P, NULL, 1, 1, 64, 64, float("nan"), 0), -1),  # scale NaN
+    ((P + 2, P, P, P, NULL, 1, 1, 64, 64, 0.125, 0), -3),     # misaligned q
+    ((P, P, P, P, P + 4, 1, 1, 64, 64, 0.125, 0), -3),        # misaligned lse
+    ((P, P, P, P, NULL, 0, 1, 64, 64, 0.125, 0), 0),          # empty batch: no-op
+    ((P, P, P, P, NULL, 1, 1, 0, 64, 0.125, 0), 0),           # N = 0: no-op
+])
+def test_forward_argument_checks(lib, args, expect):
+    for fn in (lib.fa_forward, lib.fa_forward_fp32):
+        assert fn(*args, None) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((NULL, P, P, P, P, P, 1, 1, 128, 16, 4, 0.1), -1),       # null q
+    ((P, P, P, P, P, P, 1, 1, 64, 16, 4, 0.1), -2),           # head_size 64
+    ((P, P, P, P, P, P, 1, 1, 128, 32, 4, 0.1), -2),          # block_size 32
+    ((P, P, P, P, P, P, 1, 0, 128, 16, 4, 0.1), -1),          # no heads
+    ((P, P, P, P, P, P, 1, 1, 128, 16, 0, 0.1), -1),          # no block-table columns
+    ((P, P + 8, P, P, P, P, 1, 1, 128, 16, 4, 0.1), -3),      # misaligned k_cache
+    ((P, P, P, P, P, P, 0, 1, 128, 16, 4, 0.1), 0),           # no sequences: no-op
+])
+def test_decode_argument_checks(lib, args, expect):
+    assert lib.fa_paged_decode(*args, None) == expect
+
+
+def test_valid_call_without_gpu_fails_loudly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc = lib.fa_forward(P, P, P, P, None, 1, 1, 64, 64, 0.125, 0, None)
+    assert rc == -7  # FA_ERR_NO_DEVICE: never a silent CPU path
+    with pytest.raises(fa.FattnError):
+        fa.fa_forward(P, P, P, P, None, 1, 1, 64, 64, 0.125, 0, None)
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    monkeypatch.setattr(fa, "_LIB_PATH", str(tmp_path / "libfattn.so"))
+    monkeypatch.setattr(fa, "_lib", None)
+    with pytest.raises(RuntimeError, match="not found"):
+        fa.load()
