@@ -54,6 +54,26 @@ def read_peaks():
     return PEAKS_FALLBACK, "fallback"
 
 
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu record, or None when the
+    kernel's sources changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    for src, digest in rec["sources"].items():
+        try:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest()[:16] != digest:
+                    return None
+        except OSError:
+            return None
+    return rec["dram_read_bytes"] + rec["dram_write_bytes"]
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -290,11 +310,13 @@ def gpu_arm(args):
             "bytes_per_launch": dec_bytes,
             "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1), "peak": peak_h,
                          "unit": "GB/s", "frac": round(per_gpu_gbs / peak_h, 4),
-                         "traffic": None, "peak_kind": peak_kind},
+                         "traffic": recorded_traffic("paged_decode_kernel"),
+                         "peak_kind": peak_kind},
         },
         "roofline": {"bound": "tensor", "achieved": round(per_gpu_tflops, 2), "peak": peak_t,
                      "unit": "TFLOP/s", "frac": round(per_gpu_tflops / peak_t, 4),
-                     "traffic": None, "peak_kind": f"{peak_kind} bf16 burst",
+                     "traffic": recorded_traffic("fwd_bf16_tc_kernel<128>"),
+                     "peak_kind": f"{peak_kind} bf16 burst",
                      "kernel": "fwd_bf16_tc_kernel<128>", "flops_per_launch": flops},
         "e2e": {"value": round(ws * flops / (e2e_fwd_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "decode_gbs": round(ws * dec_bytes / (e2e_dec_ms * 1e-3) / 1e9, 1),
