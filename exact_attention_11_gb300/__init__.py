@@ -16,7 +16,8 @@ import ctypes
 import os
 import threading
 
-__all__ = ["fa_forward", "fa_forward_fp32", "fa_paged_decode", "fa_status_string",
+__all__ = ["fa_forward", "fa_forward_fp32", "fa_paged_decode", "fa_paged_decode_noalloc",
+           "fa_status_string",
            "fa_device_status", "fa_release", "forward", "paged_decode", "FattnError",
            "library_path", "load"]
 
@@ -47,6 +48,7 @@ EXPORTS = {
     "fa_forward": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_forward_fp32": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_paged_decode": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_paged_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_status_string": ([_i], ctypes.c_char_p),
     "fa_device_status": ([], _i),
     "fa_release": ([], None),
@@ -93,6 +95,21 @@ def fa_forward_fp32(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
 def fa_paged_decode(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, num_heads,
                     head_size, block_size, max_num_blocks_per_seq, scale, stream) -> int:
     return _check("fa_paged_decode", load().fa_paged_decode(
+        q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, num_heads, head_size,
+        block_size, max_num_blocks_per_seq, scale, stream))
+
+
+def fa_paged_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs,
+                            num_heads, head_size, block_size, max_num_blocks_per_seq, scale,
+                            stream) -> int:
+    """fa_paged_decode for callers that cannot allocate device memory during
+    the call (a process whose memory pool owns all of HBM, a loop that cannot
+    afford cudaMalloc's synchronisation).  The split-K scratch is a fixed
+    12 MiB device array inside the library; larger problems raise
+    FattnError(FA_ERR_UNSUPPORTED).  All calls on a device share that array,
+    so calls that overlap on the GPU must not be issued; the first call on a
+    device should come before any stream capture."""
+    return _check("fa_paged_decode_noalloc", load().fa_paged_decode_noalloc(
         q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, num_heads, head_size,
         block_size, max_num_blocks_per_seq, scale, stream))
 

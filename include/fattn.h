@@ -120,6 +120,38 @@ int fa_paged_decode(const void *q, const void *k_cache, const void *v_cache,
                     int num_seqs, int num_heads, int head_size, int block_size,
                     int max_num_blocks_per_seq, float scale, fa_stream_t stream);
 
+/*
+ * fa_paged_decode_noalloc -- fa_paged_decode for callers that cannot allocate
+ * device memory during a call.  The attention pages have no counterpart to
+ * this entry point; it exists for deployment reasons only.
+ *
+ * Some callers are not allowed to allocate at call time: a serving process
+ * that hands all device memory to its own pool at start-up, a latency-bound
+ * loop that cannot accept the synchronisation cudaMalloc/cudaFree may cause,
+ * a plug-in whose host framework owns every allocation.  fa_paged_decode grows
+ * a library-owned workspace on first use; this call instead keeps the split-K
+ * partials and counters in a fixed 12 MiB device array that is part of the
+ * library image (each device that loads the library holds it until the
+ * process exits), and it calls no allocating CUDA or library routine.
+ *
+ * Arguments, layouts, result and errors are those of fa_paged_decode, plus:
+ *  - FA_ERR_UNSUPPORTED when the problem needs more than the 12 MiB:
+ *    round_up_256(4 * num_seqs * num_heads) +
+ *    520 * num_seqs * num_heads * ceil(max_num_blocks_per_seq / 32) bytes
+ *    (64 sequences x 32 heads x 256 blocks needs about 8.5 MB).
+ *  - Every call on a device shares the one array and leaves its contents in
+ *    place; the counters that must start at zero are cleared on `stream` at
+ *    the start of each call.  Calls whose work overlaps on the GPU race on
+ *    the array: order them on one stream or with events.
+ *  - The first call on a device looks up the array's address
+ *    (cudaGetSymbolAddress) and may load the library's module there; make
+ *    that first call before any stream capture begins.
+ */
+int fa_paged_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                            const int *block_tables, const int *context_lens, void *out,
+                            int num_seqs, int num_heads, int head_size, int block_size,
+                            int max_num_blocks_per_seq, float scale, fa_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *fa_status_string(int status);
 
