@@ -45,6 +45,28 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
+# Kernels that rebalance registers with setmaxnreg: ptxas must give them
+# exactly this many registers per thread at launch, or the warpgroups that
+# raise their count could wait forever for registers that do not exist.
+SETMAXNREG_KERNELS = {"fwd_bf16.cu": ("fwd_bf16_tc_kernel", 168)}
+
+
+def _check_registers(src: str, ptxas_log: str) -> None:
+    if src not in SETMAXNREG_KERNELS:
+        return
+    name, want = SETMAXNREG_KERNELS[src]
+    found = []
+    current = None
+    for line in ptxas_log.splitlines():
+        if "Compiling entry function" in line:
+            current = line
+        elif "Used" in line and "registers" in line and current and name in current:
+            found.append(int(line.split("Used")[1].split("registers")[0]))
+    if not found or any(r != want for r in found):
+        raise RuntimeError(f"{src}: {name} must be built with exactly {want} registers per "
+                           f"thread for its setmaxnreg split; ptxas reported {found}")
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if not force and up_to_date():
         return LIB
@@ -53,10 +75,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [cc, *ARCH, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
+        flags = list(extra_flags)
+        if src in SETMAXNREG_KERNELS and "-Xptxas" not in flags:
+            flags += ["-Xptxas", "-v"]
+        cmd = [cc, *ARCH, *FLAGS, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        _check_registers(src, r.stdout + r.stderr)
         if verbose and (r.stdout or r.stderr):
             print(r.stdout + r.stderr, file=sys.stderr)
         return obj
