@@ -34,6 +34,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 FWD = dict(B=2, H=16, N=4096, d=128, causal=True, seed=3)
+# The long-sequence forward, timed separately and reported nested.
+FWD_LONG = dict(B=1, H=8, N=16384, d=128, causal=True, seed=4, amp=0.5)
 DEC = dict(num_seqs=64, num_heads=32, head_size=128, block_size=16, max_ctx=4096, seed=5)
 L2_FLUSH_BYTES = 512 << 20
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -41,6 +43,8 @@ METRIC = "fwd attention TFLOPS & % of BF16 tensor peak; paged-decode HBM GB/s"
 
 
 def fwd_flops(B, H, N, d, causal, **_):
+    """Algorithmic FLOPs of one forward: QK^T and PV, 2*N*N*d each per head,
+    halved under the causal mask."""
     f = 4.0 * B * H * N * N * d
     return f / 2 if causal else f
 
@@ -218,6 +222,34 @@ def gpu_arm(args):
     dec_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K
     status = fa.fa_device_status()
 
+    peaks, peak_kind = read_peaks()
+
+    # The long-sequence forward: timed the same way, reported as "fwd_long".
+    LB, LH, LN, Ld = FWD_LONG["B"], FWD_LONG["H"], FWD_LONG["N"], FWD_LONG["d"]
+    lq, lk, lv = (t.to(dev) for t in inputs.forward_inputs(
+        LB, LH, LN, Ld, torch.bfloat16, seed=FWD_LONG["seed"] + 1000 * rank, amp=FWD_LONG["amp"]))
+    lo = torch.empty_like(lq)
+    llse = torch.empty((LB, LH, LN), dtype=torch.float32, device=dev)
+
+    def run_long():
+        fa.fa_forward(lq.data_ptr(), lk.data_ptr(), lv.data_ptr(), lo.data_ptr(), llse.data_ptr(),
+                      LB, LH, LN, Ld, Ld ** -0.5, True, sptr)
+
+    kl = max(3, min(K // 4, 100))
+    lev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(kl)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush.zero_()
+            run_long()
+        for i in range(kl):
+            flush.zero_()
+            lev[i][0].record(stream)
+            run_long()
+            lev[i][1].record(stream)
+    stream.synchronize()
+    long_ms = sum(e[0].elapsed_time(e[1]) for e in lev) / kl
+    del lq, lk, lv, lo, llse
+
     # End to end through the C ABI with pinned host buffers.
     hq, hk, hv = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3))
     for h, t in zip((hq, hk, hv), (q, k, v)):
@@ -266,15 +298,14 @@ def gpu_arm(args):
     d2h = o.numel() * 2 + lse.numel() * 4 + out.numel() * 2
 
     if ws > 1:
-        t = torch.tensor([fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall], device=dev,
+        t = torch.tensor([fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms], device=dev,
                          dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall = t.tolist()
+        fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms = t.tolist()
         st = torch.tensor([status], device=dev, dtype=torch.int32)
         dist.all_reduce(st, op=dist.ReduceOp.MIN)
         status = int(st.item())
 
-    peaks, peak_kind = read_peaks()
     tflops = ws * flops / (fwd_ms * 1e-3) / 1e12
     per_gpu_tflops = flops / (fwd_ms * 1e-3) / 1e12
     gbs = ws * dec_bytes / (dec_ms * 1e-3) / 1e9
@@ -302,8 +333,17 @@ def gpu_arm(args):
             "decode_sum_ctx": int(ctx.sum()),
             "l2": "flushed (512 MiB write) before every timed launch",
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+            "sms": torch.cuda.get_device_properties(dev).multi_processor_count,
         },
         "fwd_ms": round(fwd_ms, 4),
+        "fwd_long": {
+            "workload": "fa_forward bf16 B=1 H=8 N=16384 d=128 causal, inputs N(0,1)*0.5",
+            "ms": round(long_ms, 4),
+            "value": round(ws * fwd_flops(**FWD_LONG) / (long_ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s",
+            "frac_of_bf16_peak": round(fwd_flops(**FWD_LONG) / (long_ms * 1e-3) / 1e12
+                                       / peaks["bf16_tflops"], 4),
+        },
         "fwd_frac_of_bf16_peak": round(per_gpu_tflops / peak_t, 4),
         "decode": {
             "value": round(gbs, 1), "unit": "GB/s", "ms": round(dec_ms, 4),
@@ -323,7 +363,7 @@ def gpu_arm(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "KV cache resident (serving state); q, K, V, q_decode, block table, "
                         "context lens copied in and O, LSE, out copied back every step"},
-        "gpu_launches": 2 * K,
+        "gpu_launches": 2 * K + kl + 2 * ke,  # library kernels inside timed regions
         "clocks": clk,
         "device_status": status,
         "wall_s": round(wall, 3),

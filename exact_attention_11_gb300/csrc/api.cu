@@ -25,6 +25,8 @@ struct DeviceState {
   size_t decode_ws_bytes = 0;
   int *decode_counters = nullptr; // one int per (sequence, head), kept at zero
   size_t decode_counter_count = 0;
+  int *fwd_sched = nullptr;       // kFwdSchedSlots pairs of forward work counters, kept at zero
+  unsigned fwd_sched_next = 0;    // slot for the next forward launch
   int checked = 0;                // 1: sm_103 verified, -1: unsupported
 };
 
@@ -56,6 +58,11 @@ int current_device(int *dev_out) {
   if (st.status == nullptr) {
     if (cudaMalloc(&st.status, sizeof(int)) != cudaSuccess) return FA_ERR_NO_MEMORY;
     if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  if (st.fwd_sched == nullptr) {
+    const size_t bytes = sizeof(int) * 2 * fattn::kFwdSchedSlots;
+    if (cudaMalloc(&st.fwd_sched, bytes) != cudaSuccess) return FA_ERR_NO_MEMORY;
+    if (cudaMemset(st.fwd_sched, 0, bytes) != cudaSuccess) return FA_ERR_CUDA;
   }
   *dev_out = dev;
   return FA_OK;
@@ -132,16 +139,19 @@ int fa_forward(const void *q, const void *k, const void *v, void *o, float *lse,
   const int BH = B * H;
   if (BH == 0 || N == 0) return FA_OK;
   int dev = 0;
+  int *sched = nullptr;
   CUtensorMap tq, tk, tv;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if ((rc = current_device(&dev)) != FA_OK) return rc;
     if ((rc = get_encoder()) != FA_OK) return rc;
+    DeviceState &st = g_dev[dev];
+    sched = st.fwd_sched + 2 * (st.fwd_sched_next++ % fattn::kFwdSchedSlots);
   }
   if ((rc = encode_qkv_map(&tq, q, BH, N, d)) != FA_OK) return rc;
   if ((rc = encode_qkv_map(&tk, k, BH, N, d)) != FA_OK) return rc;
   if ((rc = encode_qkv_map(&tv, v, BH, N, d)) != FA_OK) return rc;
-  return cuda_status(launch_fwd_bf16(tq, tk, tv, o, lse, BH, N, d, scale, causal ? 1 : 0,
+  return cuda_status(launch_fwd_bf16(tq, tk, tv, o, lse, BH, N, d, scale, causal ? 1 : 0, sched,
                                      g_dev[dev].status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -231,6 +241,7 @@ void fa_release(void) {
   if (st.decode_ws) cudaFree(st.decode_ws);
   if (st.decode_counters) cudaFree(st.decode_counters);
   if (st.status) cudaFree(st.status);
+  if (st.fwd_sched) cudaFree(st.fwd_sched);
   st = DeviceState{};
 }
 

@@ -10,19 +10,26 @@
 // is rescaled as in eq. (4) and normalised once at the end (youngju.dev,
 // section 8.1), so the score matrix never leaves the SM.
 //
-// GB300 mapping.  One CTA owns two 128-row query tiles, A and B, of one head
-// (256 rows); both use every K/V tile the CTA loads.  Warp roles (the
+// GB300 mapping.  The kernel is persistent: one CTA per SM takes work items
+// from a device-wide counter until none are left, an item being two 128-row
+// query tiles (A and B, 256 rows) of one head.  Items are numbered heaviest
+// first (under the causal mask later query blocks see more keys), so the
+// greedy claim order balances the CTAs' totals (longest-first list
+// scheduling).  The producer warp claims each item and hands its number to
+// the other roles through a two-entry ring in shared memory.  Both tiles of
+// an item use every K/V tile the CTA loads.  Warp roles (the
 // warp-specialised design of youngju.dev section 9.2, "FlashAttention-3",
 // rebuilt on tcgen05 and TMEM):
-//   warp 0      TMA producer: Q_A and Q_B once, then K and V tiles into
-//               separate multi-stage rings
-//   warp 1      MMA issuer:   S_T = Q_T K^T into TMEM; O_T += P_T V with P_T
-//               read from TMEM (T = A, B)
-//   warps 2-3   idle (they complete the producer warpgroup)
-//   warps 4-7   softmax of tile A, one query row per thread
-//   warps 8-11  softmax of tile B
+//   warp 0       TMA producer: Q_A and Q_B per item, K and V tiles into
+//                separate multi-stage rings that run on across items
+//   warp 1       MMA issuer: S_T = Q_T K^T into TMEM; O_T += P_T V with P_T
+//                read from TMEM (T = A, B)
+//   warps 2-3    idle (they complete the producer warpgroup)
+//   warps 4-7    softmax of tile A, one query row per thread, and its epilogue
+//                (O_A / l from TMEM to bf16 rows, and the LSE)
+//   warps 8-11   the same for tile B
 // TMEM (512 columns): S_A | S_B | O_A | O_B.  P_T is written as bf16 over the
-// first half of S_T.  The MMA warp issues, per key tile j,
+// first half of S_T.  Per key tile j the MMA warp issues
 //     PV_A(j)  QK_A(j+1)  PV_B(j)  QK_B(j+1)
 // so while the softmax of A works on S_A(j+1) the tensor core runs PV_B(j)
 // and QK_B(j+1), and vice versa: the two softmax warpgroups take turns on the
@@ -31,6 +38,9 @@
 // order, so QK_T(j+1) overwriting S_T (and the P_T inside it) never overtakes
 // PV_T(j), and the commit that signals S_T(j+1) also certifies that PV_T(j)
 // finished, which lets the softmax warps rescale O_T without another wait.
+// While a softmax warpgroup writes one item's output, the tensor core already
+// computes the next item's first S tiles; the next PV_T cannot start before
+// those warps have read O_T, because it waits for their first P_T.
 //
 // Rescaling the TMEM-resident output is skipped while the row max has grown
 // by at most 8 (log2 units) since the value in use: exponentials are taken
@@ -60,6 +70,7 @@ constexpr uint32_t kRegsProducer = 72, kRegsSoftmax = 216;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+
 template <int D>
 struct Cfg {
   static constexpr int kStages = D == 64 ? 4 : 2;   // K and V ring depth
@@ -79,20 +90,27 @@ struct Cfg {
 // Barrier slots (8 bytes each).
 enum : int {
   kBarQFull = 0,
-  kBarSFull = 1,    // +tile (A, B)
-  kBarPReady = 3,   // +tile
-  kBarODone = 5,    // +tile
-  kBarDrain = 7,
-  kBarKFull = 8,    // +stage (up to 4)
-  kBarKEmpty = 12,
-  kBarVFull = 16,
-  kBarVEmpty = 20,
-  kNumBars = 24
+  kBarQEmpty = 1,
+  kBarSFull = 2,       // +tile (A, B)
+  kBarPReady = 4,      // +tile
+  kBarODone = 6,       // +tile
+  kBarDrain = 12,
+  kBarItemFull = 13,   // +ring slot (2)
+  kBarItemEmpty = 32,  // +ring slot (2)
+  kBarKFull = 16,      // +stage (up to 4)
+  kBarKEmpty = 20,
+  kBarVFull = 24,
+  kBarVEmpty = 28,
+  kNumBars = 34
 };
+// Arrivals that free an item-ring slot: the MMA thread plus every warp of the
+// two softmax warpgroups.
+constexpr int kItemConsumers = 1 + 4 + 4;
 
 struct SmemMisc {
   uint32_t tmem_base;
   int abort;
+  int item[2];
 };
 
 // Waits with a time limit for the phase of parity `ph` of an mbarrier; used
@@ -103,13 +121,25 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t ph) {
   }
 }
 
+// Work item w -> query block, head and the key tiles each query tile needs.
+struct ItemDecoder {
+  int BH, n_qblocks, n_kv_total, causal;
+  __device__ void decode(int w, int &q0, int &bh, int &n_a, int &n_b) const {
+    const int qb = n_qblocks - 1 - w / BH;
+    bh = w % BH;
+    q0 = qb * 2 * BM;
+    n_a = causal ? min(2 * qb + 1, n_kv_total) : n_kv_total;
+    n_b = causal ? min(2 * qb + 2, n_kv_total) : n_kv_total;
+  }
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ o,
                        float *__restrict__ lse, int N, int BH, int n_qblocks, float scale_log2,
-                       int causal, int *__restrict__ dev_status) {
+                       int causal, int *__restrict__ sched, int *__restrict__ dev_status) {
   using C = Cfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -121,25 +151,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   SmemMisc *misc = reinterpret_cast<SmemMisc *>(smem + C::kBar + 8 * kNumBars);
   volatile int *abort_flag = &misc->abort;
 
-  // Heaviest query blocks first: under the causal mask they see more keys.
-  const int qb = n_qblocks - 1 - static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int q0 = qb * 2 * BM;
-  const int n_kv_total = (N + BN - 1) / BN;
-  // Key tiles each query tile needs (causal: up to and including its diagonal).
-  const int n_a = causal ? min(2 * qb + 1, n_kv_total) : n_kv_total;
-  const int n_b = causal ? min(2 * qb + 2, n_kv_total) : n_kv_total;
-  const int n_kv = n_b;  // >= n_a
+  ItemDecoder sch;
+  sch.BH = BH;
+  sch.n_qblocks = n_qblocks;
+  sch.n_kv_total = (N + BN - 1) / BN;
+  sch.causal = causal;
+  const int n_items = n_qblocks * BH;
+  // Consumer side of the item ring: every lane of the calling warp waits for
+  // ring entry k, reads it, and one arrival per warp (or the lone MMA thread)
+  // frees the slot.
+  auto fetch_item = [&](int k, int &w, bool whole_warp) -> bool {
+    const int slot = k & 1;
+    if (!mbar_wait(bar(kBarItemFull + slot), (k >> 1) & 1, abort_flag)) return false;
+    w = *reinterpret_cast<volatile int *>(&misc->item[slot]);
+    if (whole_warp) __syncwarp();
+    if (!whole_warp || (threadIdx.x & 31) == 0) mbar_arrive(bar(kBarItemEmpty + slot));
+    return true;
+  };
 
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarQEmpty), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(kBarSFull + t), 1);
-      mbar_init(bar(kBarPReady + t), 128);
+      mbar_init(bar(kBarPReady + t), 4);   // one arrival per softmax warp
       mbar_init(bar(kBarODone + t), 1);
     }
     mbar_init(bar(kBarDrain), 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar(kBarItemFull + k), 1);
+      mbar_init(bar(kBarItemEmpty + k), kItemConsumers);
+    }
     for (int s = 0; s < S; ++s) {
       mbar_init(bar(kBarKFull + s), 1);
       mbar_init(bar(kBarKEmpty + s), 1);
@@ -157,53 +200,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
+
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (elect_one()) {
+    static_assert(kRegsProducer + 2 * kRegsSoftmax == 3 * 168,
+                  "the warpgroup register split must use exactly the launch budget");
+    if (warp == 0 && elect_one()) {
+      // ---------------------------------------------------------- TMA producer
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar(kBarQFull), 2 * C::kTileBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(s_base + C::kQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, b * 64,
-                      q0 + t * BM, bh, bar(kBarQFull));
-      int nk = 0, nv = 0;  // tiles issued
+      int it = 0, kv = 0, nk = 0, nv = 0;
       bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int st = j % S;
-        const uint32_t ph = (j / S) & 1;
-        if (!(ok = mbar_wait(bar(kBarKEmpty + st), ph ^ 1, abort_flag))) break;
-        mbar_arrive_expect_tx(bar(kBarKFull + st), C::kTileBytes);
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(s_base + C::kK0 + st * C::kTileBytes + b * C::kBoxBytes, &tm_k, b * 64,
-                      j * BN, bh, bar(kBarKFull + st));
-        ++nk;
-        if (!(ok = mbar_wait(bar(kBarVEmpty + st), ph ^ 1, abort_flag))) break;
-        mbar_arrive_expect_tx(bar(kBarVFull + st), C::kTileBytes);
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(s_base + C::kV0 + st * C::kTileBytes + b * C::kBoxBytes, &tm_v, b * 64,
-                      j * BN, bh, bar(kBarVFull + st));
-        ++nv;
+      for (int k = 0; ok; ++k) {
+        // Claim the next item and publish it to the other roles.
+        const int slot = k & 1;
+        if (!(ok = mbar_wait(bar(kBarItemEmpty + slot), ((k >> 1) & 1) ^ 1, abort_flag))) break;
+        const int w = atomicAdd(sched, 1);
+        misc->item[slot] = w;
+        mbar_arrive(bar(kBarItemFull + slot));
+        if (w >= n_items) break;
+        int q0, bh, n_a, n_b;
+        sch.decode(w, q0, bh, n_a, n_b);
+        if (!(ok = mbar_wait(bar(kBarQEmpty), (it & 1) ^ 1, abort_flag))) break;
+        mbar_arrive_expect_tx(bar(kBarQFull), 2 * C::kTileBytes);
+        for (int t = 0; t < 2; ++t)
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(s_base + C::kQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, b * 64,
+                        q0 + t * BM, bh, bar(kBarQFull));
+        for (int j = 0; j < n_b; ++j, ++kv) {
+          const int st = kv % S;
+          const uint32_t ph = (kv / S) & 1;
+          if (!(ok = mbar_wait(bar(kBarKEmpty + st), ph ^ 1, abort_flag))) break;
+          mbar_arrive_expect_tx(bar(kBarKFull + st), C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(s_base + C::kK0 + st * C::kTileBytes + b * C::kBoxBytes, &tm_k, b * 64,
+                        j * BN, bh, bar(kBarKFull + st));
+          nk = kv + 1;
+          if (!(ok = mbar_wait(bar(kBarVEmpty + st), ph ^ 1, abort_flag))) break;
+          mbar_arrive_expect_tx(bar(kBarVFull + st), C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(s_base + C::kV0 + st * C::kTileBytes + b * C::kBoxBytes, &tm_v, b * 64,
+                        j * BN, bh, bar(kBarVFull + st));
+          nv = kv + 1;
+        }
+        ++it;
       }
       if (!ok) {
         // Let the copies in flight land before the CTA exits.
-        drain_wait(bar(kBarQFull), 0);
+        if (it > 0) drain_wait(bar(kBarQFull), (it - 1) & 1);
         for (int i = (nk > S ? nk - S : 0); i < nk; ++i)
           drain_wait(bar(kBarKFull + i % S), (i / S) & 1);
         for (int i = (nv > S ? nv - S : 0); i < nv; ++i)
           drain_wait(bar(kBarVFull + i % S), (i / S) & 1);
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (elect_one()) {
+    } else if (warp == 1 && elect_one()) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
-      auto qk = [&](int t, int j) {
-        const uint32_t k_addr = s_base + C::kK0 + (j % S) * C::kTileBytes;
+      auto qk = [&](int t, int kvi) {
+        const uint32_t k_addr = s_base + C::kK0 + (kvi % S) * C::kTileBytes;
         const uint32_t q_addr = s_base + C::kQ + t * C::kTileBytes;
         const uint32_t s_col = t ? C::kColS1 : C::kColS0;
 #pragma unroll
@@ -214,146 +270,167 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar(kBarSFull + t));
       };
-      auto pv = [&](int t, int j) {
-        const uint32_t v_addr = s_base + C::kV0 + (j % S) * C::kTileBytes;
+      auto pv = [&](int t, int kvi, bool first) {
+        const uint32_t v_addr = s_base + C::kV0 + (kvi % S) * C::kTileBytes;
         const uint32_t s_col = t ? C::kColS1 : C::kColS0;
         const uint32_t o_col = t ? C::kColO1 : C::kColO0;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts(tmem + o_col, tmem + s_col + kk * 8,
                  smem_desc_sw128(v_addr + kk * 2048, C::kBoxBytes, 1024), idesc_pv,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+                 (!first || kk > 0) ? 1u : 0u);
       };
-      auto wait_k = [&](int j) {
-        return mbar_wait(bar(kBarKFull + j % S), (j / S) & 1, abort_flag);
+      auto wait_k = [&](int kvi) {
+        return mbar_wait(bar(kBarKFull + kvi % S), (kvi / S) & 1, abort_flag);
       };
-      bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag) && wait_k(0);
-      if (ok) {
+      int it = 0, kv = 0, cnt_a = 0, cnt_b = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        int w;
+        if (!(ok = fetch_item(k, w, false)) || w >= n_items) break;
+        int q0, bh, n_a, n_b;
+        sch.decode(w, q0, bh, n_a, n_b);
+        if (!(ok = mbar_wait(bar(kBarQFull), it & 1, abort_flag) && wait_k(kv))) break;
         tc_fence_after();
-        qk(0, 0);
-        qk(1, 0);
-        mma_commit(bar(kBarKEmpty + 0));
-      }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int st = j % S;
-        if (!(ok = mbar_wait(bar(kBarVFull + st), (j / S) & 1, abort_flag))) break;
-        bool k_next_ready = false;
-        if (j < n_a) {
-          if (!(ok = mbar_wait(bar(kBarPReady + 0), j & 1, abort_flag))) break;
-          tc_fence_after();
-          pv(0, j);
-          if (j == n_a - 1) mma_commit(bar(kBarODone + 0));
-          if (j + 1 < n_a) {
-            if (!(ok = wait_k(j + 1))) break;
-            k_next_ready = true;
+        qk(0, kv);
+        qk(1, kv);
+        mma_commit(bar(kBarKEmpty + kv % S));
+        if (n_b == 1) mma_commit(bar(kBarQEmpty));
+        for (int j = 0; j < n_b; ++j) {
+          const int kvj = kv + j;
+          const int st = kvj % S;
+          if (!(ok = mbar_wait(bar(kBarVFull + st), (kvj / S) & 1, abort_flag))) break;
+          bool k_next_ready = false;
+          if (j < n_a) {
+            if (!(ok = mbar_wait(bar(kBarPReady + 0), cnt_a & 1, abort_flag))) break;
             tc_fence_after();
-            qk(0, j + 1);
+            pv(0, kvj, j == 0);
+            ++cnt_a;
+            if (j == n_a - 1) mma_commit(bar(kBarODone + 0));
+            if (j + 1 < n_a) {
+              if (!(ok = wait_k(kvj + 1))) break;
+              k_next_ready = true;
+              tc_fence_after();
+              qk(0, kvj + 1);
+            }
+          }
+          if (!(ok = mbar_wait(bar(kBarPReady + 1), cnt_b & 1, abort_flag))) break;
+          tc_fence_after();
+          pv(1, kvj, j == 0);
+          ++cnt_b;
+          mma_commit(bar(kBarVEmpty + st));
+          if (j == n_b - 1) mma_commit(bar(kBarODone + 1));
+          if (j + 1 < n_b) {
+            if (!k_next_ready && !(ok = wait_k(kvj + 1))) break;
+            tc_fence_after();
+            qk(1, kvj + 1);
+            mma_commit(bar(kBarKEmpty + (kvj + 1) % S));
+            if (j + 2 == n_b) mma_commit(bar(kBarQEmpty));  // last QK of the item
           }
         }
-        if (!(ok = mbar_wait(bar(kBarPReady + 1), j & 1, abort_flag))) break;
-        tc_fence_after();
-        pv(1, j);
-        mma_commit(bar(kBarVEmpty + st));
-        if (j == n_b - 1) mma_commit(bar(kBarODone + 1));
-        if (j + 1 < n_b) {
-          if (!k_next_ready && !(ok = wait_k(j + 1))) break;
-          tc_fence_after();
-          qk(1, j + 1);
-          mma_commit(bar(kBarKEmpty + (j + 1) % S));
-        }
+        kv += n_b;
+        ++it;
       }
       // Drain: every MMA issued above has completed once this phase does.
       mma_commit(bar(kBarDrain));
       drain_wait(bar(kBarDrain), 0);
     }
-  }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;                 // query tile: 0 = A, 1 = B
     const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31
-    const int r = quarter * 32 + (threadIdx.x & 31);
-    const int row = q0 + t * BM + r;
+    const int r_local = quarter * 32 + (threadIdx.x & 31);
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_tmem = tmem + lane_off + (t ? C::kColS1 : C::kColS0);
     const uint32_t o_tmem = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
-    const int n_mine = t ? n_b : n_a;
     const uint64_t c2 = f2(scale_log2, scale_log2);
-    float m = -INFINITY, l = 0.f;
+    int it = 0, sc = 0;
     bool ok = true;
-    for (int j = 0; j < n_mine; ++j) {
-      if (!(ok = mbar_wait(bar(kBarSFull + t), j & 1, abort_flag))) break;
-      tc_fence_after();
-      uint32_t sv[4][32];
+    for (int k = 0; ok; ++k) {
+      int w;
+      if (!(ok = fetch_item(k, w, true)) || w >= n_items) break;
+      int q0, bh, n_a, n_b;
+      sch.decode(w, q0, bh, n_a, n_b);
+      const int row = q0 + t * BM + r_local;
+      const int n_mine = t ? n_b : n_a;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < n_mine; ++j, ++sc) {
+        if (!(ok = mbar_wait(bar(kBarSFull + t), sc & 1, abort_flag))) break;
+        tc_fence_after();
+        uint32_t sv[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + c * 32, sv[c]);
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + c * 32, sv[c]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_wait_ld(sv[c]);
+        for (int c = 0; c < 4; ++c) tmem_wait_ld(sv[c]);
 #define S_(c) sv[(c) >> 5][(c) & 31]
-      if (j == n_mine - 1) {
-        // Keys past the sequence end, and (causal) keys after the query row.
-        const int lim = (causal ? min(N, row + 1) : N) - j * BN;
+        if (j == n_mine - 1) {
+          // Keys past the sequence end, and (causal) keys after the query row.
+          const int lim = (causal ? min(N, row + 1) : N) - j * BN;
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c >= lim) S_(c) = __float_as_uint(-INFINITY);
-      }
-      float mx[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-        mx[a] = fmaxf(__uint_as_float(S_(2 * a)), __uint_as_float(S_(2 * a + 1)));
-#pragma unroll
-      for (int c = 8; c < BN; c += 8)
+          for (int c = 0; c < BN; ++c)
+            if (c >= lim) S_(c) = __float_as_uint(-INFINITY);
+        }
+        float mx[4];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
-          mx[a] = fmax3(mx[a], __uint_as_float(S_(c + 2 * a)), __uint_as_float(S_(c + 2 * a + 1)));
-      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
-      float alpha = 1.f;
-      if (tmax > m + kRescaleThreshold) {  // also true while m = -inf
-        alpha = ex2_approx(m - tmax);
-        m = tmax;
-      }
-      const uint64_t nm2 = f2(-m, -m);
-      uint64_t sum2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+          mx[a] = fmaxf(__uint_as_float(S_(2 * a)), __uint_as_float(S_(2 * a + 1)));
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
+        for (int c = 8; c < BN; c += 8)
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float2 x = f2_split(
-              ffma2(f2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), c2, nm2));
-          const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-          sum2[(e >> 1) & 1] = fadd2(sum2[(e >> 1) & 1], f2(p0, p1));
-          pk[e >> 1] = pack_bf16x2(p0, p1);
+          for (int a = 0; a < 4; ++a)
+            mx[a] = fmax3(mx[a], __uint_as_float(S_(c + 2 * a)), __uint_as_float(S_(c + 2 * a + 1)));
+        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+        float alpha = 1.f;
+        if (tmax > m + kRescaleThreshold) {  // also true while m = -inf
+          alpha = ex2_approx(m - tmax);
+          m = tmax;
         }
-        tmem_st16(s_tmem + c * 16, pk);
-      }
-#undef S_
-      const float2 sa = f2_split(fadd2(sum2[0], sum2[1]));
-      l = l * alpha + (sa.x + sa.y);
-      // PV_T(j-1) was issued before QK_T(j), so O_T is complete: rescale it.
-      if (j > 0 && __any_sync(~0u, alpha != 1.f)) {
-        const uint64_t a2 = f2(alpha, alpha);
+        const uint64_t nm2 = f2(-m, -m);
+        uint64_t sum2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(o_tmem + c * 32, ov);
-          tmem_wait_ld(ov);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float2 x =
-                f2_split(fmul2(f2(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])), a2));
-            ov[e] = __float_as_uint(x.x);
-            ov[e + 1] = __float_as_uint(x.y);
+            const uint64_t x2 =
+                ffma2(f2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), c2, nm2);
+            const float2 x = f2_split(x2);
+            const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            sum2[(e >> 1) & 1] = fadd2(sum2[(e >> 1) & 1], f2(p.x, p.y));
+            pk[e >> 1] = pack_bf16x2(p.x, p.y);
           }
-          tmem_st32(o_tmem + c * 32, ov);
+          tmem_st16(s_tmem + c * 16, pk);
         }
+#undef S_
+        const float2 sa = f2_split(fadd2(sum2[0], sum2[1]));
+        l = l * alpha + (sa.x + sa.y);
+        // PV_T(j-1) was issued before QK_T(j), so O_T is complete: rescale it.
+        if (j > 0 && __any_sync(~0u, alpha != 1.f)) {
+          const uint64_t a2 = f2(alpha, alpha);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(o_tmem + c * 32, ov);
+            tmem_wait_ld(ov);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 x =
+                  f2_split(fmul2(f2(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])), a2));
+              ov[e] = __float_as_uint(x.x);
+              ov[e + 1] = __float_as_uint(x.y);
+            }
+            tmem_st32(o_tmem + c * 32, ov);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(bar(kBarPReady + t));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(kBarPReady + t));
-    }
-    if (ok) ok = mbar_wait(bar(kBarODone + t), 0, abort_flag);
-    if (ok) {
+      if (!ok) break;
+      // Epilogue: O_T / l as bf16 rows and the LSE, once the last PV_T is done.
+      if (!(ok = mbar_wait(bar(kBarODone + t), it & 1, abort_flag))) break;
       tc_fence_after();
       const float inv_l = 1.f / l;
       __nv_bfloat16 *orow = o + (static_cast<int64_t>(bh) * N + row) * D;
@@ -366,21 +443,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv_l,
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv_l,
                               __uint_as_float(ov[8 * e + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv_l,
+            v.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv_l,
                               __uint_as_float(ov[8 * e + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv_l,
+            v.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv_l,
                               __uint_as_float(ov[8 * e + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv_l,
+            v.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv_l,
                               __uint_as_float(ov[8 * e + 7]) * inv_l);
-            dst[e] = w;
+            dst[e] = v;
           }
         }
       }
       if (lse != nullptr && row < N)
         lse[static_cast<int64_t>(bh) * N + row] = (m + __log2f(l)) * 0.6931471805599453f;
+      ++it;
     }
   }
 
@@ -390,23 +468,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (threadIdx.x == 0 && misc->abort) atomicExch(dev_status, kDevTimeout);
+  if (threadIdx.x == 0) {
+    if (misc->abort) atomicExch(dev_status, kDevTimeout);
+    // The last CTA to finish returns the item counter to zero for the next
+    // launch that uses this slot: every CTA has stopped claiming by now.
+    __threadfence();
+    if (atomicAdd(sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      sched[0] = 0;
+      sched[1] = 0;
+      __threadfence();
+    }
+  }
 }
+
+int g_num_sms[64] = {};
 
 template <int D>
 cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, void *o,
-                     float *lse, int BH, int N, float scale, int causal, int *dev_status,
-                     cudaStream_t stream) {
+                     float *lse, int BH, int N, float scale, int causal, int *sched,
+                     int *dev_status, cudaStream_t stream) {
   using C = Cfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_tc_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (g_num_sms[dev] == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_num_sms[dev] = n;
+  }
+  e = cudaFuncSetAttribute(fwd_bf16_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_qblocks = (N + 2 * BM - 1) / (2 * BM);
+  const long long n_items = static_cast<long long>(n_qblocks) * BH;
+  const int grid = static_cast<int>(n_items < g_num_sms[dev] ? n_items : g_num_sms[dev]);
   const float scale_log2 = scale * 1.4426950408889634f;
-  dim3 grid(n_qblocks * BH);
   fwd_bf16_tc_kernel<D><<<grid, kThreads, C::kAlloc, stream>>>(
       tq, tk, tv, reinterpret_cast<__nv_bfloat16 *>(o), lse, N, BH, n_qblocks, scale_log2, causal,
-      dev_status);
+      sched, dev_status);
   return cudaGetLastError();
 }
 
@@ -414,9 +515,10 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
 
 cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             void *o, float *lse, int BH, int N, int d, float scale, int causal,
-                            int *dev_status, cudaStream_t stream) {
-  if (d == 64) return launch_d<64>(tq, tk, tv, o, lse, BH, N, scale, causal, dev_status, stream);
-  return launch_d<128>(tq, tk, tv, o, lse, BH, N, scale, causal, dev_status, stream);
+                            int *sched, int *dev_status, cudaStream_t stream) {
+  if (d == 64)
+    return launch_d<64>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status, stream);
+  return launch_d<128>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status, stream);
 }
 
 }  // namespace fattn

@@ -16,10 +16,14 @@ cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float
                            int BH, int N, int d, float scale, int causal, cudaStream_t stream);
 
 // q, k, v tensor maps: 3-D views {d, N, B*H} of the bf16 inputs, 64 x 128 x 1
-// boxes with the 128-byte swizzle.
+// boxes with the 128-byte swizzle.  `sched` points to two ints (the item
+// counter and the finished-CTA counter) that are zero before the launch; the
+// kernel leaves them zero.  Launches that may run at the same time need
+// different `sched` slots.
+constexpr int kFwdSchedSlots = 64;
 cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             void *o, float *lse, int BH, int N, int d, float scale, int causal,
-                            int *dev_status, cudaStream_t stream);
+                            int *sched, int *dev_status, cudaStream_t stream);
 
 int decode_max_parts(int max_num_blocks_per_seq);
 // Split-K workspace: per (sequence, head, partition) an unnormalised output
