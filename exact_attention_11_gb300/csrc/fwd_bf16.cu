@@ -92,8 +92,8 @@ enum : int {
   kBarQFull = 0,
   kBarQEmpty = 1,
   kBarSFull = 2,       // +tile (A, B)
-  kBarPReady = 4,      // +tile
-  kBarODone = 6,       // +tile
+  kBarPReady = 4,      // +2 * tile + half: the first / second 64 columns of P
+  kBarODone = 8,       // +tile
   kBarDrain = 12,
   kBarItemFull = 13,   // +ring slot (2)
   kBarItemEmpty = 32,  // +ring slot (2)
@@ -175,7 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarQEmpty), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(kBarSFull + t), 1);
-      mbar_init(bar(kBarPReady + t), 4);   // one arrival per softmax warp
+      mbar_init(bar(kBarPReady + 2 * t), 4);      // one arrival per softmax warp
+      mbar_init(bar(kBarPReady + 2 * t + 1), 4);
       mbar_init(bar(kBarODone + t), 1);
     }
     mbar_init(bar(kBarDrain), 1);
@@ -258,27 +259,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
+      // Shared-memory descriptors are built once; moving an operand by `off`
+      // bytes adds off >> 4 to the start-address field, which cannot carry
+      // out of its 14 bits for addresses inside the 228 KB shared window.
+      const uint64_t dq = smem_desc_sw128(s_base + C::kQ, 16, 1024);
+      const uint64_t dk = smem_desc_sw128(s_base + C::kK0, 16, 1024);
+      const uint64_t dv = smem_desc_sw128(s_base + C::kV0, C::kBoxBytes, 1024);
       auto qk = [&](int t, int kvi) {
-        const uint32_t k_addr = s_base + C::kK0 + (kvi % S) * C::kTileBytes;
-        const uint32_t q_addr = s_base + C::kQ + t * C::kTileBytes;
-        const uint32_t s_col = t ? C::kColS1 : C::kColS0;
+        const uint64_t a = dq + ((t * C::kTileBytes) >> 4);
+        const uint64_t b = dk + (((kvi % S) * C::kTileBytes) >> 4);
+        const uint32_t s_col = tmem + (t ? C::kColS1 : C::kColS0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + s_col, smem_desc_sw128(q_addr + off, 16, 1024),
-                 smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(s_col, a + off, b + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(kBarSFull + t));
       };
-      auto pv = [&](int t, int kvi, bool first) {
-        const uint32_t v_addr = s_base + C::kV0 + (kvi % S) * C::kTileBytes;
-        const uint32_t s_col = t ? C::kColS1 : C::kColS0;
-        const uint32_t o_col = t ? C::kColO1 : C::kColO0;
+      // Half h of O_T += P_T V: keys 64h .. 64h+63 of the tile.
+      auto pv = [&](int t, int kvi, bool first, int h) {
+        const uint64_t b = dv + (((kvi % S) * C::kTileBytes) >> 4);
+        const uint32_t s_col = tmem + (t ? C::kColS1 : C::kColS0);
+        const uint32_t o_col = tmem + (t ? C::kColO1 : C::kColO0);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + o_col, tmem + s_col + kk * 8,
-                 smem_desc_sw128(v_addr + kk * 2048, C::kBoxBytes, 1024), idesc_pv,
+        for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+          mma_ts(o_col, s_col + kk * 8, b + ((kk * 2048) >> 4), idesc_pv,
                  (!first || kk > 0) ? 1u : 0u);
+      };
+      auto wait_p = [&](int t, int h, int cnt) {
+        return mbar_wait(bar(kBarPReady + 2 * t + h), cnt & 1, abort_flag);
       };
       auto wait_k = [&](int kvi) {
         return mbar_wait(bar(kBarKFull + kvi % S), (kvi / S) & 1, abort_flag);
@@ -302,9 +311,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(bar(kBarVFull + st), (kvj / S) & 1, abort_flag))) break;
           bool k_next_ready = false;
           if (j < n_a) {
-            if (!(ok = mbar_wait(bar(kBarPReady + 0), cnt_a & 1, abort_flag))) break;
+            if (!(ok = wait_p(0, 0, cnt_a))) break;
             tc_fence_after();
-            pv(0, kvj, j == 0);
+            pv(0, kvj, j == 0, 0);
+            if (!(ok = wait_p(0, 1, cnt_a))) break;
+            tc_fence_after();
+            pv(0, kvj, j == 0, 1);
             ++cnt_a;
             if (j == n_a - 1) mma_commit(bar(kBarODone + 0));
             if (j + 1 < n_a) {
@@ -314,9 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               qk(0, kvj + 1);
             }
           }
-          if (!(ok = mbar_wait(bar(kBarPReady + 1), cnt_b & 1, abort_flag))) break;
+          if (!(ok = wait_p(1, 0, cnt_b))) break;
           tc_fence_after();
-          pv(1, kvj, j == 0);
+          pv(1, kvj, j == 0, 0);
+          if (!(ok = wait_p(1, 1, cnt_b))) break;
+          tc_fence_after();
+          pv(1, kvj, j == 0, 1);
           ++cnt_b;
           mma_commit(bar(kBarVEmpty + st));
           if (j == n_b - 1) mma_commit(bar(kBarODone + 1));
@@ -386,26 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha = ex2_approx(m - tmax);
           m = tmax;
         }
-        const uint64_t nm2 = f2(-m, -m);
-        uint64_t sum2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const uint64_t x2 =
-                ffma2(f2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), c2, nm2);
-            const float2 x = f2_split(x2);
-            const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            sum2[(e >> 1) & 1] = fadd2(sum2[(e >> 1) & 1], f2(p.x, p.y));
-            pk[e >> 1] = pack_bf16x2(p.x, p.y);
-          }
-          tmem_st16(s_tmem + c * 16, pk);
-        }
-#undef S_
-        const float2 sa = f2_split(fadd2(sum2[0], sum2[1]));
-        l = l * alpha + (sa.x + sa.y);
-        // PV_T(j-1) was issued before QK_T(j), so O_T is complete: rescale it.
+        // PV_T(j-1) was issued before QK_T(j), so O_T is complete: rescale it
+        // before the first half of P lets PV_T(j) accumulate into it.
         if (j > 0 && __any_sync(~0u, alpha != 1.f)) {
           const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
@@ -423,10 +420,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(o_tmem + c * 32, ov);
           }
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if ((threadIdx.x & 31) == 0) mbar_arrive(bar(kBarPReady + t));
+        const uint64_t nm2 = f2(-m, -m);
+        uint64_t sum2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const uint64_t x2 =
+                ffma2(f2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), c2, nm2);
+            const float2 x = f2_split(x2);
+            const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            sum2[(e >> 1) & 1] = fadd2(sum2[(e >> 1) & 1], f2(p.x, p.y));
+            pk[e >> 1] = pack_bf16x2(p.x, p.y);
+          }
+          tmem_st16(s_tmem + c * 16, pk);
+          if (c & 1) {
+            // Columns 0-63 (then 64-127) of P are in TMEM: let PV_T use them.
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(bar(kBarPReady + 2 * t + (c >> 1)));
+          }
+        }
+#undef S_
+        const float2 sa = f2_split(fadd2(sum2[0], sum2[1]));
+        l = l * alpha + (sa.x + sa.y);
       }
       if (!ok) break;
       // Epilogue: O_T / l as bf16 rows and the LSE, once the last PV_T is done.
