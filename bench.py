@@ -378,54 +378,71 @@ def gpu_arm(args):
 # ---------------------------------------------------------------------------
 # The float64 CPU oracle, timed on the host cores
 
-def _oracle_sample(target_s: float):
-    """Times the oracle forward on whole causal heads of the benchmark's
-    forward workload until about target_s seconds have passed."""
-    import torch
+class OracleSampler:
+    """Times the float64 oracle on the forward workload, in units of 256
+    consecutive query rows of one head (causal), visited in a fixed order, until
+    a time budget is spent.  Inputs are drawn once, like the GPU arm's."""
 
-    import oracle
-    from exact_attention_11_gb300 import inputs
-    oracle.build()
-    B, H, N, d = FWD["B"], FWD["H"], FWD["N"], FWD["d"]
-    q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=FWD["seed"])
-    q, k, v = (t.double().numpy() for t in (q, k, v))
-    per_head = fwd_flops(1, 1, N, d, True)
-    cores = oracle.max_threads()
-    heads, t_total = 0, 0.0
-    while heads < B * H:
-        b, h = divmod(heads, H)
-        t0 = time.perf_counter()
-        oracle.attention_forward(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1],
-                                 d ** -0.5, True)
-        t_total += time.perf_counter() - t0
-        heads += 1
-        if t_total >= target_s:
-            break
-    return heads, t_total, per_head * heads / t_total / 1e12, cores
+    ROWS = 256
+
+    def __init__(self):
+        import torch
+
+        import oracle
+        from exact_attention_11_gb300 import inputs
+        oracle.build()
+        self.oracle = oracle
+        B, H, N, d = FWD["B"], FWD["H"], FWD["N"], FWD["d"]
+        q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=FWD["seed"])
+        self.q, self.k, self.v = (t.double().reshape(B * H, N, d).numpy() for t in (q, k, v))
+        self.N, self.d, self.BH = N, d, B * H
+        self.units = [(h, r0) for r0 in range(0, N, self.ROWS) for h in range(B * H)]
+        self.next = 0
+        self.cores = oracle.max_threads()
+
+    def unit_flops(self, r0):
+        r1 = min(self.N, r0 + self.ROWS)
+        # causal: row i sees i + 1 keys; QK^T and PV cost 2 * (i + 1) * d each
+        return 4.0 * self.d * sum(i + 1 for i in range(r0, r1))
+
+    def run(self, budget_s):
+        flops, secs, n = 0.0, 0.0, 0
+        while n == 0 or secs < budget_s:
+            h, r0 = self.units[self.next % len(self.units)]
+            self.next += 1
+            rows = list(range(r0, min(self.N, r0 + self.ROWS)))
+            sl = slice(h, h + 1)
+            t0 = time.perf_counter()
+            self.oracle.attention_forward_rows(self.q[sl][None], self.k[sl][None],
+                                               self.v[sl][None], rows, self.d ** -0.5, True)
+            secs += time.perf_counter() - t0
+            flops += self.unit_flops(r0)
+            n += 1
+        return flops, secs, n
 
 
 def cpu_baseline(target_s: float):
-    heads, secs, tflops, cores = _oracle_sample(target_s)
-    return {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{heads} of the 32 causal heads (N=4096, d=128) of the forward workload, "
-                      f"float64, {secs:.1f} s"}
+    smp = OracleSampler()
+    flops, secs, n = smp.run(target_s)
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": smp.cores, "kind": "oracle",
+            "sample": f"{n} blocks of 256 causal query rows (of the 512 blocks of the "
+                      f"2x16x4096x128 forward), float64, {secs:.1f} s"}
 
 
 def reference_arm(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return None
-    per_step = []
+    smp = OracleSampler()
+    # Each step is a bounded sample, sized so the whole run stays near 150 s.
+    budget = max(0.02, min(0.5, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        _oracle_sample(0.0)
-    vals, heads_tot, secs_tot, cores = [], 0, 0.0, 1
+        smp.run(budget)
+    flops, secs, units = 0.0, 0.0, 0
     for _ in range(args.steps):
-        heads, secs, tflops, cores = _oracle_sample(args.ref_step_seconds)
-        vals.append(tflops)
-        heads_tot += heads
-        secs_tot += secs
-        per_step.append(secs)
-    value = fwd_flops(1, 1, FWD["N"], FWD["d"], True) * heads_tot / secs_tot / 1e12
+        f, s_, n = smp.run(budget)
+        flops, secs, units = flops + f, secs + s_, units + n
+    value = flops / secs / 1e12
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -434,16 +451,17 @@ def reference_arm(args):
         "n_gpus": ws,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": 1e3 * secs_tot / args.steps,
+        "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) inputs; no dataset)",
-        "config": {"workload": "fa_forward bf16 B=2 H=16 N=4096 d=128 causal (oracle: whole "
-                               "causal heads per step)"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{heads_tot} causal heads over {args.steps} steps"},
+        "config": {"workload": "fa_forward bf16 B=2 H=16 N=4096 d=128 causal (oracle: blocks "
+                               "of 256 query rows per step)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": smp.cores, "kind": "oracle",
+                         "sample": f"{units} blocks of 256 causal query rows over "
+                                   f"{args.steps} steps, float64"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -458,7 +476,6 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="approximate CPU time for the oracle baseline sample")
-    ap.add_argument("--ref-step-seconds", type=float, default=0.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":

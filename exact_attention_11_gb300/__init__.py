@@ -52,6 +52,7 @@ EXPORTS = {
     "fa_status_string": ([_i], ctypes.c_char_p),
     "fa_device_status": ([], _i),
     "fa_release": ([], None),
+    "fa_debug_inject_fault": ([_i], _i),
     "fa_version": ([], _i),
 }
 
@@ -127,6 +128,12 @@ def fa_device_status() -> int:
 
 def fa_release() -> None:
     load().fa_release()
+
+
+def fa_debug_inject_fault(mode: int) -> int:
+    """Test hook: arm (1) or disarm (0) a lost-copy fault in the next forward
+    launch on the current device (see fattn.h)."""
+    return _check("fa_debug_inject_fault", load().fa_debug_inject_fault(mode))
 
 
 # ---------------------------------------------------------------- torch helpers

@@ -27,6 +27,7 @@ struct DeviceState {
   size_t decode_counter_count = 0;
   int *fwd_sched = nullptr;       // kFwdSchedSlots pairs of forward work counters, kept at zero
   unsigned fwd_sched_next = 0;    // slot for the next forward launch
+  int inject_fault = 0;           // fa_debug_inject_fault: armed for the next forward
   int checked = 0;                // 1: sm_103 verified, -1: unsupported
 };
 
@@ -138,7 +139,7 @@ int fa_forward(const void *q, const void *k, const void *v, void *o, float *lse,
   if (rc != FA_OK) return rc;
   const int BH = B * H;
   if (BH == 0 || N == 0) return FA_OK;
-  int dev = 0;
+  int dev = 0, fault_cta = -1;
   int *sched = nullptr;
   CUtensorMap tq, tk, tv;
   {
@@ -147,12 +148,15 @@ int fa_forward(const void *q, const void *k, const void *v, void *o, float *lse,
     if ((rc = get_encoder()) != FA_OK) return rc;
     DeviceState &st = g_dev[dev];
     sched = st.fwd_sched + 2 * (st.fwd_sched_next++ % fattn::kFwdSchedSlots);
+    fault_cta = st.inject_fault ? 0 : -1;
+    st.inject_fault = 0;
   }
   if ((rc = encode_qkv_map(&tq, q, BH, N, d)) != FA_OK) return rc;
   if ((rc = encode_qkv_map(&tk, k, BH, N, d)) != FA_OK) return rc;
   if ((rc = encode_qkv_map(&tv, v, BH, N, d)) != FA_OK) return rc;
   return cuda_status(launch_fwd_bf16(tq, tk, tv, o, lse, BH, N, d, scale, causal ? 1 : 0, sched,
-                                     g_dev[dev].status, reinterpret_cast<cudaStream_t>(stream)));
+                                     g_dev[dev].status, fault_cta,
+                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int fa_forward_fp32(const float *q, const float *k, const float *v, float *o, float *lse, int B,
@@ -231,6 +235,15 @@ int fa_device_status(void) {
     return FA_ERR_CUDA;
   if (h != 0 && cudaMemset(g_dev[dev].status, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
   return h;
+}
+
+int fa_debug_inject_fault(int mode) {
+  if (mode != 0 && mode != 1) return FA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0, rc;
+  if ((rc = current_device(&dev)) != FA_OK) return rc;
+  g_dev[dev].inject_fault = mode;
+  return FA_OK;
 }
 
 void fa_release(void) {

@@ -139,7 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ o,
                        float *__restrict__ lse, int N, int BH, int n_qblocks, float scale_log2,
-                       int causal, int *__restrict__ sched, int *__restrict__ dev_status) {
+                       int causal, int *__restrict__ sched, int *__restrict__ dev_status,
+                       int fault_cta) {
   using C = Cfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int it = 0, kv = 0, nk = 0, nv = 0;
+      int it = 0, kv = 0, nk = 0, nv = 0, nq = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
         // Claim the next item and publish it to the other roles.
@@ -229,6 +230,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(s_base + C::kQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, b * 64,
                         q0 + t * BM, bh, bar(kBarQFull));
+        ++nq;
+        if (static_cast<int>(blockIdx.x) == fault_cta) {
+          // Failure-path test: stop here, as if the key-tile copies were lost;
+          // the MMA warp's bounded wait for them runs out.
+          ok = false;
+          break;
+        }
         for (int j = 0; j < n_b; ++j, ++kv) {
           const int st = kv % S;
           const uint32_t ph = (kv / S) & 1;
@@ -249,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         // Let the copies in flight land before the CTA exits.
-        if (it > 0) drain_wait(bar(kBarQFull), (it - 1) & 1);
+        if (nq > 0) drain_wait(bar(kBarQFull), (nq - 1) & 1);
         for (int i = (nk > S ? nk - S : 0); i < nk; ++i)
           drain_wait(bar(kBarKFull + i % S), (i / S) & 1);
         for (int i = (nv > S ? nv - S : 0); i < nv; ++i)
@@ -505,7 +513,7 @@ int g_num_sms[64] = {};
 template <int D>
 cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, void *o,
                      float *lse, int BH, int N, float scale, int causal, int *sched,
-                     int *dev_status, cudaStream_t stream) {
+                     int *dev_status, int fault_cta, cudaStream_t stream) {
   using C = Cfg<D>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -526,7 +534,7 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
   const float scale_log2 = scale * 1.4426950408889634f;
   fwd_bf16_tc_kernel<D><<<grid, kThreads, C::kAlloc, stream>>>(
       tq, tk, tv, reinterpret_cast<__nv_bfloat16 *>(o), lse, N, BH, n_qblocks, scale_log2, causal,
-      sched, dev_status);
+      sched, dev_status, fault_cta);
   return cudaGetLastError();
 }
 
@@ -534,10 +542,12 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
 
 cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             void *o, float *lse, int BH, int N, int d, float scale, int causal,
-                            int *sched, int *dev_status, cudaStream_t stream) {
+                            int *sched, int *dev_status, int fault_cta, cudaStream_t stream) {
   if (d == 64)
-    return launch_d<64>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status, stream);
-  return launch_d<128>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status, stream);
+    return launch_d<64>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status, fault_cta,
+                        stream);
+  return launch_d<128>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status, fault_cta,
+                       stream);
 }
 
 }  // namespace fattn

@@ -21,9 +21,11 @@ cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float
 // kernel leaves them zero.  Launches that may run at the same time need
 // different `sched` slots.
 constexpr int kFwdSchedSlots = 64;
+// fault_cta >= 0 makes that CTA's producer stop after its first Q loads (the
+// failure-path test); -1 in normal use.
 cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             void *o, float *lse, int BH, int N, int d, float scale, int causal,
-                            int *sched, int *dev_status, cudaStream_t stream);
+                            int *sched, int *dev_status, int fault_cta, cudaStream_t stream);
 
 int decode_max_parts(int max_num_blocks_per_seq);
 // Split-K workspace: per (sequence, head, partition) an unnormalised output

@@ -152,6 +152,20 @@ int fa_paged_decode_noalloc(const void *q, const void *k_cache, const void *v_ca
                             int num_seqs, int num_heads, int head_size, int block_size,
                             int max_num_blocks_per_seq, float scale, fa_stream_t stream);
 
+/*
+ * fa_debug_inject_fault -- test hook for the device-side failure path.
+ *
+ * mode 1 arms the current device: the next fa_forward launched on it makes
+ * its first CTA's TMA producer stop after loading that CTA's first query
+ * tiles, as if a copy had been lost.  The MMA warp's bounded wait for the
+ * missing key tile then runs out (after about 2 s), the CTA unwinds (in-flight
+ * copies and MMAs drained, tensor memory freed) and fa_device_status()
+ * returns FA_ERR_TIMEOUT.  That launch's output is incomplete; the CUDA
+ * context and the library stay usable.  mode 0 disarms.  Returns FA_OK, or
+ * FA_ERR_INVALID_ARG for another mode, or FA_ERR_NO_DEVICE.
+ */
+int fa_debug_inject_fault(int mode);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *fa_status_string(int status);
 

@@ -1,0 +1,47 @@
+"""Device-side failure detection without a GPU fault.
+
+fa_debug_inject_fault(1) makes one CTA of the next forward lose its key-tile
+copies (its producer stops after the query tiles).  The MMA warp's bounded
+wait for them runs out after about 2 s, the CTA unwinds, and the host reads
+FA_ERR_TIMEOUT from fa_device_status().  Nothing traps, faults or hangs: the
+context stays usable and the next forward is correct.
+"""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import exact_attention_11_gb300 as fa
+from exact_attention_11_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def test_lost_copy_times_out_and_context_survives():
+    dev = torch.device("cuda:0")
+    q, k, v = inputs.forward_inputs(1, 4, 640, 128, torch.bfloat16, seed=31)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    assert fa.fa_device_status() == 0
+    fa.fa_debug_inject_fault(1)
+    t0 = time.perf_counter()
+    fa.forward(qd, kd, vd, causal=True)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert fa.fa_device_status() == -5          # FA_ERR_TIMEOUT, reported once
+    assert fa.fa_device_status() == 0
+    assert 1.0 < waited < 30.0                  # the 2 s limit ran out, nothing hung
+    # The armed fault was consumed: the next call is clean and correct.
+    o, lse = fa.forward(qd, kd, vd, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    ro, rl = oracle.attention_forward(q, k, v, 128 ** -0.5, True)
+    assert np.abs(o.float().cpu().numpy() - ro).max() <= 2e-2
+    assert np.abs(lse.cpu().numpy() - rl).max() <= 1e-2
+
+
+def test_inject_rejects_unknown_mode():
+    with pytest.raises(fa.FattnError):
+        fa.fa_debug_inject_fault(7)
+    fa.fa_debug_inject_fault(0)
