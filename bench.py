@@ -78,6 +78,24 @@ def recorded_traffic(kernel: str):
     return rec["dram_read_bytes"] + rec["dram_write_bytes"]
 
 
+def reduce_over_ranks(times, status, device):
+    """The job's figures across ranks: every time is the slowest rank's (max)
+    and the status is the worst one (min: error codes are negative)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(times), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    st = torch.tensor([int(status)], device=device, dtype=torch.int32)
+    dist.all_reduce(st, op=dist.ReduceOp.MIN)
+    return t.tolist(), int(st.item())
+
+
+def weak_scaling_rate(units_per_rank, world_size, max_ms, unit_scale):
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (each rank runs its own replica of the workload)."""
+    return world_size * units_per_rank / (max_ms * 1e-3) / unit_scale
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -298,18 +316,13 @@ def gpu_arm(args):
     d2h = o.numel() * 2 + lse.numel() * 4 + out.numel() * 2
 
     if ws > 1:
-        t = torch.tensor([fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms], device=dev,
-                         dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms = t.tolist()
-        st = torch.tensor([status], device=dev, dtype=torch.int32)
-        dist.all_reduce(st, op=dist.ReduceOp.MIN)
-        status = int(st.item())
+        (fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms), status = reduce_over_ranks(
+            [fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms], status, dev)
 
-    tflops = ws * flops / (fwd_ms * 1e-3) / 1e12
-    per_gpu_tflops = flops / (fwd_ms * 1e-3) / 1e12
-    gbs = ws * dec_bytes / (dec_ms * 1e-3) / 1e9
-    per_gpu_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    tflops = weak_scaling_rate(flops, ws, fwd_ms, 1e12)
+    per_gpu_tflops = weak_scaling_rate(flops, 1, fwd_ms, 1e12)
+    gbs = weak_scaling_rate(dec_bytes, ws, dec_ms, 1e9)
+    per_gpu_gbs = weak_scaling_rate(dec_bytes, 1, dec_ms, 1e9)
     peak_t = peaks["bf16_tflops"]
     peak_h = peaks["hbm_gbs"]
     result = {
@@ -339,7 +352,7 @@ def gpu_arm(args):
         "fwd_long": {
             "workload": "fa_forward bf16 B=1 H=8 N=16384 d=128 causal, inputs N(0,1)*0.5",
             "ms": round(long_ms, 4),
-            "value": round(ws * fwd_flops(**FWD_LONG) / (long_ms * 1e-3) / 1e12, 2),
+            "value": round(weak_scaling_rate(fwd_flops(**FWD_LONG), ws, long_ms, 1e12), 2),
             "unit": "TFLOP/s",
             "frac_of_bf16_peak": round(fwd_flops(**FWD_LONG) / (long_ms * 1e-3) / 1e12
                                        / peaks["bf16_tflops"], 4),
@@ -358,8 +371,8 @@ def gpu_arm(args):
                      "traffic": recorded_traffic("fwd_bf16_tc_kernel<128>"),
                      "peak_kind": f"{peak_kind} bf16 burst",
                      "kernel": "fwd_bf16_tc_kernel<128>", "flops_per_launch": flops},
-        "e2e": {"value": round(ws * flops / (e2e_fwd_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "decode_gbs": round(ws * dec_bytes / (e2e_dec_ms * 1e-3) / 1e9, 1),
+        "e2e": {"value": round(weak_scaling_rate(flops, ws, e2e_fwd_ms, 1e12), 2), "unit": "TFLOP/s",
+                "decode_gbs": round(weak_scaling_rate(dec_bytes, ws, e2e_dec_ms, 1e9), 1),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "KV cache resident (serving state); q, K, V, q_decode, block table, "
                         "context lens copied in and O, LSE, out copied back every step"},
