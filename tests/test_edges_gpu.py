@@ -1,0 +1,103 @@
+"""Edge cases of the CUDA path against the float64 oracle: writes stay inside
+the outputs, concurrent calls on two streams, many small work items, long
+non-causal rows, and decode shapes with ragged block tables."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import exact_attention_11_gb300 as fa
+from exact_attention_11_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+TOL_O, TOL_L = 2e-2, 1e-2
+
+
+def _ref(q, k, v, causal, rows=None):
+    d = q.shape[-1]
+    if rows is None:
+        return oracle.attention_forward(q, k, v, d ** -0.5, causal)
+    return oracle.attention_forward_rows(q, k, v, rows, d ** -0.5, causal)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("N,d,causal", [(333, 128, True), (97, 64, False), (1, 128, True)])
+def test_outputs_do_not_spill_past_their_end(dtype, N, d, causal):
+    B, H = 1, 3
+    q, k, v = inputs.forward_inputs(B, H, N, d, dtype, seed=N)
+    guard = 4096
+    o_buf = torch.full((B * H * N * d + guard,), 7.0, dtype=dtype, device=DEV)
+    l_buf = torch.full((B * H * N + guard,), 7.0, dtype=torch.float32, device=DEV)
+    o = o_buf[:B * H * N * d].view(B, H, N, d)
+    lse = l_buf[:B * H * N].view(B, H, N)
+    fa.forward(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert (o_buf[B * H * N * d:] == 7.0).all()
+    assert (l_buf[B * H * N:] == 7.0).all()
+    ro, rl = _ref(q, k, v, causal)
+    tol = (TOL_O, TOL_L) if dtype == torch.bfloat16 else (1e-5, 1e-5)
+    assert np.abs(o.float().cpu().numpy() - ro).max() <= tol[0]
+    assert np.abs(lse.cpu().numpy() - rl).max() <= tol[1]
+
+
+def test_two_streams_at_once():
+    """Two forwards in flight together on different streams (separate work
+    counters) both match the oracle."""
+    qa, ka, va = (t.to(DEV) for t in inputs.forward_inputs(2, 8, 1536, 128, torch.bfloat16, seed=41))
+    qb, kb, vb = (t.to(DEV) for t in inputs.forward_inputs(1, 16, 1024, 64, torch.bfloat16, seed=42))
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        with torch.cuda.stream(sa):
+            oa, la = fa.forward(qa, ka, va, causal=True)
+        with torch.cuda.stream(sb):
+            ob, lb = fa.forward(qb, kb, vb, causal=False)
+    torch.cuda.synchronize()
+    rows = [0, 511, 1024, 1535]
+    ro, rl = _ref(qa.cpu(), ka.cpu(), va.cpu(), True, rows)
+    assert np.abs(oa[:, :, rows].float().cpu().numpy() - ro).max() <= TOL_O
+    assert np.abs(la[:, :, rows].cpu().numpy() - rl).max() <= TOL_L
+    ro, rl = _ref(qb.cpu(), kb.cpu(), vb.cpu(), False)
+    assert np.abs(ob.float().cpu().numpy() - ro).max() <= TOL_O
+    assert np.abs(lb.cpu().numpy() - rl).max() <= TOL_L
+    assert fa.fa_device_status() == 0
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", [
+    (8, 64, 256, 64, True),      # 512 small items: more items than SMs, several rounds
+    (3, 5, 2300, 128, False),    # long non-causal rows with a ragged tail
+    (1, 2, 2048, 64, True),      # d = 64 with many key tiles
+])
+def test_more_forward_shapes(B, H, N, d, causal):
+    q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=B * H + N)
+    o, lse = fa.forward(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal)
+    torch.cuda.synchronize()
+    rows = sorted(set(inputs.sample_rows(N, 64, seed=N).tolist()) | {0, N - 1})
+    ro, rl = _ref(q, k, v, causal, rows)
+    assert np.abs(o[:, :, rows].float().cpu().numpy() - ro).max() <= TOL_O
+    assert np.abs(lse[:, :, rows].cpu().numpy() - rl).max() <= TOL_L
+
+
+def test_fp32_longer_causal():
+    q, k, v = inputs.forward_inputs(1, 2, 2048, 128, torch.float32, seed=77)
+    o, lse = fa.forward(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
+    torch.cuda.synchronize()
+    rows = [0, 1, 700, 2047]
+    ro, rl = _ref(q, k, v, True, rows)
+    assert np.abs(o[:, :, rows].cpu().numpy() - ro).max() <= 1e-5
+    assert np.abs(lse[:, :, rows].cpu().numpy() - rl).max() <= 1e-5
+
+
+@pytest.mark.parametrize("S,H,max_ctx,ctx", [
+    (3, 1, 1000, [1000, 999, 17]),        # one head, 63-block tables
+    (4, 7, 33, [33, 32, 16, 1]),          # tables of 3 blocks
+    (2, 2, 5000, [5000, 4097]),           # more partitions than the benchmark workload
+])
+def test_decode_shapes(S, H, max_ctx, ctx):
+    di = inputs.decode_inputs(S, H, 128, 16, max_ctx, seed=S * H, device=DEV)
+    di.context_lens.copy_(torch.tensor(ctx, dtype=torch.int32, device=DEV))
+    out = fa.paged_decode(di.q, di.k_cache, di.v_cache, di.block_tables, di.context_lens, di.scale)
+    torch.cuda.synchronize()
+    ro, _ = oracle.paged_decode(di.q, di.k_cache, di.v_cache, di.block_tables, di.context_lens,
+                                di.scale)
+    assert np.abs(out.float().cpu().numpy() - ro).max() <= TOL_O
