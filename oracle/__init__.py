@@ -62,9 +62,11 @@ def _bind(lib):
                                      ctypes.c_double, ctypes.c_int, _dp]
     lib.oracle_paged_decode.argtypes = [_dp, _dp, _dp, _ip, _ip, _dp, _dp] + [
         ctypes.c_long] * 7 + [ctypes.c_double, ctypes.c_int]
+    lib.oracle_backward.argtypes = [_dp] * 7 + [ctypes.c_long] * 4 + [ctypes.c_double, ctypes.c_int,
+                                                                     ctypes.c_int]
     lib.oracle_max_threads.argtypes = []
     for f in (lib.oracle_forward, lib.oracle_forward_rows, lib.oracle_probs_row,
-              lib.oracle_paged_decode, lib.oracle_max_threads):
+              lib.oracle_paged_decode, lib.oracle_backward, lib.oracle_max_threads):
         f.restype = ctypes.c_int
     return lib
 
@@ -179,6 +181,22 @@ def probs_row(q, k, i: int, scale: float, causal: bool):
     if rc != 0:
         raise ValueError("oracle_probs_row rejected its arguments")
     return p
+
+
+def attention_backward(q, k, v, dout, scale: float, causal: bool, nthreads: int = 0):
+    """Gradients (dQ, dK, dV), each [B,H,N,d], of the loss whose gradient with
+    respect to the attention output is ``dout``."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    if q.ndim != 4 or not (k.shape == v.shape == dout.shape == q.shape):
+        raise ValueError("q, k, v, dout must share one [B,H,N,d] shape")
+    B, H, N, d = q.shape
+    dq, dk, dv = np.zeros(q.shape), np.zeros(q.shape), np.zeros(q.shape)
+    rc = _load().oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                                 int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_backward rejected its arguments")
+    return dq, dk, dv
 
 
 def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,

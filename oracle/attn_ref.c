@@ -233,3 +233,88 @@ int oracle_paged_decode(const double *q, const double *k_cache, const double *v_
     }
     return failed ? -1 : 0;
 }
+
+/* Backward pass of the same attention: given dO = dLoss/dO, the gradients
+ * of the loss with respect to Q, K and V, obtained by differentiating the
+ * forward definition above ("FlashAttention: GPU 메모리 계층을 활용한 어텐션
+ * 최적화 분석", youngju.dev, section 7 describes the backward as recomputing
+ * S and P from Q, K and the saved row statistics; the gradient formulas are
+ * the chain rule through O = P V, P = softmax(S), S = scale * Q K^T):
+ *
+ *     dV_j  = sum_i P_ij dO_i
+ *     dP_ij = dO_i . V_j
+ *     D_i   = sum_j P_ij dP_ij
+ *     dS_ij = P_ij (dP_ij - D_i)
+ *     dQ_i  = scale * sum_j dS_ij K_j
+ *     dK_j  = scale * sum_i dS_ij Q_i
+ *
+ * over visible pairs only (causal: j <= i).  Each row's P is materialised
+ * from scratch exactly as in the forward.  Heads are independent and run in
+ * parallel; inside a head the rows are visited in order, so the sums into
+ * dK and dV have a fixed order.  All of dq, dk, dv are [B,H,N,d] and are
+ * overwritten.  Returns 0, or -1 on a bad argument / allocation failure. */
+int oracle_backward(const double *q, const double *k, const double *v, const double *dout,
+                    double *dq, double *dk, double *dv, long B, long H, long N, long d,
+                    double scale, int causal, int nthreads)
+{
+    if (B < 0 || H < 0 || N < 0 || d <= 0) return -1;
+    if (N == 0) return 0;
+    set_threads(nthreads);
+    const long BH = B * H;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)N);
+        double *dp = (double *)malloc(sizeof(double) * (size_t)N);
+        if (!p || !dp) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (long bh = 0; bh < BH; ++bh) {
+                const long base = bh * N * d;
+                const double *qh = q + base, *kh = k + base, *vh = v + base, *doh = dout + base;
+                double *dqh = dq + base, *dkh = dk + base, *dvh = dv + base;
+                for (long x = 0; x < N * d; ++x) dqh[x] = dkh[x] = dvh[x] = 0.0;
+                for (long i = 0; i < N; ++i) {
+                    const long n_keys = causal ? i + 1 : N;
+                    const double *qi = qh + i * d, *doi = doh + i * d;
+                    /* P row (safe softmax of the scaled scores). */
+                    double m = -INFINITY;
+                    for (long j = 0; j < n_keys; ++j) {
+                        double acc = 0.0;
+                        for (long c = 0; c < d; ++c) acc += qi[c] * kh[j * d + c];
+                        p[j] = scale * acc;
+                        if (p[j] > m) m = p[j];
+                    }
+                    double l = 0.0;
+                    for (long j = 0; j < n_keys; ++j) {
+                        p[j] = exp(p[j] - m);
+                        l += p[j];
+                    }
+                    for (long j = 0; j < n_keys; ++j) p[j] /= l;
+                    /* dP row and D_i. */
+                    double D = 0.0;
+                    for (long j = 0; j < n_keys; ++j) {
+                        double acc = 0.0;
+                        for (long c = 0; c < d; ++c) acc += doi[c] * vh[j * d + c];
+                        dp[j] = acc;
+                        D += p[j] * acc;
+                    }
+                    /* Accumulate the three gradients. */
+                    for (long j = 0; j < n_keys; ++j) {
+                        const double ds = p[j] * (dp[j] - D);
+                        for (long c = 0; c < d; ++c) {
+                            dqh[i * d + c] += scale * ds * kh[j * d + c];
+                            dkh[j * d + c] += scale * ds * qi[c];
+                            dvh[j * d + c] += p[j] * doi[c];
+                        }
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+    return failed ? -1 : 0;
+}

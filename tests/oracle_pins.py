@@ -310,3 +310,81 @@ ALL_CHECKS = [check_hand_examples, check_brute_force_tiny, check_library_sdpa,
               check_invariants, check_large_logits, check_online_recurrence,
               check_layout_fixture, check_decode_matches_gathered_forward,
               check_decode_one_hot]
+
+
+# --------------------------------------------------------------------------
+# Backward
+
+def check_backward_hand_example():
+    """Hand-derived gradients (tests/golden/hand_examples.json)."""
+    with open(os.path.join(GOLDEN, "hand_examples.json")) as f:
+        fx = json.load(f)
+    for ex in fx["backward_examples"]:
+        arr = lambda key: np.array([[_expr(c) for c in r] for r in ex[key]])[None, None]
+        dq, dk, dv = oracle.attention_backward(arr("q"), arr("k"), arr("v"), arr("dout"),
+                                               ex["scale"], False)
+        for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+            want = np.array([[_expr(c) for c in r] for r in ex["noncausal"][name]])
+            np.testing.assert_allclose(got[0, 0], want, rtol=0, atol=1e-13,
+                                       err_msg=f"{ex['name']} {name}")
+
+
+def check_backward_finite_differences():
+    """Central differences of L = sum(O * dO), O from the forward oracle,
+    agree with the backward oracle on small heads."""
+    r = _rng(17)
+    for causal in (False, True):
+        N, d, scale = 5, 3, 0.6
+        q, k, v, do = (r.standard_normal((1, 1, N, d)) for _ in range(4))
+        dq, dk, dv = oracle.attention_backward(q, k, v, do, scale, causal)
+        h = 1e-6
+        for x, g in ((q, dq), (k, dk), (v, dv)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(*x.shape):
+                old = x[idx]
+                x[idx] = old + h
+                lp = (oracle.attention_forward(q, k, v, scale, causal)[0] * do).sum()
+                x[idx] = old - h
+                lm = (oracle.attention_forward(q, k, v, scale, causal)[0] * do).sum()
+                x[idx] = old
+                num[idx] = (lp - lm) / (2 * h)
+            np.testing.assert_allclose(g, num, rtol=0, atol=1e-7)
+
+
+def check_backward_library_autograd():
+    """PyTorch autograd through float64 scaled_dot_product_attention."""
+    F = torch.nn.functional
+    g = torch.Generator().manual_seed(23)
+    for (B, H, N, d, causal) in ((1, 2, 37, 16, True), (2, 1, 50, 8, False)):
+        q, k, v, do = (torch.randn(B, H, N, d, generator=g, dtype=torch.float64) for _ in range(4))
+        scale = d ** -0.5
+        qq, kk, vv = (t.clone().requires_grad_(True) for t in (q, k, v))
+        o = F.scaled_dot_product_attention(qq, kk, vv, is_causal=causal, scale=scale)
+        o.backward(do)
+        dq, dk, dv = oracle.attention_backward(q, k, v, do, scale, causal)
+        for got, ref in ((dq, qq.grad), (dk, kk.grad), (dv, vv.grad)):
+            np.testing.assert_allclose(got, ref.numpy(), rtol=0, atol=1e-11)
+
+
+def check_backward_invariants():
+    """Rows of P sum to one and each row of dS sums to zero, so the key
+    gradients sum to zero and the value gradients sum to the output
+    gradients; identical value rows make dQ and dK vanish; causal row 0 has
+    one key, so dQ_0 = 0."""
+    r = _rng(29)
+    N, d = 33, 6
+    q, k, v, do = (r.standard_normal((1, 1, N, d)) for _ in range(4))
+    for causal in (False, True):
+        dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.5, causal)
+        np.testing.assert_allclose(dk[0, 0].sum(axis=0), np.zeros(d), atol=1e-12)
+        np.testing.assert_allclose(dv[0, 0].sum(axis=0), do[0, 0].sum(axis=0), atol=1e-12)
+        if causal:
+            np.testing.assert_allclose(dq[0, 0, 0], np.zeros(d), atol=1e-15)
+    same = np.broadcast_to(r.standard_normal(d), (1, 1, N, d)).copy()
+    dq, dk, dv = oracle.attention_backward(q, k, same, do, 0.5, True)
+    np.testing.assert_allclose(dq, 0, atol=1e-12)
+    np.testing.assert_allclose(dk, 0, atol=1e-12)
+
+
+ALL_CHECKS += [check_backward_hand_example, check_backward_finite_differences,
+               check_backward_library_autograd, check_backward_invariants]

@@ -31,6 +31,18 @@ MUTANTS = [
      "V[tok * D + c] = vb[off * D + c];"),
     ("block_table_index_mod", "block_tables[s * max_blocks + tok / block_size]",
      "block_tables[s * max_blocks + tok % block_size]"),
+    ("bwd_D_sign", "const double ds = p[j] * (dp[j] - D);", "const double ds = p[j] * (dp[j] + D);"),
+    ("bwd_dq_no_scale", "dqh[i * d + c] += scale * ds * kh[j * d + c];",
+     "dqh[i * d + c] += ds * kh[j * d + c];"),
+    ("bwd_dk_uses_k", "dkh[j * d + c] += scale * ds * qi[c];",
+     "dkh[j * d + c] += scale * ds * kh[j * d + c];"),
+    ("bwd_dv_without_p", "dvh[j * d + c] += p[j] * doi[c];", "dvh[j * d + c] += doi[c];"),
+    ("bwd_dp_uses_k", "for (long c = 0; c < d; ++c) acc += doi[c] * vh[j * d + c];",
+     "for (long c = 0; c < d; ++c) acc += doi[c] * kh[j * d + c];"),
+    ("bwd_unnormalised_p", "for (long j = 0; j < n_keys; ++j) p[j] /= l;",
+     "for (long j = 0; j < n_keys; ++j) p[j] /= 1.0;"),
+    ("bwd_causal_off_by_one", "const long n_keys = causal ? i + 1 : N;\n                    const double *qi",
+     "const long n_keys = causal ? i : N;\n                    const double *qi"),
 ]
 
 
