@@ -1,10 +1,10 @@
-"""Python binding of libfattn: exact attention forward and paged decode on GB300.
+"""Python binding of libfattn: exact attention forward, backward and paged decode on GB300.
 
 The C ABI (``include/fattn.h``) is reached through ctypes.  The functions
-``fa_forward``, ``fa_forward_fp32`` and ``fa_paged_decode`` take the same
+``fa_forward``, ``fa_forward_fp32``, ``fa_backward`` and ``fa_paged_decode`` take the same
 arguments as their C counterparts (device pointers as ints, sizes, a stream
 handle) and only marshal them; every step of the computation runs in the CUDA
-kernels of ``libfattn.so``.  ``forward`` and ``paged_decode`` are torch
+kernels of ``libfattn.so``.  ``forward``, ``backward`` and ``paged_decode`` are torch
 conveniences that allocate the outputs and pass the tensors' device pointers.
 
 There is no fallback: if ``libfattn.so`` is missing, cannot be loaded, or the
@@ -17,7 +17,7 @@ import os
 import threading
 
 __all__ = ["fa_forward", "fa_forward_fp32", "fa_paged_decode", "fa_paged_decode_noalloc",
-           "fa_status_string",
+           "fa_backward", "fa_backward_workspace_bytes", "backward", "fa_status_string",
            "fa_device_status", "fa_release", "forward", "paged_decode", "FattnError",
            "library_path", "load"]
 
@@ -49,6 +49,9 @@ EXPORTS = {
     "fa_forward_fp32": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_paged_decode": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_paged_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_backward_workspace_bytes": ([_i, _i, _i, _i], ctypes.c_ulonglong),
+    "fa_backward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp,
+                     ctypes.c_ulonglong, _vp], _i),
     "fa_status_string": ([_i], ctypes.c_char_p),
     "fa_device_status": ([], _i),
     "fa_release": ([], None),
@@ -115,6 +118,17 @@ def fa_paged_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, out
         block_size, max_num_blocks_per_seq, scale, stream))
 
 
+def fa_backward_workspace_bytes(B, H, N, d) -> int:
+    return int(load().fa_backward_workspace_bytes(B, H, N, d))
+
+
+def fa_backward(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+                workspace_bytes, stream) -> int:
+    return _check("fa_backward", load().fa_backward(
+        q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, int(causal), workspace,
+        workspace_bytes, stream))
+
+
 def fa_status_string(status: int) -> str:
     try:
         return load().fa_status_string(status).decode()
@@ -169,6 +183,36 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, want_lse=True
     fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, float(scale), bool(causal),
        _stream(q))
     return out, lse
+
+
+def backward(q, k, v, o, lse, dout, scale=None, causal=False, workspace=None):
+    """Gradients (dQ, dK, dV) of the bf16 forward on [B,H,N,d] CUDA tensors.
+
+    ``o`` and ``lse`` are what ``forward`` returned for the same q, k, v,
+    scale and causal.  ``workspace`` (optional) is a CUDA tensor of at least
+    ``fa_backward_workspace_bytes`` bytes; one is allocated when it is None.
+    Runs on the current torch stream."""
+    import torch
+    for t in (q, k, v, o, dout):
+        if t.dim() != 4 or t.shape != q.shape:
+            raise ValueError("q, k, v, o, dout must share one [B,H,N,d] shape")
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16):
+            raise ValueError("q, k, v, o, dout must be contiguous bf16 CUDA tensors")
+    B, H, N, d = q.shape
+    if lse is None or tuple(lse.shape) != (B, H, N) or lse.dtype != torch.float32 \
+            or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B,H,N] tensor")
+    if scale is None:
+        scale = d ** -0.5
+    nbytes = fa_backward_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                _ptr(dv), B, H, N, d, float(scale), bool(causal), _ptr(workspace), ws_bytes,
+                _stream(q))
+    return dq, dk, dv
 
 
 def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale=None, out=None):

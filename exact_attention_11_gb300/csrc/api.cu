@@ -175,6 +175,44 @@ int fa_forward_fp32(const float *q, const float *k, const float *v, float *o, fl
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
+unsigned long long fa_backward_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 0 || H < 0 || N < 0 || d < 0) return 0;
+  return static_cast<unsigned long long>(
+      fattn::bwd_workspace_bytes(static_cast<int>((long long)B * H), N, d));
+}
+
+int fa_backward(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                const float *lse, void *dq, void *dk, void *dv, int B, int H, int N, int d,
+                float scale, int causal, void *workspace, unsigned long long workspace_bytes,
+                fa_stream_t stream) {
+  if (!dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  int rc = check_forward_args(q, k, v, o, lse, B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_ALIGNMENT;
+  const int BH = B * H;
+  if (BH == 0 || N == 0) return FA_OK;
+  if (!workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
+  if (workspace_bytes < fattn::bwd_workspace_bytes(BH, N, d)) return FA_ERR_INVALID_ARG;
+  int dev = 0;
+  CUtensorMap tq, tk, tv, tdo;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if ((rc = current_device(&dev)) != FA_OK) return rc;
+    if ((rc = get_encoder()) != FA_OK) return rc;
+  }
+  if ((rc = encode_qkv_map(&tq, q, BH, N, d)) != FA_OK) return rc;
+  if ((rc = encode_qkv_map(&tk, k, BH, N, d)) != FA_OK) return rc;
+  if ((rc = encode_qkv_map(&tv, v, BH, N, d)) != FA_OK) return rc;
+  if ((rc = encode_qkv_map(&tdo, dout, BH, N, d)) != FA_OK) return rc;
+  return cuda_status(fattn::launch_bwd_bf16(tq, tk, tv, tdo, o, dout, lse, dq, dk, dv, BH, N, d,
+                                            scale, causal ? 1 : 0,
+                                            reinterpret_cast<float *>(workspace),
+                                            g_dev[dev].status,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fa_paged_decode(const void *q, const void *k_cache, const void *v_cache,
                     const int *block_tables, const int *context_lens, void *out, int num_seqs,
                     int num_heads, int head_size, int block_size, int max_num_blocks_per_seq,

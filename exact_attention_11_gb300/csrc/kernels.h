@@ -27,6 +27,15 @@ cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             void *o, float *lse, int BH, int N, int d, float scale, int causal,
                             int *sched, int *dev_status, int fault_cta, cudaStream_t stream);
 
+// Backward: workspace = fp32 dQ accumulator [B*H*N*d] + D [B*H*N] + LSE2 [B*H*N].
+// tdo is the tensor map of dO (same form as tq).
+size_t bwd_workspace_bytes(int BH, int N, int d);
+cudaError_t launch_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const CUtensorMap &tdo, const void *o, const void *dout,
+                            const float *lse, void *dq, void *dk, void *dv, int BH, int N, int d,
+                            float scale, int causal, float *ws, int *dev_status,
+                            cudaStream_t stream);
+
 int decode_max_parts(int max_num_blocks_per_seq);
 // Split-K workspace: per (sequence, head, partition) an unnormalised output
 // row and its (max, sum) pair, in fp32.  `counters` holds one int per

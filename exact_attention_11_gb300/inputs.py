@@ -40,6 +40,14 @@ def forward_inputs(B: int, H: int, N: int, d: int, dtype=torch.bfloat16, seed: i
     return tuple(out)
 
 
+def grad_output(B: int, H: int, N: int, d: int, dtype=torch.bfloat16, seed: int = 0,
+                device="cpu"):
+    """An upstream gradient dO of shape [B, H, N, d], iid N(0,1), rounded RNE
+    to ``dtype`` (drawn from its own seed stream, distinct from Q, K, V)."""
+    g = torch.Generator(device="cpu").manual_seed(seed + 0x5EED)
+    return _randn((B, H, N, d), g).to(dtype).to(device)
+
+
 def sample_rows(N: int, count: int, seed: int):
     """``count`` distinct query rows in [0, N), seeded, sorted ascending."""
     g = torch.Generator(device="cpu").manual_seed(seed)

@@ -85,6 +85,48 @@ int fa_forward_fp32(const float *q, const float *k, const float *v, float *o, fl
                     fa_stream_t stream);
 
 /*
+ * fa_backward_workspace_bytes -- size in bytes of the fp32 workspace that
+ * fa_backward needs for these sizes: 4 * B*H*N * (d + 2).  Returns 0 for
+ * negative sizes.
+ */
+unsigned long long fa_backward_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * fa_backward -- gradients of the bf16 exact-attention forward.
+ *
+ * For the forward O = softmax(scale * Q K^T [+ causal mask]) V of
+ * fa_forward and an upstream gradient dO, computes dQ, dK and dV by the
+ * recomputation scheme of section 7 of "FlashAttention: GPU 메모리 계층을
+ * 활용한 어텐션 최적화 분석" (youngju.dev): the probabilities are rebuilt
+ * tile by tile from Q, K and the forward's saved lse, P = exp(S - lse), and
+ * with D_i = sum_c dO[i,c] O[i,c]:
+ *     dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),
+ *     dQ = scale * dS K,  dK = scale * dS^T Q.
+ * No N x N matrix reaches device memory.
+ *
+ *   q, k, v, o, dout  bf16 [B, H, N, d], read only; o and lse are what
+ *                     fa_forward returned for these q, k, v, scale, causal.
+ *   lse               fp32 [B, H, N] natural-log LSE from fa_forward.
+ *   dq, dk, dv        bf16 [B, H, N, d], written.
+ *   workspace         device memory owned by the caller, at least
+ *                     fa_backward_workspace_bytes(B, H, N, d) bytes, 16-byte
+ *                     aligned; its contents on entry do not matter and are
+ *                     scratch afterwards.  Two calls whose work overlaps on
+ *                     the GPU need separate workspaces.
+ *   d, scale, causal  as for fa_forward.
+ * Products accumulate in fp32 on the tensor cores; P and dS are rounded to
+ * bf16 before they multiply dO, Q and K; dQ is summed over key blocks in
+ * fp32 with atomic adds, so its last bits may vary from run to run.
+ * FA_ERR_INVALID_ARG when workspace is NULL or smaller than needed; the
+ * other errors as for fa_forward.  B*H or N equal to 0 is a no-op.
+ */
+int fa_backward(const void *q, const void *k, const void *v, const void *o,
+                const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                int B, int H, int N, int d, float scale, int causal,
+                void *workspace, unsigned long long workspace_bytes,
+                fa_stream_t stream);
+
+/*
  * fa_paged_decode -- single-query attention over a paged KV cache.
  *
  * One query token per sequence attends to all context_lens[s] tokens of its

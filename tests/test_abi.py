@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("fa_forward", "fa_forward_fp32", "fa_paged_decode", "fa_status_string",
+    for n in ("fa_forward", "fa_forward_fp32", "fa_backward", "fa_paged_decode", "fa_status_string",
               "fa_device_status", "fa_release", "fa_version"):
         assert n in names
 
@@ -77,6 +77,36 @@ def test_decode_argument_checks(lib, args, expect):
     assert lib.fa_paged_decode(*args, None) == expect
 
 
+W = 1 << 20  # a workspace size larger than any case below needs
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((NULL, P, P, P, P, P, P, P, P, 1, 1, 64, 64, 0.125, 0, P, W), -1),     # null q
+    ((P, P, P, P, NULL, P, P, P, P, 1, 1, 64, 64, 0.125, 0, P, W), -1),     # null dout
+    ((P, P, P, P, P, NULL, P, P, P, 1, 1, 64, 64, 0.125, 0, P, W), -1),     # null lse
+    ((P, P, P, P, P, P, P, P, NULL, 1, 1, 64, 64, 0.125, 0, P, W), -1),     # null dv
+    ((P, P, P, P, P, P, P, P, P, 1, 1, 64, 96, 0.125, 0, P, W), -2),        # d not 64/128
+    ((P, P, P, P, P, P, P, P, P, 1, 1, 64, 64, -1.0, 0, P, W), -1),         # negative scale
+    ((P, P, P, P, P + 2, P, P, P, P, 1, 1, 64, 64, 0.125, 0, P, W), -3),    # misaligned dout
+    ((P, P, P, P, P, P, P + 8, P, P, 1, 1, 64, 64, 0.125, 0, P, W), -3),    # misaligned dq
+    ((P, P, P, P, P, P, P, P, P, 1, 1, 64, 64, 0.125, 0, NULL, W), -1),     # no workspace
+    ((P, P, P, P, P, P, P, P, P, 1, 1, 64, 64, 0.125, 0, P + 4, W), -3),    # misaligned workspace
+    ((P, P, P, P, P, P, P, P, P, 1, 1, 64, 64, 0.125, 0, P, 64 * 66 * 4 - 1), -1),  # one byte short
+    ((P, P, P, P, P, P, P, P, P, 0, 1, 64, 64, 0.125, 0, NULL, 0), 0),      # empty batch: no-op
+    ((P, P, P, P, P, P, P, P, P, 1, 1, 0, 64, 0.125, 0, NULL, 0), 0),       # N = 0: no-op
+])
+def test_backward_argument_checks(lib, args, expect):
+    assert lib.fa_backward(*args, None) == expect
+
+
+def test_backward_workspace_size(lib):
+    # fp32 dQ accumulator [B*H*N*d] plus D and LSE2 [B*H*N] each
+    assert lib.fa_backward_workspace_bytes(2, 3, 100, 128) == 4 * 2 * 3 * 100 * 130
+    assert lib.fa_backward_workspace_bytes(1, 1, 64, 64) == 64 * 66 * 4
+    assert lib.fa_backward_workspace_bytes(-1, 1, 64, 64) == 0
+    assert fa.fa_backward_workspace_bytes(0, 4, 64, 64) == 0
+
+
 def test_valid_call_without_gpu_fails_loudly(lib):
     import torch
     if torch.cuda.is_available():
@@ -85,6 +115,8 @@ def test_valid_call_without_gpu_fails_loudly(lib):
     assert rc == -7  # FA_ERR_NO_DEVICE: never a silent CPU path
     with pytest.raises(fa.FattnError):
         fa.fa_forward(P, P, P, P, None, 1, 1, 64, 64, 0.125, 0, None)
+    rc = lib.fa_backward(P, P, P, P, P, P, P, P, P, 1, 1, 64, 64, 0.125, 0, P, W, None)
+    assert rc == -7
 
 
 def test_missing_library_raises(monkeypatch, tmp_path):
