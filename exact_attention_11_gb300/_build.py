@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfattn.so")
 SOURCES = ["api.cu", "fwd_f32.cu", "fwd_bf16.cu", "decode.cu", "decode_noalloc.cu",
-           "bwd_bf16.cu"]
+           "bwd_bf16.cu", "bwd_bf16_d128.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
          "--expt-relaxed-constexpr"]
@@ -49,7 +49,9 @@ def up_to_date() -> bool:
 # Kernels that rebalance registers with setmaxnreg: ptxas must give them
 # exactly this many registers per thread at launch, or the warpgroups that
 # raise their count could wait forever for registers that do not exist.
-SETMAXNREG_KERNELS = {"fwd_bf16.cu": ("fwd_bf16_tc_kernel", 168)}
+SETMAXNREG_KERNELS = {"fwd_bf16.cu": ("fwd_bf16_tc_kernel", 168),
+                      "bwd_bf16.cu": ("bwd_main_kernel", 168),
+                      "bwd_bf16_d128.cu": ("bwd_pipe_kernel", 168)}
 
 
 def _check_registers(src: str, ptxas_log: str) -> None:

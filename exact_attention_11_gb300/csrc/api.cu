@@ -81,17 +81,31 @@ int get_encoder() {
   return FA_OK;
 }
 
-// 3-D bf16 view {d, N, BH} of a [BH, N, d] tensor; boxes of 64 x 128 x 1
+// 3-D bf16 view {d, N, BH} of a [BH, N, d] tensor; boxes of 64 x box_rows x 1
 // (one 128-byte row segment per box row) with the 128-byte swizzle.  Rows
 // past N read as zero.
-int encode_qkv_map(CUtensorMap *m, const void *base, int BH, int N, int d) {
+int encode_qkv_map(CUtensorMap *m, const void *base, int BH, int N, int d, int box_rows = 128) {
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// 3-D fp32 view {d, N, BH} of the backward's dQ accumulator, boxes of
+// 32 x 32 x 1 (128-byte rows, 128-byte swizzle) for the TMA reduce-add.
+int encode_dq_acc_map(CUtensorMap *m, void *base, int BH, int N, int d) {
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
@@ -195,18 +209,23 @@ int fa_backward(const void *q, const void *k, const void *v, const void *o, cons
   if (!workspace) return FA_ERR_INVALID_ARG;
   if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
   if (workspace_bytes < fattn::bwd_workspace_bytes(BH, N, d)) return FA_ERR_INVALID_ARG;
+  // The preparation kernel runs 16 padded rows per block of its 1-D grid.
+  if ((long long)BH * ((N + 127) / 128) * 8 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   int dev = 0;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if ((rc = current_device(&dev)) != FA_OK) return rc;
     if ((rc = get_encoder()) != FA_OK) return rc;
   }
-  if ((rc = encode_qkv_map(&tq, q, BH, N, d)) != FA_OK) return rc;
+  const int qdo_rows = fattn::bwd_qdo_box_rows(d);
+  if ((rc = encode_qkv_map(&tq, q, BH, N, d, qdo_rows)) != FA_OK) return rc;
   if ((rc = encode_qkv_map(&tk, k, BH, N, d)) != FA_OK) return rc;
   if ((rc = encode_qkv_map(&tv, v, BH, N, d)) != FA_OK) return rc;
-  if ((rc = encode_qkv_map(&tdo, dout, BH, N, d)) != FA_OK) return rc;
-  return cuda_status(fattn::launch_bwd_bf16(tq, tk, tv, tdo, o, dout, lse, dq, dk, dv, BH, N, d,
+  if ((rc = encode_qkv_map(&tdo, dout, BH, N, d, qdo_rows)) != FA_OK) return rc;
+  if ((rc = encode_dq_acc_map(&tdq, workspace, BH, N, d)) != FA_OK) return rc;
+  return cuda_status(fattn::launch_bwd_bf16(tq, tk, tv, tdo, tdq, o, dout, lse, dq, dk, dv, BH,
+                                            N, d,
                                             scale, causal ? 1 : 0,
                                             reinterpret_cast<float *>(workspace),
                                             g_dev[dev].status,

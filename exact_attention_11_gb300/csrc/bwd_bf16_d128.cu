@@ -1,0 +1,445 @@
+// bwd_bf16_d128.cu -- the main backward kernel for head dimension 128: the
+// same arithmetic as bwd_main_kernel in bwd_bf16.cu (recomputation scheme of
+// "FlashAttention: GPU 메모리 계층을 활용한 어텐션 최적화 분석", youngju.dev,
+// section 7: P = exp(S - LSE), dV = P^T dO, dP = dO V^T, dS = P (dP - D),
+// dQ = scale dS K, dK = scale dS^T Q), scheduled so that the tensor cores and
+// the CUDA cores work at the same time.
+//
+// One CTA per (128-key block j, head) keeps K_j, V_j in shared memory and
+// dV_j, dK_j (fp32) in TMEM.  Each 128-query step is split into two 64-query
+// sub-tiles t = 0, 1, each owned by one group of four warps.  While group t
+// turns S_t, dP_t into P_t, dS_t, the MMA warp works on the other sub-tile,
+// so the two groups take turns ("ping-pong"), as the forward kernel's two
+// query tiles do.  Per sub-tile (TMEM region R_t = [128t, 128t+128)):
+//   S_t^T  = K_j Q_t^T  -> R_t[0,64)      dP_t^T = V_j dO_t^T -> R_t[64,128)
+//   group t: P_t^T = exp2(S^T scale log2e - LSE2) -> bf16 at R_t[0,32);
+//            dS_t^T = P^T (dP^T - D) -> bf16 in shared memory (128-byte
+//            swizzle, keys as rows)
+//   dQ_t'^T = K_j^T dS_t^T -> R_t[64,128) (lanes = d, columns = queries)
+//   dV_j += P_t^T dO_t  (A from TMEM),  dK_j += dS_t^T Q_t  (A from smem)
+//   group t reads dQ_t'^T out of TMEM, stages it (transposed to query rows)
+//   in the dS_t buffer once dK has read it, and adds it to the fp32 dQ
+//   accumulator with TMA reduce-adds.
+// MMA order per sub-tile: dQ'_t, dV_t, dK_t, then S_t, dP_t of the next step
+// (after group t has released R_t), then the other sub-tile.  Q and dO
+// arrive as 64-row halves through 4-slot rings, two steps ahead.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fattn {
+namespace {
+
+constexpr int D = 128;
+constexpr int BM = 128;      // keys per CTA
+constexpr int BQ = 128;      // queries per step
+constexpr int BH_ = 64;      // queries per sub-tile
+constexpr int kSlots = 4;    // Q / dO half-tile ring depth
+constexpr int kThreads = 384;
+constexpr uint32_t kRegsLoad = 104, kRegsGroup = 200;
+static_assert(kRegsLoad + 2 * kRegsGroup == 3 * 168,
+              "the warpgroup register split must use exactly the launch budget");
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Shared memory (offsets from a 1024-byte aligned base; the kernel checks
+// that the dynamic shared memory it is given starts on such a boundary).
+constexpr int kTile = BM * D * 2;          // 32 KB: K or V
+constexpr int kHalf = BH_ * D * 2;         // 16 KB: a 64-row half of Q or dO
+constexpr int kHalfBox = BH_ * 128;        // 8 KB: 64 rows x 128 bytes (64 of d)
+constexpr int kKeyBox = BM * 128;          // 16 KB: 128 rows x 128 bytes
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kTile;
+constexpr int kOffQ = kOffV + kTile;                 // kSlots halves
+constexpr int kOffDO = kOffQ + kSlots * kHalf;       // kSlots halves
+constexpr int kOffDS = kOffDO + kSlots * kHalf;      // 2 x 16 KB (per sub-tile)
+constexpr int kDSBytes = BM * BH_ * 2;               // 16 KB
+constexpr int kOffVec = kOffDS + 2 * kDSBytes;       // kSlots x [LSE2 64 | D 64] f32
+constexpr int kVecBytes = 2 * BH_ * 4;               // 512 B
+constexpr int kOffBar = kOffVec + kSlots * kVecBytes;
+constexpr int kSmemBytes = kOffBar + 256;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+enum : int {
+  kBarKV = 0,
+  kBarQFull = 1,        // + slot
+  kBarQEmpty = 5,       // + slot
+  kBarDOFull = 9,       // + slot
+  kBarDOEmpty = 13,     // + slot
+  kBarSFull = 17,       // + t
+  kBarPReady = 19,      // + t, 4 warps
+  kBarDQFull = 21,      // + t
+  kBarDKDone = 23,      // + t: dV_t, dK_t (and so every read of dS_t) complete
+  kBarTmemFree = 25,    // + t, 4 warps: dQ'_t read out of TMEM
+  kBarKVDone = 27,
+  kBarDrain = 28,
+  kNumBars = 29
+};
+static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
+
+struct Misc {
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t ph, volatile int *abort_flag) {
+  return __all_sync(~0u, mbar_wait(bar, ph, abort_flag));
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t ph) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, ph) && globaltimer_ns() - t0 < kWaitLimitNs) {
+  }
+}
+
+// Status latched when the dynamic shared memory does not start on a 1024-byte
+// boundary (the layout above assumes it; the kernel then does nothing).
+constexpr int kDevBadSmemBase = -2;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_pipe_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dq, const float *__restrict__ vecs,
+                    __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int N, int BH,
+                    float scale, int causal, int *__restrict__ dev_status) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t s_base = smem_u32(smem);
+  if ((s_base & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicExch(dev_status, kDevBadSmemBase);
+    return;
+  }
+  const uint32_t bars = s_base + kOffBar;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  Misc *misc = reinterpret_cast<Misc *>(smem + kOffBar + 8 * kNumBars);
+  volatile int *abort_flag = &misc->abort;
+
+  const int jb = static_cast<int>(blockIdx.x) / BH;   // heaviest key blocks first
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int k0 = jb * BM;
+  const int n_qb = (N + BQ - 1) / BQ;
+  const int i_first = causal ? jb : 0;
+  const int n_steps = n_qb - i_first;
+  const int n_halves = 2 * n_steps;
+
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarKV), 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(bar(kBarQFull + s), 1);
+      mbar_init(bar(kBarQEmpty + s), 1);
+      mbar_init(bar(kBarDOFull + s), 1);
+      mbar_init(bar(kBarDOEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(kBarSFull + t), 1);
+      mbar_init(bar(kBarPReady + t), 4);
+      mbar_init(bar(kBarDQFull + t), 1);
+      mbar_init(bar(kBarDKDone + t), 1);
+      mbar_init(bar(kBarTmemFree + t), 4);
+    }
+    mbar_init(bar(kBarKVDone), 1);
+    mbar_init(bar(kBarDrain), 1);
+    misc->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem_base;
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLoad));
+    if (warp == 0 && elect_one()) {
+      // ---------------------------------------------------------- TMA producer
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(bar(kBarKV), 2 * kTile);
+      for (int b = 0; b < 2; ++b) {
+        tma_load_3d(s_base + kOffK + b * kKeyBox, &tm_k, b * 64, k0, bh, bar(kBarKV));
+        tma_load_3d(s_base + kOffV + b * kKeyBox, &tm_v, b * 64, k0, bh, bar(kBarKV));
+      }
+      int nq = 0, ndo = 0;
+      bool ok = true;
+      for (int h = 0; h < n_halves && ok; ++h) {
+        const int slot = h % kSlots, use = h / kSlots;
+        const int qb = i_first + (h >> 1);
+        const int qrow = qb * BQ + (h & 1) * BH_;
+        if (!(ok = mbar_wait(bar(kBarQEmpty + slot), (use & 1) ^ 1, abort_flag))) break;
+        mbar_arrive_expect_tx(bar(kBarQFull + slot), kHalf + kVecBytes);
+        for (int b = 0; b < 2; ++b)
+          tma_load_3d(s_base + kOffQ + slot * kHalf + b * kHalfBox, &tm_q, b * 64, qrow, bh,
+                      bar(kBarQFull + slot));
+        const float *vsrc = vecs + (static_cast<int64_t>(bh) * n_qb + qb) * (2 * BQ) + (h & 1) * BH_;
+        bulk_load(s_base + kOffVec + slot * kVecBytes, vsrc, BH_ * 4, bar(kBarQFull + slot));
+        bulk_load(s_base + kOffVec + slot * kVecBytes + BH_ * 4, vsrc + BQ, BH_ * 4,
+                  bar(kBarQFull + slot));
+        nq = h + 1;
+        if (!(ok = mbar_wait(bar(kBarDOEmpty + slot), (use & 1) ^ 1, abort_flag))) break;
+        mbar_arrive_expect_tx(bar(kBarDOFull + slot), kHalf);
+        for (int b = 0; b < 2; ++b)
+          tma_load_3d(s_base + kOffDO + slot * kHalf + b * kHalfBox, &tm_do, b * 64, qrow, bh,
+                      bar(kBarDOFull + slot));
+        ndo = h + 1;
+      }
+      if (!ok) {
+        drain_wait(bar(kBarKV), 0);
+        for (int h = (nq > kSlots ? nq - kSlots : 0); h < nq; ++h)
+          drain_wait(bar(kBarQFull + h % kSlots), (h / kSlots) & 1);
+        for (int h = (ndo > kSlots ? ndo - kSlots : 0); h < ndo; ++h)
+          drain_wait(bar(kBarDOFull + h % kSlots), (h / kSlots) & 1);
+      }
+    } else if (warp == 1 && elect_one()) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BH_, false);        // S^T, dP^T
+      constexpr uint32_t idesc_q = idesc_bf16_f32(D, BH_, true, true);    // dQ'^T
+      constexpr uint32_t idesc_g = idesc_bf16_f32(BM, D, true);           // dV, dK
+      const uint64_t k_kmaj = smem_desc_sw128(s_base + kOffK, 16, 1024);
+      const uint64_t v_kmaj = smem_desc_sw128(s_base + kOffV, 16, 1024);
+      const uint64_t k_mn = smem_desc_sw128(s_base + kOffK, kKeyBox, 1024);   // K^T, M = d
+      const uint64_t q_kmaj = smem_desc_sw128(s_base + kOffQ, 16, 1024);
+      const uint64_t q_mn = smem_desc_sw128(s_base + kOffQ, kHalfBox, 1024);  // N = d
+      const uint64_t do_kmaj = smem_desc_sw128(s_base + kOffDO, 16, 1024);
+      const uint64_t do_mn = smem_desc_sw128(s_base + kOffDO, kHalfBox, 1024);
+      const uint64_t ds_kmaj = smem_desc_sw128(s_base + kOffDS, 16, 1024);    // dS^T as A
+      const uint64_t ds_mn = smem_desc_sw128(s_base + kOffDS, kDSBytes, 1024); // dS^T as B
+      // S_t^T = K Q_t^T and dP_t^T = V dO_t^T of half h into R_t.
+      auto issue_sdp = [&](int h) {
+        const uint32_t R = tmem + 128u * (h & 1);
+        const uint32_t slot_off = static_cast<uint32_t>((h % kSlots) * kHalf);
+#pragma unroll 1
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ok_ = ((kk >> 2) * kKeyBox + (kk & 3) * 32) >> 4;
+          const uint32_t oh = (slot_off + (kk >> 2) * kHalfBox + (kk & 3) * 32) >> 4;
+          mma_ss(R, k_kmaj + ok_, q_kmaj + oh, idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss(R + 64, v_kmaj + ok_, do_kmaj + oh, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(kBarSFull + (h & 1)));
+      };
+      bool ok = mbar_wait(bar(kBarKV), 0, abort_flag);
+      for (int h = 0; h < 2 && h < n_halves && ok; ++h) {
+        if (!(ok = mbar_wait(bar(kBarQFull + h), 0, abort_flag))) break;
+        if (!(ok = mbar_wait(bar(kBarDOFull + h), 0, abort_flag))) break;
+        tc_fence_after();
+        issue_sdp(h);
+      }
+      for (int h = 0; h < n_halves && ok; ++h) {
+        const int t = h & 1, i = h >> 1, slot = h % kSlots;
+        const uint32_t R = tmem + 128u * t;
+        const uint32_t slot_off = static_cast<uint32_t>(slot * kHalf);
+        if (!(ok = mbar_wait(bar(kBarPReady + t), i & 1, abort_flag))) break;
+        tc_fence_after();
+        // dQ_t'^T = K^T dS_t^T: M = d, N = 64 queries, K = 128 keys.
+#pragma unroll 1
+        for (int kk = 0; kk < BM / 16; ++kk) {
+          const uint32_t off = (kk * 2048) >> 4;
+          mma_ss(R + 64, k_mn + off, ds_mn + ((t * kDSBytes) >> 4) + off, idesc_q,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(kBarDQFull + t));
+        // dV += P_t^T dO_t (A from TMEM), dK += dS_t^T Q_t (A from smem);
+        // K = 64 queries.
+#pragma unroll 1
+        for (int kk = 0; kk < BH_ / 16; ++kk) {
+          const uint32_t ob = (slot_off + kk * 2048) >> 4;
+          const uint32_t acc = (h > 0 || kk > 0) ? 1u : 0u;
+          mma_ts(tmem + 256, R + kk * 8, do_mn + ob, idesc_g, acc);
+          mma_ss(tmem + 256 + D, ds_kmaj + ((t * kDSBytes + kk * 32) >> 4), q_mn + ob, idesc_g,
+                 acc);
+        }
+        mma_commit(bar(kBarDKDone + t));
+        mma_commit(bar(kBarQEmpty + slot));
+        mma_commit(bar(kBarDOEmpty + slot));
+        const int h2 = h + 2;
+        if (h2 < n_halves) {
+          const int s2 = h2 % kSlots;
+          if (!(ok = mbar_wait(bar(kBarTmemFree + t), i & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(bar(kBarQFull + s2), (h2 / kSlots) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(bar(kBarDOFull + s2), (h2 / kSlots) & 1, abort_flag))) break;
+          tc_fence_after();
+          issue_sdp(h2);
+        }
+      }
+      if (ok) mma_commit(bar(kBarKVDone));
+      mma_commit(bar(kBarDrain));
+      drain_wait(bar(kBarDrain), 0);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsGroup));
+    // ------------------------- groups: P, dS, dQ' read-out and reduce, epilogue
+    const int t = (warp - 4) >> 2;            // sub-tile of this group
+    const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
+    const int lane = threadIdx.x & 31;
+    const int r = quarter * 32 + lane;        // key row of S^T, dP^T; d row of dQ'^T
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t R = tmem + lane_off + 128u * t;
+    const int key = k0 + r;
+    const float c = scale * kLog2e;
+    uint8_t *ds_buf = smem + kOffDS + t * kDSBytes;
+    // The 4 KB of the dS_t buffer holding this warp's own 32 key rows doubles
+    // as its dQ' staging tile: 32 queries x 32 fp32 (128-byte rows, 128-byte
+    // swizzle), the box of the accumulator's tensor map.
+    uint8_t *stage = ds_buf + quarter * 4096;
+    const uint32_t stage_u32 = s_base + kOffDS + t * kDSBytes + quarter * 4096;
+    bool ok = true;
+    for (int i = 0; i < n_steps && ok; ++i) {
+      const int h = 2 * i + t, slot = h % kSlots;
+      const int q0 = (i_first + i) * BQ + t * BH_;   // first query of the sub-tile
+      if (!(ok = wait_warp(bar(kBarSFull + t), i & 1, abort_flag))) break;
+      // [LSE2 | D] of the sub-tile came with Q_t on QFull, which S_t needed.
+      if (!(ok = wait_warp(bar(kBarQFull + slot), (h / kSlots) & 1, abort_flag))) break;
+      tc_fence_after();
+      const float *vec = reinterpret_cast<const float *>(smem + kOffVec + slot * kVecBytes);
+      const bool diag = causal && (q0 < k0 + BM) && (q0 + BH_ > k0);
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32(R + ch * 32, sv);
+        tmem_ld32(R + 64 + ch * 32, dp);
+        tmem_wait_ld(sv);
+        tmem_wait_ld(dp);
+        uint32_t pk[16], dsk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          // LSE2 and D of queries ch*32+e .. +3 (the same for every lane).
+          const float4 l4 = *reinterpret_cast<const float4 *>(vec + ch * 32 + e);
+          const float4 d4 = *reinterpret_cast<const float4 *>(vec + BH_ + ch * 32 + e);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float p4[4], g4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float p = ex2_approx(fmaf(__uint_as_float(sv[e + u]), c, -lv[u]));
+            if (key >= N || (diag && key > q0 + ch * 32 + e + u)) p = 0.f;
+            p4[u] = p;
+            g4[u] = p * (__uint_as_float(dp[e + u]) - dv4[u]);
+          }
+          pk[e >> 1] = pack_bf16x2(p4[0], p4[1]);
+          pk[(e >> 1) + 1] = pack_bf16x2(p4[2], p4[3]);
+          dsk[e >> 1] = pack_bf16x2(g4[0], g4[1]);
+          dsk[(e >> 1) + 1] = pack_bf16x2(g4[2], g4[3]);
+        }
+        // P^T: packed bf16 pairs over the fp32 columns this chunk has read.
+        tmem_st16(R + ch * 16, pk);
+        // dS^T row r: 16-byte chunk j = 4*ch + u of the 128-byte row, stored
+        // at chunk j XOR (r % 8).
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint4 w;
+          w.x = dsk[u * 4 + 0];
+          w.y = dsk[u * 4 + 1];
+          w.z = dsk[u * 4 + 2];
+          w.w = dsk[u * 4 + 3];
+          *reinterpret_cast<uint4 *>(ds_buf + r * 128 + (((4 * ch + u) ^ (r & 7)) << 4)) = w;
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarPReady + t));
+
+      // dQ_t'^T row d = r: 64 query columns, read out, then R_t is released.
+      if (!(ok = wait_warp(bar(kBarDQFull + t), i & 1, abort_flag))) break;
+      tc_fence_after();
+      uint32_t g0[32], g1[32];
+      tmem_ld32(R + 64, g0);
+      tmem_ld32(R + 96, g1);
+      tmem_wait_ld(g0);
+      tmem_wait_ld(g1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarTmemFree + t));
+      // Once dK has read dS_t, stage 32 queries at a time as query rows (this
+      // lane writes column d % 32 of every row) and reduce-add them.
+      if (!(ok = wait_warp(bar(kBarDKDone + t), i & 1, abort_flag))) break;
+#pragma unroll
+      for (int rd = 0; rd < 2; ++rd) {
+        if (rd > 0) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+        }
+        const uint32_t *gv = rd ? g1 : g0;
+#pragma unroll
+        for (int qq = 0; qq < 32; ++qq)
+          *reinterpret_cast<uint32_t *>(stage + qq * 128 + (((lane >> 2) ^ (qq & 7)) << 4) +
+                                        (lane & 3) * 4) = gv[qq];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&tm_dq, stage_u32, quarter * 32, q0 + rd * 32, bh);
+          bulk_commit();
+        }
+      }
+      // The staging tile holds this warp's dS rows of the next step.
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+
+    // Epilogue: group 0 writes dV_j, group 1 dK_j = scale * (dS^T Q), as bf16
+    // rows (rows >= N are not stored).
+    if (ok) ok = wait_warp(bar(kBarKVDone), 0, abort_flag);
+    if (ok) {
+      tc_fence_after();
+      const int64_t off = (static_cast<int64_t>(bh) * N + key) * D;
+      __nv_bfloat16 *dst = (t ? dk : dv) + off;
+      const float mul = t ? scale : 1.f;
+      const uint32_t col = t ? 256u + D : 256u;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + col + ch * 32, v);
+        tmem_wait_ld(v);
+        if (key < N) {
+          uint4 *w = reinterpret_cast<uint4 *>(dst + ch * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 x;
+            x.x = pack_bf16x2(__uint_as_float(v[8 * e + 0]) * mul, __uint_as_float(v[8 * e + 1]) * mul);
+            x.y = pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul);
+            x.z = pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul);
+            x.w = pack_bf16x2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul);
+            w[e] = x;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && misc->abort) atomicExch(dev_status, kDevTimeout);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
+                                 const CUtensorMap &tv, const CUtensorMap &tdo64,
+                                 const CUtensorMap &tdq, const float *vecs, void *dk, void *dv,
+                                 int BH, int N, float scale, int causal, int *dev_status,
+                                 cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(bwd_pipe_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int n_qb = (N + BQ - 1) / BQ;
+  bwd_pipe_kernel<<<n_qb * BH, kThreads, kSmemBytes, stream>>>(
+      tq64, tk, tv, tdo64, tdq, vecs, reinterpret_cast<__nv_bfloat16 *>(dk),
+      reinterpret_cast<__nv_bfloat16 *>(dv), N, BH, scale, causal, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace fattn

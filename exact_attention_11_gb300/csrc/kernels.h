@@ -27,14 +27,25 @@ cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             void *o, float *lse, int BH, int N, int d, float scale, int causal,
                             int *sched, int *dev_status, int fault_cta, cudaStream_t stream);
 
-// Backward: workspace = fp32 dQ accumulator [B*H*N*d] + D [B*H*N] + LSE2 [B*H*N].
-// tdo is the tensor map of dO (same form as tq).
+// Backward: workspace = fp32 dQ accumulator [B*H*N*d], then [LSE2 | D] (2 x 128
+// fp32) per 128-query block.  tq and tdo (the map of dO) are bf16 maps like
+// the forward's but with boxes of bwd_qdo_box_rows(d) rows; tk, tv as in the
+// forward; tdq is the fp32 map of the accumulator (boxes of 32 x 32 x 1,
+// 128-byte swizzle).
+inline int bwd_qdo_box_rows(int d) { return d == 128 ? 64 : 128; }
 size_t bwd_workspace_bytes(int BH, int N, int d);
 cudaError_t launch_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                            const CUtensorMap &tdo, const void *o, const void *dout,
-                            const float *lse, void *dq, void *dk, void *dv, int BH, int N, int d,
-                            float scale, int causal, float *ws, int *dev_status,
-                            cudaStream_t stream);
+                            const CUtensorMap &tdo, const CUtensorMap &tdq, const void *o,
+                            const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                            int BH, int N, int d, float scale, int causal, float *ws,
+                            int *dev_status, cudaStream_t stream);
+
+// The d = 128 main kernel (bwd_bf16_d128.cu); vecs = the [LSE2 | D] blocks.
+cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
+                                 const CUtensorMap &tv, const CUtensorMap &tdo64,
+                                 const CUtensorMap &tdq, const float *vecs, void *dk, void *dv,
+                                 int BH, int N, float scale, int causal, int *dev_status,
+                                 cudaStream_t stream);
 
 int decode_max_parts(int max_num_blocks_per_seq);
 // Split-K workspace: per (sequence, head, partition) an unnormalised output
