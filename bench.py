@@ -13,6 +13,8 @@ Printed JSON line (rank 0):
   decode         decode GB/s over the algorithmic bytes (K/V of every context
                  token, q, block table entries read, out)
   roofline       the forward (dominant kernel) against the measured bf16 peak
+  backward       fa_backward (dQ, dK, dV) of the forward workload, TFLOP/s with
+                 FLOPs = 2.5 x the forward's, and its own roofline
   e2e            the same metrics through the C ABI with pinned host buffers,
                  host<->device copies inside the timed region
   cpu_baseline   the float64 CPU oracle on the host cores, on a sample
@@ -47,6 +49,13 @@ def fwd_flops(B, H, N, d, causal, **_):
     halved under the causal mask."""
     f = 4.0 * B * H * N * N * d
     return f / 2 if causal else f
+
+
+def bwd_flops_of(B, H, N, d, causal, **_):
+    """Algorithmic FLOPs of one backward: the S recomputation and dP = dO V^T,
+    dV, dK and dQ products, 2*N*N*d each per head (five against the forward's
+    two), halved under the causal mask."""
+    return 2.5 * fwd_flops(B, H, N, d, causal)
 
 
 def read_peaks():
@@ -198,6 +207,7 @@ def gpu_arm(args):
                            out.data_ptr(), S, Hd, D, di.block_size, di.max_blocks, di.scale, sptr)
 
     flops = fwd_flops(**FWD)
+    bwd_flops = bwd_flops_of(**FWD)
     ctx = di.context_lens.to(torch.int64)
     n_blk = int(((ctx + di.block_size - 1) // di.block_size).sum())
     dec_bytes = (di.kv_bytes_read() + di.q.numel() * 2 + out.numel() * 2 + n_blk * 4
@@ -268,6 +278,35 @@ def gpu_arm(args):
     long_ms = sum(e[0].elapsed_time(e[1]) for e in lev) / kl
     del lq, lk, lv, lo, llse
 
+    # The backward (dQ, dK, dV) of the main forward workload, timed the same
+    # way on the forward's own O and LSE, reported as "backward".
+    g_out = inputs.grad_output(B, H, N, d, torch.bfloat16, seed=FWD["seed"] + 1000 * rank).to(dev)
+    gq, gk, gv = (torch.empty_like(q) for _ in range(3))
+    bws_bytes = fa.fa_backward_workspace_bytes(B, H, N, d)
+    bws = torch.empty((bws_bytes,), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        run_fwd()
+
+    def run_bwd():
+        fa.fa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), g_out.data_ptr(),
+                       lse.data_ptr(), gq.data_ptr(), gk.data_ptr(), gv.data_ptr(), B, H, N, d,
+                       scale, causal, bws.data_ptr(), bws_bytes, sptr)
+
+    kb = max(3, min(K // 4, 100))
+    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(kb)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush.zero_()
+            run_bwd()
+        for i in range(kb):
+            flush.zero_()
+            bev[i][0].record(stream)
+            run_bwd()
+            bev[i][1].record(stream)
+    stream.synchronize()
+    bwd_ms = sum(e[0].elapsed_time(e[1]) for e in bev) / kb
+    del g_out, gq, gk, gv, bws
+
     # End to end through the C ABI with pinned host buffers.
     hq, hk, hv = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3))
     for h, t in zip((hq, hk, hv), (q, k, v)):
@@ -316,8 +355,9 @@ def gpu_arm(args):
     d2h = o.numel() * 2 + lse.numel() * 4 + out.numel() * 2
 
     if ws > 1:
-        (fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms), status = reduce_over_ranks(
-            [fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms], status, dev)
+        (fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms, bwd_ms), status = \
+            reduce_over_ranks([fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms, bwd_ms],
+                              status, dev)
 
     tflops = weak_scaling_rate(flops, ws, fwd_ms, 1e12)
     per_gpu_tflops = weak_scaling_rate(flops, 1, fwd_ms, 1e12)
@@ -357,6 +397,21 @@ def gpu_arm(args):
             "frac_of_bf16_peak": round(fwd_flops(**FWD_LONG) / (long_ms * 1e-3) / 1e12
                                        / peaks["bf16_tflops"], 4),
         },
+        "backward": {
+            "workload": "fa_backward bf16 B=2 H=16 N=4096 d=128 causal (dQ, dK, dV of the "
+                        "forward workload, upstream gradient N(0,1))",
+            "ms": round(bwd_ms, 4),
+            "value": round(weak_scaling_rate(bwd_flops, ws, bwd_ms, 1e12), 2),
+            "unit": "TFLOP/s",
+            "flops_per_launch": bwd_flops,
+            "roofline": {"bound": "tensor",
+                         "achieved": round(weak_scaling_rate(bwd_flops, 1, bwd_ms, 1e12), 2),
+                         "peak": peak_t, "unit": "TFLOP/s",
+                         "frac": round(weak_scaling_rate(bwd_flops, 1, bwd_ms, 1e12) / peak_t, 4),
+                         "traffic": recorded_traffic("bwd_pipe_kernel"),
+                         "peak_kind": f"{peak_kind} bf16 burst",
+                         "kernel": "bwd_prep_kernel + bwd_pipe_kernel + bwd_dq_kernel"},
+        },
         "fwd_frac_of_bf16_peak": round(per_gpu_tflops / peak_t, 4),
         "decode": {
             "value": round(gbs, 1), "unit": "GB/s", "ms": round(dec_ms, 4),
@@ -376,7 +431,8 @@ def gpu_arm(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "KV cache resident (serving state); q, K, V, q_decode, block table, "
                         "context lens copied in and O, LSE, out copied back every step"},
-        "gpu_launches": 2 * K + kl + 2 * ke,  # library kernels inside timed regions
+        # library kernels inside timed regions (a backward is three launches)
+        "gpu_launches": 2 * K + kl + 3 * kb + 2 * ke,
         "clocks": clk,
         "device_status": status,
         "wall_s": round(wall, 3),

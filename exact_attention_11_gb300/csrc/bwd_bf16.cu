@@ -12,9 +12,10 @@
 //
 // Kernels:
 //   bwd_prep_kernel   D = rowsum(dO * O) and the LSE in log2 units, written
-//                     per 128-query block as [LSE2 x 128 | D x 128] (rows
-//                     past N padded with LSE2 = +inf, D = 0) so one bulk copy
-//                     brings a block's vectors; zeroes the fp32 dQ
+//                     negated per 128-query block as [-LSE2 x 128 | -D x 128]
+//                     (rows past N padded with -LSE2 = -inf, -D = 0) so one
+//                     bulk copy brings a block's vectors and the packed fp32
+//                     FMA/ADD use them as they are; zeroes the fp32 dQ
 //                     accumulator
 //   bwd_main_kernel   (head dimension 64; 128 runs the pipelined kernel of
 //                     bwd_bf16_d128.cu, same arithmetic and workspace)
@@ -24,7 +25,9 @@
 //                     outer order of FlashAttention-2's backward).  dQ is
 //                     summed across CTAs by TMA reduce-add (fp32, at L2) of
 //                     shared-memory tiles into the accumulator.
-//   bwd_dq_kernel     dQ = scale * accumulator, rounded to bf16
+//   bwd_dq_kernel     dQ = scale * accumulator, rounded to bf16 (the d = 128
+//                     accumulator is stored query-contiguous, [BH][d][Npad],
+//                     and transposed back here)
 //
 // bwd_main_kernel roles (384 threads): warp 0 loads with TMA, warp 1 issues
 // the MMAs (warps 2-3 only take part in the register split), warps 4-11 are
@@ -125,10 +128,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t ph) {
   }
 }
 
-// One 16-thread group per padded row (bh, i), i < n_qb * 128:
-//   i < N:  vec[LSE2] = LSE * log2(e), vec[D] = rowsum(dO * O), dQ acc row = 0
-//   i >= N: vec[LSE2] = +inf, vec[D] = 0 (padding: P = 0 there).
-template <int D>
+// One 16-thread group per padded row (bh, i), i < n_qb * 128 (a block's 16
+// rows always belong to one head):
+//   i < N:  vec[-LSE2] = -LSE * log2(e), vec[-D] = -rowsum(dO * O)
+//   i >= N: vec[-LSE2] = -inf, vec[-D] = 0 (padding: P = 0 there)
+// and the block zeroes its rows of the dQ accumulator: row-major [BH][N][D]
+// (rows < N), or, when TRANSPOSED, query-contiguous [BH][D][Npad].
+template <int D, bool TRANSPOSED>
 __global__ void __launch_bounds__(256)
     bwd_prep_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
                     const float *__restrict__ lse, float *__restrict__ vec,
@@ -136,10 +142,12 @@ __global__ void __launch_bounds__(256)
   const int64_t prow = static_cast<int64_t>(blockIdx.x) * 16 + (threadIdx.x >> 4);
   const int part = threadIdx.x & 15;
   const bool live = prow < padded_rows;
-  const int64_t bh = live ? prow / (static_cast<int64_t>(n_qb) * BQ) : 0;
-  const int i = live ? static_cast<int>(prow - bh * n_qb * BQ) : 0;
+  const int64_t npad = static_cast<int64_t>(n_qb) * BQ;
+  const int64_t bh = live ? prow / npad : 0;
+  const int i = live ? static_cast<int>(prow - bh * npad) : 0;
   const bool real = live && i < N;
   const int64_t row = bh * N + i;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   float acc = 0.f;
   if (real) {
     for (int c = part * 8; c < D; c += 128) {
@@ -152,15 +160,24 @@ __global__ void __launch_bounds__(256)
         acc = fmaf(__uint_as_float(aw[e] & 0xffff0000u), __uint_as_float(bw[e] & 0xffff0000u), acc);
       }
     }
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = part * 4; c < D; c += 64) *reinterpret_cast<float4 *>(dq_acc + row * D + c) = z;
+    if (!TRANSPOSED)
+      for (int c = part * 4; c < D; c += 64) *reinterpret_cast<float4 *>(dq_acc + row * D + c) = z;
+  }
+  if (TRANSPOSED) {
+    // 16 consecutive padded queries x D columns: D*4 float4 stores.
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * 16;
+    if (first < padded_rows) {
+      const int64_t hb = first / npad, i0 = first - hb * npad;
+      for (int w = threadIdx.x; w < D * 4; w += 256)
+        *reinterpret_cast<float4 *>(dq_acc + (hb * D + (w >> 2)) * npad + i0 + (w & 3) * 4) = z;
+    }
   }
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(~0u, acc, off);
   if (live && part == 0) {
     float *v = vec + (bh * n_qb + i / BQ) * kVecFloats;
-    v[i % BQ] = real ? lse[row] * kLog2e : INFINITY;
-    v[BQ + i % BQ] = real ? acc : 0.f;
+    v[i % BQ] = real ? -lse[row] * kLog2e : -INFINITY;
+    v[BQ + i % BQ] = real ? -acc : 0.f;
   }
 }
 
@@ -370,17 +387,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16], dsk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          // LSE2 and D of queries qbase+e .. +3 (same for every lane: broadcast).
+          // -LSE2 and -D of queries qbase+e .. +3 (same for every lane: broadcast).
           const float4 l4 = *reinterpret_cast<const float4 *>(vec + qbase + e);
           const float4 d4 = *reinterpret_cast<const float4 *>(vec + BQ + qbase + e);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
           float p4[4], g4[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            float p = ex2_approx(fmaf(__uint_as_float(sv[e + u]), c, -lv[u]));
+            float p = ex2_approx(fmaf(__uint_as_float(sv[e + u]), c, lv[u]));
             if (key >= N || (diag && key > q0 + qbase + e + u)) p = 0.f;
             p4[u] = p;
-            g4[u] = p * (__uint_as_float(dp[e + u]) - dv4[u]);
+            g4[u] = p * (__uint_as_float(dp[e + u]) + dv4[u]);
           }
           pk[e >> 1] = pack_bf16x2(p4[0], p4[1]);
           pk[(e >> 1) + 1] = pack_bf16x2(p4[2], p4[3]);
@@ -493,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && misc->abort) atomicExch(dev_status, kDevTimeout);
 }
 
-// dQ = scale * accumulator as bf16, eight elements per thread.
+// dQ = scale * accumulator as bf16, eight elements per thread (row-major
+// accumulator [BH][N][D]).
 __global__ void __launch_bounds__(256)
     bwd_dq_kernel(const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, int64_t n8,
                   float scale) {
@@ -509,6 +527,38 @@ __global__ void __launch_bounds__(256)
   reinterpret_cast<uint4 *>(dq)[i] = w;
 }
 
+// The same from the query-contiguous accumulator [BH][D][Npad]: one block per
+// (head, 32 queries) goes through a padded shared-memory tile.
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_dq_t_kernel(const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, int N,
+                    int npad, float scale) {
+  __shared__ float tile[D][33];
+  const int per_head = npad / 32;
+  const int bh = static_cast<int>(blockIdx.x / per_head);
+  const int i0 = static_cast<int>(blockIdx.x % per_head) * 32;
+  const float *src = acc + static_cast<int64_t>(bh) * D * npad + i0;
+  for (int w = threadIdx.x; w < D * 8; w += 256) {     // D rows x 8 float4
+    const int c = w >> 3, part = w & 7;
+    const float4 v = *reinterpret_cast<const float4 *>(src + static_cast<int64_t>(c) * npad + part * 4);
+    tile[c][part * 4 + 0] = v.x;
+    tile[c][part * 4 + 1] = v.y;
+    tile[c][part * 4 + 2] = v.z;
+    tile[c][part * 4 + 3] = v.w;
+  }
+  __syncthreads();
+  for (int w = threadIdx.x; w < 32 * (D / 8); w += 256) {   // 32 rows x D/8 uint4
+    const int r = w / (D / 8), cb = (w % (D / 8)) * 8;
+    if (i0 + r >= N) continue;
+    uint4 x;
+    x.x = pack_bf16x2(tile[cb + 0][r] * scale, tile[cb + 1][r] * scale);
+    x.y = pack_bf16x2(tile[cb + 2][r] * scale, tile[cb + 3][r] * scale);
+    x.z = pack_bf16x2(tile[cb + 4][r] * scale, tile[cb + 5][r] * scale);
+    x.w = pack_bf16x2(tile[cb + 6][r] * scale, tile[cb + 7][r] * scale);
+    *reinterpret_cast<uint4 *>(dq + (static_cast<int64_t>(bh) * N + i0 + r) * D + cb) = x;
+  }
+}
+
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const CUtensorMap &tdo, const CUtensorMap &tdq, const void *o,
@@ -519,9 +569,12 @@ cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   const int64_t rows = static_cast<int64_t>(BH) * N;
   const int n_qb = (N + BQ - 1) / BQ;
   const int64_t padded = static_cast<int64_t>(BH) * n_qb * BQ;
-  // Workspace: fp32 dQ accumulator [BH, N, D], then [LSE2 | D] per query block.
-  float *dq_acc = ws, *vecs = ws + rows * D;
-  bwd_prep_kernel<D><<<static_cast<unsigned>((padded + 15) / 16), 256, 0, stream>>>(
+  constexpr bool kT = bwd_dq_acc_transposed(D);
+  // Workspace: fp32 dQ accumulator (BH * Npad * D floats; row-major [BH][N][D]
+  // in its first BH * N * D, or query-contiguous [BH][D][Npad]), then
+  // [-LSE2 | -D] per query block.
+  float *dq_acc = ws, *vecs = ws + padded * D;
+  bwd_prep_kernel<D, kT><<<static_cast<unsigned>((padded + 15) / 16), 256, 0, stream>>>(
       reinterpret_cast<const __nv_bfloat16 *>(o), reinterpret_cast<const __nv_bfloat16 *>(dout),
       lse, vecs, dq_acc, N, n_qb, padded);
   cudaError_t e = cudaGetLastError();
@@ -543,18 +596,23 @@ cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;
-  const int64_t n8 = rows * D / 8;
-  bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
-      dq_acc, reinterpret_cast<__nv_bfloat16 *>(dq), n8, scale);
+  if constexpr (kT) {
+    bwd_dq_t_kernel<D><<<static_cast<unsigned>(static_cast<int64_t>(BH) * n_qb * (BQ / 32)), 256,
+                         0, stream>>>(dq_acc, reinterpret_cast<__nv_bfloat16 *>(dq), N,
+                                      n_qb * BQ, scale);
+  } else {
+    const int64_t n8 = rows * D / 8;
+    bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
+        dq_acc, reinterpret_cast<__nv_bfloat16 *>(dq), n8, scale);
+  }
   return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t bwd_workspace_bytes(int BH, int N, int d) {
-  const size_t rows = static_cast<size_t>(BH) * N;
   const size_t n_qb = (static_cast<size_t>(N) + BQ - 1) / BQ;
-  return sizeof(float) * (rows * static_cast<size_t>(d) + static_cast<size_t>(BH) * n_qb * kVecFloats);
+  return sizeof(float) * static_cast<size_t>(BH) * n_qb * BQ * (static_cast<size_t>(d) + 2);
 }
 
 cudaError_t launch_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

@@ -17,9 +17,10 @@
 //            swizzle, keys as rows)
 //   dQ_t'^T = K_j^T dS_t^T -> R_t[64,128) (lanes = d, columns = queries)
 //   dV_j += P_t^T dO_t  (A from TMEM),  dK_j += dS_t^T Q_t  (A from smem)
-//   group t reads dQ_t'^T out of TMEM, stages it (transposed to query rows)
-//   in the dS_t buffer once dK has read it, and adds it to the fp32 dQ
-//   accumulator with TMA reduce-adds.
+//   group t reads dQ_t'^T out of TMEM, stages it in the dS_t buffer once dK
+//   has read it, and adds it with TMA reduce-adds to the fp32 dQ accumulator,
+//   which is stored query-contiguous ([BH][d][Npad]) so that a lane's d row
+//   is a contiguous run of queries.
 // MMA order per sub-tile: dQ'_t, dV_t, dK_t, then S_t, dP_t of the next step
 // (after group t has released R_t), then the other sub-tile.  Q and dO
 // arrive as 64-row halves through 4-slot rings, two steps ahead.
@@ -93,6 +94,61 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t ph, volatile in
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t ph) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, ph) && globaltimer_ns() - t0 < kWaitLimitNs) {
+  }
+}
+
+// P^T and dS^T for this lane's key row r over the sub-tile's 64 queries (two
+// chunks of 32 columns).  vec holds [-LSE2 x 64 | -D x 64]; c2 = scale*log2e
+// in both halves.  P^T goes back to TMEM as packed bf16 over the columns the
+// chunk has read; dS^T row r goes to shared memory (128-byte swizzle).  With
+// MASKED, P = 0 for keys >= N and, when diag (the causal diagonal block),
+// for keys later than the query.
+template <bool MASKED>
+__device__ __forceinline__ void chunks(uint32_t R, const float *vec, uint8_t *ds_buf, int r,
+                                       int key, int q0, int N, bool diag, uint64_t c2) {
+#pragma unroll
+  for (int ch = 0; ch < 2; ++ch) {
+    uint32_t sv[32], dp[32];
+    tmem_ld32(R + ch * 32, sv);
+    tmem_ld32(R + 64 + ch * 32, dp);
+    tmem_wait_ld(sv);
+    tmem_wait_ld(dp);
+    uint32_t pk[16], dsk[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      // -LSE2 and -D of queries ch*32+e .. +3 as packed pairs (broadcast).
+      const ulonglong2 nl = *reinterpret_cast<const ulonglong2 *>(vec + ch * 32 + e);
+      const ulonglong2 nd = *reinterpret_cast<const ulonglong2 *>(vec + BH_ + ch * 32 + e);
+      const float2 x01 = f2_split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                        c2, nl.x));
+      const float2 x23 = f2_split(ffma2(f2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
+                                        c2, nl.y));
+      float p[4] = {ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y)};
+      if (MASKED) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (key >= N || (diag && key > q0 + ch * 32 + e + u)) p[u] = 0.f;
+      }
+      const uint64_t p01 = f2(p[0], p[1]), p23 = f2(p[2], p[3]);
+      const float2 g01 = f2_split(fmul2(
+          p01, fadd2(f2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd.x)));
+      const float2 g23 = f2_split(fmul2(
+          p23, fadd2(f2(__uint_as_float(dp[e + 2]), __uint_as_float(dp[e + 3])), nd.y)));
+      pk[e >> 1] = pack_bf16x2(p[0], p[1]);
+      pk[(e >> 1) + 1] = pack_bf16x2(p[2], p[3]);
+      dsk[e >> 1] = pack_bf16x2(g01.x, g01.y);
+      dsk[(e >> 1) + 1] = pack_bf16x2(g23.x, g23.y);
+    }
+    tmem_st16(R + ch * 16, pk);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      uint4 w;
+      w.x = dsk[u * 4 + 0];
+      w.y = dsk[u * 4 + 1];
+      w.z = dsk[u * 4 + 2];
+      w.w = dsk[u * 4 + 3];
+      *reinterpret_cast<uint4 *>(ds_buf + r * 128 + (((4 * ch + u) ^ (r & 7)) << 4)) = w;
+    }
   }
 }
 
@@ -283,11 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t R = tmem + lane_off + 128u * t;
     const int key = k0 + r;
-    const float c = scale * kLog2e;
+    const uint64_t c2 = f2(scale * kLog2e, scale * kLog2e);
     uint8_t *ds_buf = smem + kOffDS + t * kDSBytes;
     // The 4 KB of the dS_t buffer holding this warp's own 32 key rows doubles
-    // as its dQ' staging tile: 32 queries x 32 fp32 (128-byte rows, 128-byte
-    // swizzle), the box of the accumulator's tensor map.
+    // as its dQ' staging tile: 32 d rows x 32 queries fp32 (128-byte rows,
+    // 128-byte swizzle), the box of the accumulator's tensor map.
     uint8_t *stage = ds_buf + quarter * 4096;
     const uint32_t stage_u32 = s_base + kOffDS + t * kDSBytes + quarter * 4096;
     bool ok = true;
@@ -299,48 +355,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = wait_warp(bar(kBarQFull + slot), (h / kSlots) & 1, abort_flag))) break;
       tc_fence_after();
       const float *vec = reinterpret_cast<const float *>(smem + kOffVec + slot * kVecBytes);
+      // Masking is needed only where a key of this warp is past N or, on the
+      // diagonal block, later than a query (warp-uniform).
       const bool diag = causal && (q0 < k0 + BM) && (q0 + BH_ > k0);
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t sv[32], dp[32];
-        tmem_ld32(R + ch * 32, sv);
-        tmem_ld32(R + 64 + ch * 32, dp);
-        tmem_wait_ld(sv);
-        tmem_wait_ld(dp);
-        uint32_t pk[16], dsk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          // LSE2 and D of queries ch*32+e .. +3 (the same for every lane).
-          const float4 l4 = *reinterpret_cast<const float4 *>(vec + ch * 32 + e);
-          const float4 d4 = *reinterpret_cast<const float4 *>(vec + BH_ + ch * 32 + e);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float p4[4], g4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float p = ex2_approx(fmaf(__uint_as_float(sv[e + u]), c, -lv[u]));
-            if (key >= N || (diag && key > q0 + ch * 32 + e + u)) p = 0.f;
-            p4[u] = p;
-            g4[u] = p * (__uint_as_float(dp[e + u]) - dv4[u]);
-          }
-          pk[e >> 1] = pack_bf16x2(p4[0], p4[1]);
-          pk[(e >> 1) + 1] = pack_bf16x2(p4[2], p4[3]);
-          dsk[e >> 1] = pack_bf16x2(g4[0], g4[1]);
-          dsk[(e >> 1) + 1] = pack_bf16x2(g4[2], g4[3]);
-        }
-        // P^T: packed bf16 pairs over the fp32 columns this chunk has read.
-        tmem_st16(R + ch * 16, pk);
-        // dS^T row r: 16-byte chunk j = 4*ch + u of the 128-byte row, stored
-        // at chunk j XOR (r % 8).
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint4 w;
-          w.x = dsk[u * 4 + 0];
-          w.y = dsk[u * 4 + 1];
-          w.z = dsk[u * 4 + 2];
-          w.w = dsk[u * 4 + 3];
-          *reinterpret_cast<uint4 *>(ds_buf + r * 128 + (((4 * ch + u) ^ (r & 7)) << 4)) = w;
-        }
-      }
+      const bool masked = diag || (k0 + quarter * 32 + 31 >= N);
+      if (masked)
+        chunks<true>(R, vec, ds_buf, r, key, q0, N, diag, c2);
+      else
+        chunks<false>(R, vec, ds_buf, r, key, q0, N, diag, c2);
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
@@ -358,8 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarTmemFree + t));
-      // Once dK has read dS_t, stage 32 queries at a time as query rows (this
-      // lane writes column d % 32 of every row) and reduce-add them.
+      // Once dK has read dS_t, stage 32 queries at a time (row d = this lane,
+      // 32 fp32 = 128 bytes, 16-byte chunk j at j XOR (lane % 8)) and
+      // reduce-add them into the query-contiguous accumulator.
       if (!(ok = wait_warp(bar(kBarDKDone + t), i & 1, abort_flag))) break;
 #pragma unroll
       for (int rd = 0; rd < 2; ++rd) {
@@ -369,13 +392,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t *gv = rd ? g1 : g0;
 #pragma unroll
-        for (int qq = 0; qq < 32; ++qq)
-          *reinterpret_cast<uint32_t *>(stage + qq * 128 + (((lane >> 2) ^ (qq & 7)) << 4) +
-                                        (lane & 3) * 4) = gv[qq];
+        for (int j = 0; j < 8; ++j) {
+          uint4 w;
+          w.x = gv[4 * j + 0];
+          w.y = gv[4 * j + 1];
+          w.z = gv[4 * j + 2];
+          w.w = gv[4 * j + 3];
+          *reinterpret_cast<uint4 *>(stage + lane * 128 + ((j ^ (lane & 7)) << 4)) = w;
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_3d(&tm_dq, stage_u32, quarter * 32, q0 + rd * 32, bh);
+          tma_reduce_add_3d(&tm_dq, stage_u32, q0 + rd * 32, quarter * 32, bh);
           bulk_commit();
         }
       }

@@ -86,8 +86,9 @@ int fa_forward_fp32(const float *q, const float *k, const float *v, float *o, fl
 
 /*
  * fa_backward_workspace_bytes -- size in bytes of the fp32 workspace that
- * fa_backward needs for these sizes: 4 * (B*H*N*d + 256*B*H*ceil(N/128))
- * (an fp32 dQ accumulator, then two fp32 vectors per 128-query block).
+ * fa_backward needs for these sizes: 4 * B*H*Npad*(d + 2) with Npad = N
+ * rounded up to a multiple of 128 (an fp32 dQ accumulator, then two fp32
+ * vectors per 128-query block).
  * Returns 0 for negative sizes.
  */
 unsigned long long fa_backward_workspace_bytes(int B, int H, int N, int d);

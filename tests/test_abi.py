@@ -91,7 +91,7 @@ W = 1 << 20  # a workspace size larger than any case below needs
     ((P, P, P, P, P, P, P + 8, P, P, 1, 1, 64, 64, 0.125, 0, P, W), -3),    # misaligned dq
     ((P, P, P, P, P, P, P, P, P, 1, 1, 64, 64, 0.125, 0, NULL, W), -1),     # no workspace
     ((P, P, P, P, P, P, P, P, P, 1, 1, 64, 64, 0.125, 0, P + 4, W), -3),    # misaligned workspace
-    ((P, P, P, P, P, P, P, P, P, 1, 1, 64, 64, 0.125, 0, P, 4 * (64 * 64 + 256) - 1), -1),  # short
+    ((P, P, P, P, P, P, P, P, P, 1, 1, 64, 64, 0.125, 0, P, 4 * 128 * 66 - 1), -1),  # one byte short
     ((P, P, P, P, P, P, P, P, P, 0, 1, 64, 64, 0.125, 0, NULL, 0), 0),      # empty batch: no-op
     ((P, P, P, P, P, P, P, P, P, 1, 1, 0, 64, 0.125, 0, NULL, 0), 0),       # N = 0: no-op
 ])
@@ -100,10 +100,10 @@ def test_backward_argument_checks(lib, args, expect):
 
 
 def test_backward_workspace_size(lib):
-    # fp32 dQ accumulator [B*H*N*d], then [LSE2 | D] (256 floats) per 128-query block
-    assert lib.fa_backward_workspace_bytes(2, 3, 100, 128) == 4 * (2 * 3 * 100 * 128 + 6 * 256)
-    assert lib.fa_backward_workspace_bytes(1, 1, 64, 64) == 4 * (64 * 64 + 256)
-    assert lib.fa_backward_workspace_bytes(1, 2, 129, 64) == 4 * (2 * 129 * 64 + 2 * 2 * 256)
+    # fp32 dQ accumulator over N rounded up to 128, then two vectors per 128-query block
+    assert lib.fa_backward_workspace_bytes(2, 3, 100, 128) == 4 * 2 * 3 * 128 * 130
+    assert lib.fa_backward_workspace_bytes(1, 1, 64, 64) == 4 * 128 * 66
+    assert lib.fa_backward_workspace_bytes(1, 2, 129, 64) == 4 * 2 * 256 * 66
     assert lib.fa_backward_workspace_bytes(-1, 1, 64, 64) == 0
     assert fa.fa_backward_workspace_bytes(0, 4, 64, 64) == 0
 
