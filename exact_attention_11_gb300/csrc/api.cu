@@ -96,16 +96,11 @@ int encode_qkv_map(CUtensorMap *m, const void *base, int BH, int N, int d, int b
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// 3-D fp32 view of the backward's dQ accumulator, boxes of 32 x 32 x 1
-// (128-byte rows, 128-byte swizzle) for the TMA reduce-add: {d, N, BH} when
-// row-major, {Npad, d, BH} when query-contiguous.
+// 3-D fp32 view {d, N, BH} of the backward's row-major dQ accumulator, boxes
+// of 32 x 32 x 1 (128-byte rows, 128-byte swizzle) for the TMA reduce-add.
 int encode_dq_acc_map(CUtensorMap *m, void *base, int BH, int N, int d) {
-  const cuuint64_t npad = (cuuint64_t)((N + 127) / 128) * 128;
-  const bool tr = fattn::bwd_dq_acc_transposed(d);
-  const cuuint64_t dims[3] = {tr ? npad : (cuuint64_t)d, tr ? (cuuint64_t)d : (cuuint64_t)N,
-                              (cuuint64_t)BH};
-  const cuuint64_t strides[2] = {tr ? npad * 4 : (cuuint64_t)d * 4,
-                                 tr ? (cuuint64_t)d * npad * 4 : (cuuint64_t)N * d * 4};
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
   const cuuint32_t box[3] = {32, 32, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box,

@@ -23,11 +23,10 @@
 //                     in shared memory and dK_j, dV_j in TMEM while the CTA
 //                     visits every query block i that sees block j (the KV-
 //                     outer order of FlashAttention-2's backward).  dQ is
-//                     summed across CTAs by TMA reduce-add (fp32, at L2) of
-//                     shared-memory tiles into the accumulator.
-//   bwd_dq_kernel     dQ = scale * accumulator, rounded to bf16 (the d = 128
-//                     accumulator is stored query-contiguous, [BH][d][Npad],
-//                     and transposed back here)
+//                     summed across CTAs into an fp32 accumulator [BH][N][d]
+//                     (TMA reduce-add of shared-memory tiles here; the d = 128
+//                     kernel adds from registers).
+//   bwd_dq_kernel     dQ = scale * accumulator, rounded to bf16
 //
 // bwd_main_kernel roles (384 threads): warp 0 loads with TMA, warp 1 issues
 // the MMAs (warps 2-3 only take part in the register split), warps 4-11 are
@@ -128,13 +127,11 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t ph) {
   }
 }
 
-// One 16-thread group per padded row (bh, i), i < n_qb * 128 (a block's 16
-// rows always belong to one head):
-//   i < N:  vec[-LSE2] = -LSE * log2(e), vec[-D] = -rowsum(dO * O)
-//   i >= N: vec[-LSE2] = -inf, vec[-D] = 0 (padding: P = 0 there)
-// and the block zeroes its rows of the dQ accumulator: row-major [BH][N][D]
-// (rows < N), or, when TRANSPOSED, query-contiguous [BH][D][Npad].
-template <int D, bool TRANSPOSED>
+// One 16-thread group per padded row (bh, i), i < n_qb * 128:
+//   i < N:  vec[-LSE2] = -LSE * log2(e), vec[-D] = -rowsum(dO * O), and the
+//           row of the dQ accumulator is zeroed
+//   i >= N: vec[-LSE2] = -inf, vec[-D] = 0 (padding: P = 0 there).
+template <int D>
 __global__ void __launch_bounds__(256)
     bwd_prep_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
                     const float *__restrict__ lse, float *__restrict__ vec,
@@ -147,7 +144,6 @@ __global__ void __launch_bounds__(256)
   const int i = live ? static_cast<int>(prow - bh * npad) : 0;
   const bool real = live && i < N;
   const int64_t row = bh * N + i;
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   float acc = 0.f;
   if (real) {
     for (int c = part * 8; c < D; c += 128) {
@@ -160,17 +156,8 @@ __global__ void __launch_bounds__(256)
         acc = fmaf(__uint_as_float(aw[e] & 0xffff0000u), __uint_as_float(bw[e] & 0xffff0000u), acc);
       }
     }
-    if (!TRANSPOSED)
-      for (int c = part * 4; c < D; c += 64) *reinterpret_cast<float4 *>(dq_acc + row * D + c) = z;
-  }
-  if (TRANSPOSED) {
-    // 16 consecutive padded queries x D columns: D*4 float4 stores.
-    const int64_t first = static_cast<int64_t>(blockIdx.x) * 16;
-    if (first < padded_rows) {
-      const int64_t hb = first / npad, i0 = first - hb * npad;
-      for (int w = threadIdx.x; w < D * 4; w += 256)
-        *reinterpret_cast<float4 *>(dq_acc + (hb * D + (w >> 2)) * npad + i0 + (w & 3) * 4) = z;
-    }
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = part * 4; c < D; c += 64) *reinterpret_cast<float4 *>(dq_acc + row * D + c) = z;
   }
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(~0u, acc, off);
@@ -527,38 +514,6 @@ __global__ void __launch_bounds__(256)
   reinterpret_cast<uint4 *>(dq)[i] = w;
 }
 
-// The same from the query-contiguous accumulator [BH][D][Npad]: one block per
-// (head, 32 queries) goes through a padded shared-memory tile.
-template <int D>
-__global__ void __launch_bounds__(256)
-    bwd_dq_t_kernel(const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, int N,
-                    int npad, float scale) {
-  __shared__ float tile[D][33];
-  const int per_head = npad / 32;
-  const int bh = static_cast<int>(blockIdx.x / per_head);
-  const int i0 = static_cast<int>(blockIdx.x % per_head) * 32;
-  const float *src = acc + static_cast<int64_t>(bh) * D * npad + i0;
-  for (int w = threadIdx.x; w < D * 8; w += 256) {     // D rows x 8 float4
-    const int c = w >> 3, part = w & 7;
-    const float4 v = *reinterpret_cast<const float4 *>(src + static_cast<int64_t>(c) * npad + part * 4);
-    tile[c][part * 4 + 0] = v.x;
-    tile[c][part * 4 + 1] = v.y;
-    tile[c][part * 4 + 2] = v.z;
-    tile[c][part * 4 + 3] = v.w;
-  }
-  __syncthreads();
-  for (int w = threadIdx.x; w < 32 * (D / 8); w += 256) {   // 32 rows x D/8 uint4
-    const int r = w / (D / 8), cb = (w % (D / 8)) * 8;
-    if (i0 + r >= N) continue;
-    uint4 x;
-    x.x = pack_bf16x2(tile[cb + 0][r] * scale, tile[cb + 1][r] * scale);
-    x.y = pack_bf16x2(tile[cb + 2][r] * scale, tile[cb + 3][r] * scale);
-    x.z = pack_bf16x2(tile[cb + 4][r] * scale, tile[cb + 5][r] * scale);
-    x.w = pack_bf16x2(tile[cb + 6][r] * scale, tile[cb + 7][r] * scale);
-    *reinterpret_cast<uint4 *>(dq + (static_cast<int64_t>(bh) * N + i0 + r) * D + cb) = x;
-  }
-}
-
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const CUtensorMap &tdo, const CUtensorMap &tdq, const void *o,
@@ -569,19 +524,17 @@ cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   const int64_t rows = static_cast<int64_t>(BH) * N;
   const int n_qb = (N + BQ - 1) / BQ;
   const int64_t padded = static_cast<int64_t>(BH) * n_qb * BQ;
-  constexpr bool kT = bwd_dq_acc_transposed(D);
-  // Workspace: fp32 dQ accumulator (BH * Npad * D floats; row-major [BH][N][D]
-  // in its first BH * N * D, or query-contiguous [BH][D][Npad]), then
-  // [-LSE2 | -D] per query block.
+  // Workspace: fp32 dQ accumulator (row-major [BH][N][D] in the first
+  // BH * N * D of BH * Npad * D floats), then [-LSE2 | -D] per query block.
   float *dq_acc = ws, *vecs = ws + padded * D;
-  bwd_prep_kernel<D, kT><<<static_cast<unsigned>((padded + 15) / 16), 256, 0, stream>>>(
+  bwd_prep_kernel<D><<<static_cast<unsigned>((padded + 15) / 16), 256, 0, stream>>>(
       reinterpret_cast<const __nv_bfloat16 *>(o), reinterpret_cast<const __nv_bfloat16 *>(dout),
       lse, vecs, dq_acc, N, n_qb, padded);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if constexpr (D == 128) {
     // Q and dO maps have 64-row boxes here (the pipelined kernel's sub-tiles).
-    e = launch_bwd_main_d128(tq, tk, tv, tdo, tdq, vecs, dk, dv, BH, N, scale, causal,
+    e = launch_bwd_main_d128(tq, tk, tv, tdo, vecs, dq_acc, dk, dv, BH, N, scale, causal,
                              dev_status, stream);
   } else {
     // At least 120 KB so that one CTA (which takes all 512 TMEM columns) runs
@@ -596,15 +549,9 @@ cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;
-  if constexpr (kT) {
-    bwd_dq_t_kernel<D><<<static_cast<unsigned>(static_cast<int64_t>(BH) * n_qb * (BQ / 32)), 256,
-                         0, stream>>>(dq_acc, reinterpret_cast<__nv_bfloat16 *>(dq), N,
-                                      n_qb * BQ, scale);
-  } else {
-    const int64_t n8 = rows * D / 8;
-    bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
-        dq_acc, reinterpret_cast<__nv_bfloat16 *>(dq), n8, scale);
-  }
+  const int64_t n8 = rows * D / 8;
+  bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
+      dq_acc, reinterpret_cast<__nv_bfloat16 *>(dq), n8, scale);
   return cudaGetLastError();
 }
 

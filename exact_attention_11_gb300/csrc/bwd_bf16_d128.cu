@@ -12,15 +12,17 @@
 // so the two groups take turns ("ping-pong"), as the forward kernel's two
 // query tiles do.  Per sub-tile (TMEM region R_t = [128t, 128t+128)):
 //   S_t^T  = K_j Q_t^T  -> R_t[0,64)      dP_t^T = V_j dO_t^T -> R_t[64,128)
-//   group t: P_t^T = exp2(S^T scale log2e - LSE2) -> bf16 at R_t[0,32);
-//            dS_t^T = P^T (dP^T - D) -> bf16 in shared memory (128-byte
-//            swizzle, keys as rows)
+//   group t: P_t^T = exp2(S^T scale log2e - LSE2) and dS_t^T = P^T (dP^T - D)
+//            as packed bf16 at R_t[0,32) and R_t[32,64); dS^T also to shared
+//            memory (128-byte swizzle, keys as rows)
 //   dQ_t'^T = K_j^T dS_t^T -> R_t[64,128) (lanes = d, columns = queries)
-//   dV_j += P_t^T dO_t  (A from TMEM),  dK_j += dS_t^T Q_t  (A from smem)
-//   group t reads dQ_t'^T out of TMEM, stages it in the dS_t buffer once dK
-//   has read it, and adds it with TMA reduce-adds to the fp32 dQ accumulator,
-//   which is stored query-contiguous ([BH][d][Npad]) so that a lane's d row
-//   is a contiguous run of queries.
+//   dV_j += P_t^T dO_t,  dK_j += dS_t^T Q_t            (A operands from TMEM)
+//   group t reads dQ_t'^T out of TMEM and adds it to the fp32 dQ accumulator
+//   from registers: for each query the warp's 32 lanes (32 consecutive d)
+//   add one contiguous 128-byte run of its row.
+// The kernel is bound by shared-memory bandwidth (MMA operands, TMA writes,
+// dS stores), so operands come from TMEM wherever the TMEM budget allows and
+// dQ' never passes through shared memory.
 // MMA order per sub-tile: dQ'_t, dV_t, dK_t, then S_t, dP_t of the next step
 // (after group t has released R_t), then the other sub-tile.  Q and dO
 // arrive as 64-row halves through 4-slot rings, two steps ahead.
@@ -74,11 +76,10 @@ enum : int {
   kBarSFull = 17,       // + t
   kBarPReady = 19,      // + t, 4 warps
   kBarDQFull = 21,      // + t
-  kBarDKDone = 23,      // + t: dV_t, dK_t (and so every read of dS_t) complete
-  kBarTmemFree = 25,    // + t, 4 warps: dQ'_t read out of TMEM
-  kBarKVDone = 27,
-  kBarDrain = 28,
-  kNumBars = 29
+  kBarTmemFree = 23,    // + t, 4 warps: dQ'_t read out of TMEM
+  kBarKVDone = 25,
+  kBarDrain = 26,
+  kNumBars = 27
 };
 static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
 
@@ -97,59 +98,71 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t ph) {
   }
 }
 
-// P^T and dS^T for this lane's key row r over the sub-tile's 64 queries (two
-// chunks of 32 columns).  vec holds [-LSE2 x 64 | -D x 64]; c2 = scale*log2e
-// in both halves.  P^T goes back to TMEM as packed bf16 over the columns the
-// chunk has read; dS^T row r goes to shared memory (128-byte swizzle).  With
-// MASKED, P = 0 for keys >= N and, when diag (the causal diagonal block),
-// for keys later than the query.
+// P^T and dS^T of one 32-query chunk (columns ch*32 .. +31 of the sub-tile)
+// for this lane's key row r.  vec holds [-LSE2 x 64 | -D x 64]; c2 =
+// scale*log2e in both halves.  Returns both as packed bf16 pairs and stores
+// dS^T row r to shared memory (128-byte swizzle).  With MASKED, P = 0 for
+// keys >= N and, when diag (the causal diagonal block), for keys later than
+// the query.
+template <bool MASKED>
+__device__ __forceinline__ void chunk(uint32_t R, int ch, const float *vec, uint8_t *ds_buf, int r,
+                                      int key, int q0, int N, bool diag, uint64_t c2,
+                                      uint32_t (&pk)[16], uint32_t (&dsk)[16]) {
+  uint32_t sv[32], dp[32];
+  tmem_ld32(R + ch * 32, sv);
+  tmem_ld32(R + 64 + ch * 32, dp);
+  tmem_wait_ld(sv);
+  tmem_wait_ld(dp);
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    // -LSE2 and -D of queries ch*32+e .. +3 as packed pairs (broadcast).
+    const ulonglong2 nl = *reinterpret_cast<const ulonglong2 *>(vec + ch * 32 + e);
+    const ulonglong2 nd = *reinterpret_cast<const ulonglong2 *>(vec + BH_ + ch * 32 + e);
+    const float2 x01 = f2_split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                      c2, nl.x));
+    const float2 x23 = f2_split(ffma2(f2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
+                                      c2, nl.y));
+    float p[4] = {ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y)};
+    if (MASKED) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (key >= N || (diag && key > q0 + ch * 32 + e + u)) p[u] = 0.f;
+    }
+    const uint64_t p01 = f2(p[0], p[1]), p23 = f2(p[2], p[3]);
+    const float2 g01 = f2_split(fmul2(
+        p01, fadd2(f2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd.x)));
+    const float2 g23 = f2_split(fmul2(
+        p23, fadd2(f2(__uint_as_float(dp[e + 2]), __uint_as_float(dp[e + 3])), nd.y)));
+    pk[e >> 1] = pack_bf16x2(p[0], p[1]);
+    pk[(e >> 1) + 1] = pack_bf16x2(p[2], p[3]);
+    dsk[e >> 1] = pack_bf16x2(g01.x, g01.y);
+    dsk[(e >> 1) + 1] = pack_bf16x2(g23.x, g23.y);
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    uint4 w;
+    w.x = dsk[u * 4 + 0];
+    w.y = dsk[u * 4 + 1];
+    w.z = dsk[u * 4 + 2];
+    w.w = dsk[u * 4 + 3];
+    *reinterpret_cast<uint4 *>(ds_buf + r * 128 + (((4 * ch + u) ^ (r & 7)) << 4)) = w;
+  }
+}
+
+// Both chunks of the sub-tile.  P^T ends at R[0,32) and dS^T at R[32,64) as
+// packed bf16 pairs (queries 2c, 2c+1 in column c): chunk 1 (S columns 32-63)
+// goes first so that dS^T of chunk 1 may overwrite S columns 48-63 at once;
+// P^T of chunk 1 waits in registers until chunk 0 has read columns 0-31.
 template <bool MASKED>
 __device__ __forceinline__ void chunks(uint32_t R, const float *vec, uint8_t *ds_buf, int r,
                                        int key, int q0, int N, bool diag, uint64_t c2) {
-#pragma unroll
-  for (int ch = 0; ch < 2; ++ch) {
-    uint32_t sv[32], dp[32];
-    tmem_ld32(R + ch * 32, sv);
-    tmem_ld32(R + 64 + ch * 32, dp);
-    tmem_wait_ld(sv);
-    tmem_wait_ld(dp);
-    uint32_t pk[16], dsk[16];
-#pragma unroll
-    for (int e = 0; e < 32; e += 4) {
-      // -LSE2 and -D of queries ch*32+e .. +3 as packed pairs (broadcast).
-      const ulonglong2 nl = *reinterpret_cast<const ulonglong2 *>(vec + ch * 32 + e);
-      const ulonglong2 nd = *reinterpret_cast<const ulonglong2 *>(vec + BH_ + ch * 32 + e);
-      const float2 x01 = f2_split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
-                                        c2, nl.x));
-      const float2 x23 = f2_split(ffma2(f2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
-                                        c2, nl.y));
-      float p[4] = {ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y)};
-      if (MASKED) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (key >= N || (diag && key > q0 + ch * 32 + e + u)) p[u] = 0.f;
-      }
-      const uint64_t p01 = f2(p[0], p[1]), p23 = f2(p[2], p[3]);
-      const float2 g01 = f2_split(fmul2(
-          p01, fadd2(f2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd.x)));
-      const float2 g23 = f2_split(fmul2(
-          p23, fadd2(f2(__uint_as_float(dp[e + 2]), __uint_as_float(dp[e + 3])), nd.y)));
-      pk[e >> 1] = pack_bf16x2(p[0], p[1]);
-      pk[(e >> 1) + 1] = pack_bf16x2(p[2], p[3]);
-      dsk[e >> 1] = pack_bf16x2(g01.x, g01.y);
-      dsk[(e >> 1) + 1] = pack_bf16x2(g23.x, g23.y);
-    }
-    tmem_st16(R + ch * 16, pk);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      uint4 w;
-      w.x = dsk[u * 4 + 0];
-      w.y = dsk[u * 4 + 1];
-      w.z = dsk[u * 4 + 2];
-      w.w = dsk[u * 4 + 3];
-      *reinterpret_cast<uint4 *>(ds_buf + r * 128 + (((4 * ch + u) ^ (r & 7)) << 4)) = w;
-    }
-  }
+  uint32_t pk1[16], dsk1[16], pk0[16], dsk0[16];
+  chunk<MASKED>(R, 1, vec, ds_buf, r, key, q0, N, diag, c2, pk1, dsk1);
+  tmem_st16(R + 48, dsk1);
+  chunk<MASKED>(R, 0, vec, ds_buf, r, key, q0, N, diag, c2, pk0, dsk0);
+  tmem_st16(R + 0, pk0);
+  tmem_st16(R + 16, pk1);
+  tmem_st16(R + 32, dsk0);
 }
 
 // Status latched when the dynamic shared memory does not start on a 1024-byte
@@ -159,7 +172,7 @@ constexpr int kDevBadSmemBase = -2;
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_pipe_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_dq, const float *__restrict__ vecs,
+                    const float *__restrict__ vecs, float *__restrict__ dq_acc,
                     __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int N, int BH,
                     float scale, int causal, int *__restrict__ dev_status) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -194,7 +207,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarSFull + t), 1);
       mbar_init(bar(kBarPReady + t), 4);
       mbar_init(bar(kBarDQFull + t), 1);
-      mbar_init(bar(kBarDKDone + t), 1);
       mbar_init(bar(kBarTmemFree + t), 4);
     }
     mbar_init(bar(kBarKVDone), 1);
@@ -256,28 +268,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 1 && elect_one()) {
       // ---------------------------------------------------------- MMA issuer
+      // Fully unrolled issue with 32-bit descriptor words: a rolled loop
+      // costs the issuing thread about 60 cycles per MMA, more than an
+      // M = 128, N = 64 MMA takes on the tensor core.
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BH_, false);        // S^T, dP^T
       constexpr uint32_t idesc_q = idesc_bf16_f32(D, BH_, true, true);    // dQ'^T
       constexpr uint32_t idesc_g = idesc_bf16_f32(BM, D, true);           // dV, dK
-      const uint64_t k_kmaj = smem_desc_sw128(s_base + kOffK, 16, 1024);
-      const uint64_t v_kmaj = smem_desc_sw128(s_base + kOffV, 16, 1024);
-      const uint64_t k_mn = smem_desc_sw128(s_base + kOffK, kKeyBox, 1024);   // K^T, M = d
-      const uint64_t q_kmaj = smem_desc_sw128(s_base + kOffQ, 16, 1024);
-      const uint64_t q_mn = smem_desc_sw128(s_base + kOffQ, kHalfBox, 1024);  // N = d
-      const uint64_t do_kmaj = smem_desc_sw128(s_base + kOffDO, 16, 1024);
-      const uint64_t do_mn = smem_desc_sw128(s_base + kOffDO, kHalfBox, 1024);
-      const uint64_t ds_kmaj = smem_desc_sw128(s_base + kOffDS, 16, 1024);    // dS^T as A
-      const uint64_t ds_mn = smem_desc_sw128(s_base + kOffDS, kDSBytes, 1024); // dS^T as B
+      const uint32_t k_kmaj = sdesc_lo(s_base + kOffK, 16);
+      const uint32_t v_kmaj = sdesc_lo(s_base + kOffV, 16);
+      const uint32_t k_mn = sdesc_lo(s_base + kOffK, kKeyBox);   // K^T, M = d
+      const uint32_t q_kmaj = sdesc_lo(s_base + kOffQ, 16);
+      const uint32_t q_mn = sdesc_lo(s_base + kOffQ, kHalfBox);  // N = d
+      const uint32_t do_kmaj = sdesc_lo(s_base + kOffDO, 16);
+      const uint32_t do_mn = sdesc_lo(s_base + kOffDO, kHalfBox);
+      const uint32_t ds_mn = sdesc_lo(s_base + kOffDS, kDSBytes); // dS^T as B
       // S_t^T = K Q_t^T and dP_t^T = V dO_t^T of half h into R_t.
       auto issue_sdp = [&](int h) {
         const uint32_t R = tmem + 128u * (h & 1);
-        const uint32_t slot_off = static_cast<uint32_t>((h % kSlots) * kHalf);
-#pragma unroll 1
+        const uint32_t so = static_cast<uint32_t>((h % kSlots) * kHalf) >> 4;
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ok_ = ((kk >> 2) * kKeyBox + (kk & 3) * 32) >> 4;
-          const uint32_t oh = (slot_off + (kk >> 2) * kHalfBox + (kk & 3) * 32) >> 4;
-          mma_ss(R, k_kmaj + ok_, q_kmaj + oh, idesc_s, kk > 0 ? 1u : 0u);
-          mma_ss(R + 64, v_kmaj + ok_, do_kmaj + oh, idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t ok_ = static_cast<uint32_t>((kk >> 2) * kKeyBox + (kk & 3) * 32) >> 4;
+          const uint32_t oh = static_cast<uint32_t>((kk >> 2) * kHalfBox + (kk & 3) * 32) >> 4;
+          mma_ss_lo(R, k_kmaj + ok_, q_kmaj + so + oh, idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss_lo(R + 64, v_kmaj + ok_, do_kmaj + so + oh, idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(kBarSFull + (h & 1)));
       };
@@ -291,28 +305,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < n_halves && ok; ++h) {
         const int t = h & 1, i = h >> 1, slot = h % kSlots;
         const uint32_t R = tmem + 128u * t;
-        const uint32_t slot_off = static_cast<uint32_t>(slot * kHalf);
         if (!(ok = mbar_wait(bar(kBarPReady + t), i & 1, abort_flag))) break;
         tc_fence_after();
         // dQ_t'^T = K^T dS_t^T: M = d, N = 64 queries, K = 128 keys.
-#pragma unroll 1
+        const uint32_t dso = static_cast<uint32_t>(t * kDSBytes) >> 4;
+#pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk) {
-          const uint32_t off = (kk * 2048) >> 4;
-          mma_ss(R + 64, k_mn + off, ds_mn + ((t * kDSBytes) >> 4) + off, idesc_q,
-                 kk > 0 ? 1u : 0u);
+          const uint32_t off = static_cast<uint32_t>(kk * 2048) >> 4;
+          mma_ss_lo(R + 64, k_mn + off, ds_mn + dso + off, idesc_q, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(kBarDQFull + t));
-        // dV += P_t^T dO_t (A from TMEM), dK += dS_t^T Q_t (A from smem);
-        // K = 64 queries.
-#pragma unroll 1
+        // dV += P_t^T dO_t, dK += dS_t^T Q_t (A operands from TMEM); K = 64
+        // queries.
+        const uint32_t so = static_cast<uint32_t>(slot * kHalf) >> 4;
+#pragma unroll
         for (int kk = 0; kk < BH_ / 16; ++kk) {
-          const uint32_t ob = (slot_off + kk * 2048) >> 4;
+          const uint32_t ob = so + (static_cast<uint32_t>(kk * 2048) >> 4);
           const uint32_t acc = (h > 0 || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + 256, R + kk * 8, do_mn + ob, idesc_g, acc);
-          mma_ss(tmem + 256 + D, ds_kmaj + ((t * kDSBytes + kk * 32) >> 4), q_mn + ob, idesc_g,
-                 acc);
+          mma_ts_lo(tmem + 256, R + kk * 8, do_mn + ob, idesc_g, acc);
+          mma_ts_lo(tmem + 256 + D, R + 32 + kk * 8, q_mn + ob, idesc_g, acc);
         }
-        mma_commit(bar(kBarDKDone + t));
         mma_commit(bar(kBarQEmpty + slot));
         mma_commit(bar(kBarDOEmpty + slot));
         const int h2 = h + 2;
@@ -341,11 +353,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = k0 + r;
     const uint64_t c2 = f2(scale * kLog2e, scale * kLog2e);
     uint8_t *ds_buf = smem + kOffDS + t * kDSBytes;
-    // The 4 KB of the dS_t buffer holding this warp's own 32 key rows doubles
-    // as its dQ' staging tile: 32 d rows x 32 queries fp32 (128-byte rows,
-    // 128-byte swizzle), the box of the accumulator's tensor map.
-    uint8_t *stage = ds_buf + quarter * 4096;
-    const uint32_t stage_u32 = s_base + kOffDS + t * kDSBytes + quarter * 4096;
     bool ok = true;
     for (int i = 0; i < n_steps && ok; ++i) {
       const int h = 2 * i + t, slot = h % kSlots;
@@ -380,39 +387,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarTmemFree + t));
-      // Once dK has read dS_t, stage 32 queries at a time (row d = this lane,
-      // 32 fp32 = 128 bytes, 16-byte chunk j at j XOR (lane % 8)) and
-      // reduce-add them into the query-contiguous accumulator.
-      if (!(ok = wait_warp(bar(kBarDKDone + t), i & 1, abort_flag))) break;
+      // Add into the row-major accumulator: for query q0 + qq the 32 lanes
+      // (d = 32*quarter + lane) cover one contiguous 128-byte run of its row.
+      float *dst = dq_acc + (static_cast<int64_t>(bh) * N + q0) * D + r;
 #pragma unroll
-      for (int rd = 0; rd < 2; ++rd) {
-        if (rd > 0) {
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
-        }
-        const uint32_t *gv = rd ? g1 : g0;
+      for (int qq = 0; qq < 32; ++qq)
+        if (q0 + qq < N) red_add_f32(dst + static_cast<int64_t>(qq) * D, __uint_as_float(g0[qq]));
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint4 w;
-          w.x = gv[4 * j + 0];
-          w.y = gv[4 * j + 1];
-          w.z = gv[4 * j + 2];
-          w.w = gv[4 * j + 3];
-          *reinterpret_cast<uint4 *>(stage + lane * 128 + ((j ^ (lane & 7)) << 4)) = w;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_3d(&tm_dq, stage_u32, q0 + rd * 32, quarter * 32, bh);
-          bulk_commit();
-        }
-      }
-      // The staging tile holds this warp's dS rows of the next step.
-      if (lane == 0) bulk_wait_read_all();
-      __syncwarp();
+      for (int qq = 0; qq < 32; ++qq)
+        if (q0 + 32 + qq < N)
+          red_add_f32(dst + static_cast<int64_t>(32 + qq) * D, __uint_as_float(g1[qq]));
     }
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
 
     // Epilogue: group 0 writes dV_j, group 1 dK_j = scale * (dS^T Q), as bf16
     // rows (rows >= N are not stored).
@@ -457,15 +442,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
                                  const CUtensorMap &tv, const CUtensorMap &tdo64,
-                                 const CUtensorMap &tdq, const float *vecs, void *dk, void *dv,
-                                 int BH, int N, float scale, int causal, int *dev_status,
+                                 const float *vecs, float *dq_acc, void *dk, void *dv, int BH,
+                                 int N, float scale, int causal, int *dev_status,
                                  cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(bwd_pipe_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_qb = (N + BQ - 1) / BQ;
   bwd_pipe_kernel<<<n_qb * BH, kThreads, kSmemBytes, stream>>>(
-      tq64, tk, tv, tdo64, tdq, vecs, reinterpret_cast<__nv_bfloat16 *>(dk),
+      tq64, tk, tv, tdo64, vecs, dq_acc, reinterpret_cast<__nv_bfloat16 *>(dk),
       reinterpret_cast<__nv_bfloat16 *>(dv), N, BH, scale, causal, dev_status);
   return cudaGetLastError();
 }

@@ -27,15 +27,13 @@ cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             void *o, float *lse, int BH, int N, int d, float scale, int causal,
                             int *sched, int *dev_status, int fault_cta, cudaStream_t stream);
 
-// Backward: workspace = fp32 dQ accumulator (B*H*Npad*d floats, Npad = N
-// rounded up to 128), then [-LSE2 | -D] (2 x 128 fp32) per 128-query block:
-// 4 * B*H*Npad*(d + 2) bytes.  For d = 128 the accumulator is query-contiguous
-// ([BH][d][Npad]), else row-major ([BH][N][d]).  tq and tdo (the map of dO)
-// are bf16 maps like the forward's but with boxes of bwd_qdo_box_rows(d) rows;
-// tk, tv as in the forward; tdq is the fp32 map of the accumulator in its
-// layout (boxes of 32 x 32 x 1, 128-byte swizzle).
+// Backward: workspace = fp32 dQ accumulator (row-major [BH][N][d] inside
+// B*H*Npad*d floats, Npad = N rounded up to 128), then [-LSE2 | -D] (2 x 128
+// fp32) per 128-query block: 4 * B*H*Npad*(d + 2) bytes.  tq and tdo (the map
+// of dO) are bf16 maps like the forward's but with boxes of
+// bwd_qdo_box_rows(d) rows; tk, tv as in the forward; tdq is the fp32 map of
+// the accumulator (boxes of 32 x 32 x 1, 128-byte swizzle; used for d = 64).
 inline int bwd_qdo_box_rows(int d) { return d == 128 ? 64 : 128; }
-constexpr bool bwd_dq_acc_transposed(int d) { return d == 128; }
 size_t bwd_workspace_bytes(int BH, int N, int d);
 cudaError_t launch_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const CUtensorMap &tdo, const CUtensorMap &tdq, const void *o,
@@ -43,11 +41,12 @@ cudaError_t launch_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             int BH, int N, int d, float scale, int causal, float *ws,
                             int *dev_status, cudaStream_t stream);
 
-// The d = 128 main kernel (bwd_bf16_d128.cu); vecs = the [LSE2 | D] blocks.
+// The d = 128 main kernel (bwd_bf16_d128.cu); vecs = the [-LSE2 | -D]
+// blocks, dq_acc = the row-major fp32 accumulator.
 cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
                                  const CUtensorMap &tv, const CUtensorMap &tdo64,
-                                 const CUtensorMap &tdq, const float *vecs, void *dk, void *dv,
-                                 int BH, int N, float scale, int causal, int *dev_status,
+                                 const float *vecs, float *dq_acc, void *dk, void *dv, int BH,
+                                 int N, float scale, int causal, int *dev_status,
                                  cudaStream_t stream);
 
 int decode_max_parts(int max_num_blocks_per_seq);

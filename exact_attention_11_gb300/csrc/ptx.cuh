@@ -258,6 +258,38 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The same descriptor split in two 32-bit words.  The low word holds the
+// start address (>> 4, 14 bits) and the leading-dimension offset; adding a
+// byte offset >> 4 to it moves the start address (shared addresses stay below
+// 256 KB, so the field never carries).  The high word (stride offset 1024 B,
+// version, swizzle mode) is the same for every operand the kernels use.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+constexpr uint32_t kSdescHi1024 = (1024u >> 4) | (1u << 14) | (2u << 29);
+
+// mma_ss / mma_ts with descriptors given by their low words (high word
+// kSdescHi1024).  Cheaper to issue in unrolled loops: the per-MMA offsets are
+// 32-bit immediates.
+__device__ __forceinline__ void mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .b64 da, db;\n .reg .pred p;\n mov.b64 da, {%1, %5};\n mov.b64 db, {%2, %5};\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSdescHi1024)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .b64 db;\n .reg .pred p;\n mov.b64 db, {%2, %5};\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSdescHi1024)
+      : "memory");
+}
+
 // Instruction descriptor, kind::f16 with bf16 A and B and an fp32
 // accumulator; B is K-major or (b_mn_major) N-major, A is K-major or
 // (a_mn_major) M-major.
@@ -277,6 +309,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // Barrier among `count` threads of the CTA on named barrier `id` (1..15).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Atomic fp32 add in global memory (no return value).
+__device__ __forceinline__ void red_add_f32(float *addr, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
 }
 
 // Atomic fp32 add of four consecutive floats (16-byte aligned) in global memory.
