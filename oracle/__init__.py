@@ -62,11 +62,14 @@ def _bind(lib):
                                      ctypes.c_double, ctypes.c_int, _dp]
     lib.oracle_paged_decode.argtypes = [_dp, _dp, _dp, _ip, _ip, _dp, _dp] + [
         ctypes.c_long] * 7 + [ctypes.c_double, ctypes.c_int]
+    lib.oracle_paged_decode_gqa.argtypes = [_dp, _dp, _dp, _ip, _ip, _dp, _dp] + [
+        ctypes.c_long] * 8 + [ctypes.c_double, ctypes.c_int]
     lib.oracle_backward.argtypes = [_dp] * 7 + [ctypes.c_long] * 4 + [ctypes.c_double, ctypes.c_int,
                                                                      ctypes.c_int]
     lib.oracle_max_threads.argtypes = []
     for f in (lib.oracle_forward, lib.oracle_forward_rows, lib.oracle_probs_row,
-              lib.oracle_paged_decode, lib.oracle_backward, lib.oracle_max_threads):
+              lib.oracle_paged_decode, lib.oracle_paged_decode_gqa, lib.oracle_backward,
+              lib.oracle_max_threads):
         f.restype = ctypes.c_int
     return lib
 
@@ -203,19 +206,27 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                  nthreads: int = 0):
     """Single-query paged decode.  Returns (out [S,H,D], LSE [S,H]).
 
-    q [S,H,D]; k_cache [nb,H,D/x,bs,x]; v_cache [nb,H,D,bs];
-    block_tables int [S,max_blocks]; context_lens int [S]."""
+    q [S,H,D]; k_cache [nb,Hk,D/x,bs,x]; v_cache [nb,Hk,D,bs] with Hk dividing
+    H (Hk = H: one key/value head per query head; else query head h reads
+    key/value head h // (H // Hk)); block_tables int [S,max_blocks];
+    context_lens int [S]."""
     q, kc, vc = _f64(q), _f64(k_cache), _f64(v_cache)
     bt, cl = _i32(block_tables), _i32(context_lens)
     S, H, D = q.shape
     nb, Hk, Dx, bs, x = kc.shape
-    if Hk != H or Dx * x != D or vc.shape != (nb, H, D, bs) or bt.ndim != 2 or bt.shape[0] != S:
+    if (Hk <= 0 or H % Hk != 0 or Dx * x != D or vc.shape != (nb, Hk, D, bs) or bt.ndim != 2
+            or bt.shape[0] != S):
         raise ValueError("inconsistent paged-cache shapes")
     out = np.zeros((S, H, D))
     lse = np.zeros((S, H))
-    rc = _load().oracle_paged_decode(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt, _ip), _ptr(cl, _ip),
-                                     _ptr(out), _ptr(lse), S, H, D, bs, x, bt.shape[1], nb,
-                                     float(scale), int(nthreads))
+    if Hk == H:
+        rc = _load().oracle_paged_decode(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt, _ip),
+                                         _ptr(cl, _ip), _ptr(out), _ptr(lse), S, H, D, bs, x,
+                                         bt.shape[1], nb, float(scale), int(nthreads))
+    else:
+        rc = _load().oracle_paged_decode_gqa(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt, _ip),
+                                             _ptr(cl, _ip), _ptr(out), _ptr(lse), S, H, Hk, D,
+                                             bs, x, bt.shape[1], nb, float(scale), int(nthreads))
     if rc != 0:
-        raise ValueError("oracle_paged_decode rejected its arguments")
+        raise ValueError("oracle paged decode rejected its arguments")
     return out, lse

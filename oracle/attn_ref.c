@@ -167,25 +167,30 @@ int oracle_probs_row(const double *q, const double *k, long N, long d, long i,
     return 0;
 }
 
-/* Single-query paged decode.
+/* Single-query paged decode with grouped key/value heads.
  *   q            [num_seqs, num_heads, head_size]
- *   k_cache      [num_blocks, num_heads, head_size/x, block_size, x]
- *   v_cache      [num_blocks, num_heads, head_size, block_size]
+ *   k_cache      [num_blocks, num_kv_heads, head_size/x, block_size, x]
+ *   v_cache      [num_blocks, num_kv_heads, head_size, block_size]
  *   block_tables [num_seqs, max_blocks]  (logical block -> physical block)
  *   context_lens [num_seqs]
  *   out          [num_seqs, num_heads, head_size], lse [num_seqs, num_heads]
- * Token t of sequence s lives in physical block block_tables[s][t / block_size]
- * at offset t % block_size.  Element c of its key is
- *   k_cache[pb][h][c / x][t % block_size][c % x]
- * and element c of its value is v_cache[pb][h][c][t % block_size]. */
-int oracle_paged_decode(const double *q, const double *k_cache, const double *v_cache,
-                        const int *block_tables, const int *context_lens,
-                        double *out, double *lse, long num_seqs, long num_heads,
-                        long head_size, long block_size, long x, long max_blocks,
-                        long num_blocks, double scale, int nthreads)
+ * ("PagedAttention", data-sketchers.com, sections "Inputs", "Concepts",
+ * "Key", "Value".)  Token t of sequence s lives in physical block
+ * block_tables[s][t / block_size] at offset t % block_size.  Query head h
+ * reads key/value head kvh = h / (num_heads / num_kv_heads): the page indexes
+ * the caches by a kv_head_idx without showing how it is derived; consecutive
+ * query heads sharing one key/value head is the reading taken.  Element c of
+ * the key is k_cache[pb][kvh][c / x][t % block_size][c % x] and element c of
+ * the value is v_cache[pb][kvh][c][t % block_size]. */
+int oracle_paged_decode_gqa(const double *q, const double *k_cache, const double *v_cache,
+                            const int *block_tables, const int *context_lens,
+                            double *out, double *lse, long num_seqs, long num_heads,
+                            long num_kv_heads, long head_size, long block_size, long x,
+                            long max_blocks, long num_blocks, double scale, int nthreads)
 {
-    if (num_seqs < 0 || num_heads <= 0 || head_size <= 0 || block_size <= 0 ||
-        x <= 0 || head_size % x != 0 || max_blocks <= 0 || num_blocks <= 0)
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
+        head_size <= 0 || block_size <= 0 || x <= 0 || head_size % x != 0 || max_blocks <= 0 ||
+        num_blocks <= 0)
         return -1;
     for (long s = 0; s < num_seqs; ++s) {
         const long ctx = context_lens[s];
@@ -197,7 +202,8 @@ int oracle_paged_decode(const double *q, const double *k_cache, const double *v_
     }
     set_threads(nthreads);
     const long D = head_size;
-    const long kv_block_stride = num_heads * D * block_size;  /* same for K and V */
+    const long group = num_heads / num_kv_heads;
+    const long kv_block_stride = num_kv_heads * D * block_size;  /* same for K and V */
     const long kv_head_stride = D * block_size;
     int failed = 0;
 #pragma omp parallel
@@ -213,13 +219,14 @@ int oracle_paged_decode(const double *q, const double *k_cache, const double *v_
 #pragma omp for schedule(dynamic, 1)
             for (long t = 0; t < num_seqs * num_heads; ++t) {
                 const long s = t / num_heads, h = t % num_heads;
+                const long kvh = h / group;
                 const long ctx = context_lens[s];
                 /* Gather this (sequence, head)'s keys and values. */
                 for (long tok = 0; tok < ctx; ++tok) {
                     const long pb = block_tables[s * max_blocks + tok / block_size];
                     const long off = tok % block_size;
-                    const double *kb = k_cache + pb * kv_block_stride + h * kv_head_stride;
-                    const double *vb = v_cache + pb * kv_block_stride + h * kv_head_stride;
+                    const double *kb = k_cache + pb * kv_block_stride + kvh * kv_head_stride;
+                    const double *vb = v_cache + pb * kv_block_stride + kvh * kv_head_stride;
                     for (long c = 0; c < D; ++c) {
                         K[tok * D + c] = kb[((c / x) * block_size + off) * x + (c % x)];
                         V[tok * D + c] = vb[c * block_size + off];
@@ -232,6 +239,19 @@ int oracle_paged_decode(const double *q, const double *k_cache, const double *v_
         free(K); free(V); free(scores);
     }
     return failed ? -1 : 0;
+}
+
+/* Single-query paged decode with one key/value head per query head
+ * (num_kv_heads = num_heads): the caches are [num_blocks, num_heads, ...]. */
+int oracle_paged_decode(const double *q, const double *k_cache, const double *v_cache,
+                        const int *block_tables, const int *context_lens,
+                        double *out, double *lse, long num_seqs, long num_heads,
+                        long head_size, long block_size, long x, long max_blocks,
+                        long num_blocks, double scale, int nthreads)
+{
+    return oracle_paged_decode_gqa(q, k_cache, v_cache, block_tables, context_lens, out, lse,
+                                   num_seqs, num_heads, num_heads, head_size, block_size, x,
+                                   max_blocks, num_blocks, scale, nthreads);
 }
 
 /* Backward pass of the same attention: given dO = dLoss/dO, the gradients

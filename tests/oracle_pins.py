@@ -306,10 +306,53 @@ def check_decode_one_hot():
                 np.testing.assert_allclose(out[s, h], Vs[s][h, target], rtol=0, atol=1e-20)
 
 
+def check_gqa_decode_matches_replicated_heads():
+    """Grouped key/value heads ("PagedAttention", data-sketchers.com, section
+    "Inputs": the caches have a num_kv_heads axis): the decode with Hk key/value
+    heads equals the one-head-per-query decode on caches in which every key/value
+    head is repeated for its H/Hk consecutive query heads -- bit for bit, since the
+    gathers and sums are the same."""
+    for Hk, H in ((2, 8), (1, 4), (3, 3)):
+        r = _rng(31 + H)
+        S, D, bs, x, mb = 3, 16, 4, 8, 5
+        nb = S * mb + 2
+        tables = r.permutation(nb)[:S * mb].reshape(S, mb).astype(np.int32)
+        ctx = np.array([1, 9, mb * bs], dtype=np.int32)
+        q = r.standard_normal((S, H, D))
+        kc = r.standard_normal((nb, Hk, D // x, bs, x))
+        vc = r.standard_normal((nb, Hk, D, bs))
+        G = H // Hk
+        out_g, lse_g = oracle.paged_decode(q, kc, vc, tables, ctx, 0.3)
+        out_m, lse_m = oracle.paged_decode(q, np.repeat(kc, G, axis=1), np.repeat(vc, G, axis=1),
+                                           tables, ctx, 0.3)
+        np.testing.assert_array_equal(out_g, out_m)
+        np.testing.assert_array_equal(lse_g, lse_m)
+
+
+def check_gqa_decode_head_groups():
+    """Values constant per key/value head (head j holds j + 1 everywhere) make
+    every output row equal that constant whatever the probabilities, so query
+    head h must read key/value head h // (H / Hk)."""
+    S, H, Hk, D, bs, x, mb = 2, 6, 3, 8, 4, 8, 3
+    r = _rng(37)
+    nb = S * mb
+    tables = r.permutation(nb).reshape(S, mb).astype(np.int32)
+    ctx = np.array([5, 12], dtype=np.int32)
+    q = r.standard_normal((S, H, D))
+    kc = r.standard_normal((nb, Hk, D // x, bs, x))
+    vc = np.zeros((nb, Hk, D, bs))
+    for j in range(Hk):
+        vc[:, j] = j + 1.0
+    out, _ = oracle.paged_decode(q, kc, vc, tables, ctx, 0.5)
+    for h in range(H):
+        np.testing.assert_allclose(out[:, h], h // (H // Hk) + 1.0, rtol=0, atol=1e-12)
+
+
 ALL_CHECKS = [check_hand_examples, check_brute_force_tiny, check_library_sdpa,
               check_invariants, check_large_logits, check_online_recurrence,
               check_layout_fixture, check_decode_matches_gathered_forward,
-              check_decode_one_hot]
+              check_decode_one_hot, check_gqa_decode_matches_replicated_heads,
+              check_gqa_decode_head_groups]
 
 
 # --------------------------------------------------------------------------

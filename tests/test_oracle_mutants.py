@@ -31,6 +31,7 @@ MUTANTS = [
      "V[tok * D + c] = vb[off * D + c];"),
     ("block_table_index_mod", "block_tables[s * max_blocks + tok / block_size]",
      "block_tables[s * max_blocks + tok % block_size]"),
+    ("gqa_heads_interleaved", "const long kvh = h / group;", "const long kvh = h % num_kv_heads;"),
     ("bwd_D_sign", "const double ds = p[j] * (dp[j] - D);", "const double ds = p[j] * (dp[j] + D);"),
     ("bwd_dq_no_scale", "dqh[i * d + c] += scale * ds * kh[j * d + c];",
      "dqh[i * d + c] += ds * kh[j * d + c];"),
