@@ -15,6 +15,8 @@ Printed JSON line (rank 0):
   roofline       the forward (dominant kernel) against the measured bf16 peak
   backward       fa_backward (dQ, dK, dV) of the forward workload, TFLOP/s with
                  FLOPs = 2.5 x the forward's, and its own roofline
+  decode_gqa     fa_paged_decode_gqa on the decode's sequences with 8 key/value
+                 heads for the 32 query heads, GB/s and HBM roofline
   e2e            the same metrics through the C ABI with pinned host buffers,
                  host<->device copies inside the timed region
   cpu_baseline   the float64 CPU oracle on the host cores, on a sample
@@ -39,6 +41,8 @@ FWD = dict(B=2, H=16, N=4096, d=128, causal=True, seed=3)
 # The long-sequence forward, timed separately and reported nested.
 FWD_LONG = dict(B=1, H=8, N=16384, d=128, causal=True, seed=4, amp=0.5)
 DEC = dict(num_seqs=64, num_heads=32, head_size=128, block_size=16, max_ctx=4096, seed=5)
+# Grouped key/value heads: the same sequences and contexts, 8 cached heads.
+DEC_GQA = dict(DEC, num_kv_heads=8)
 L2_FLUSH_BYTES = 512 << 20
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "fwd attention TFLOPS & % of BF16 tensor peak; paged-decode HBM GB/s"
@@ -307,6 +311,40 @@ def gpu_arm(args):
     bwd_ms = sum(e[0].elapsed_time(e[1]) for e in bev) / kb
     del g_out, gq, gk, gv, bws
 
+    # The grouped-head decode (4 query heads per cached head), timed the same
+    # way, reported as "decode_gqa".
+    dg = inputs.decode_inputs(DEC_GQA["num_seqs"], DEC_GQA["num_heads"], DEC_GQA["head_size"],
+                              DEC_GQA["block_size"], DEC_GQA["max_ctx"],
+                              seed=DEC_GQA["seed"] + 1000 * rank, device=dev,
+                              num_kv_heads=DEC_GQA["num_kv_heads"])
+    gout = torch.empty_like(dg.q)
+    Sg, Hg, Dg = dg.q.shape
+
+    def run_gqa():
+        fa.fa_paged_decode_gqa(dg.q.data_ptr(), dg.k_cache.data_ptr(), dg.v_cache.data_ptr(),
+                               dg.block_tables.data_ptr(), dg.context_lens.data_ptr(),
+                               gout.data_ptr(), Sg, Hg, dg.num_kv_heads, Dg, dg.block_size,
+                               dg.max_blocks, dg.scale, sptr)
+
+    gctx = dg.context_lens.to(torch.int64)
+    g_blk = int(((gctx + dg.block_size - 1) // dg.block_size).sum())
+    gqa_bytes = (dg.kv_bytes_read() + dg.q.numel() * 2 + gout.numel() * 2
+                 + g_blk * 4 + Sg * 4)
+    kg = max(3, min(K // 4, 100))
+    gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(kg)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush.zero_()
+            run_gqa()
+        for i in range(kg):
+            flush.zero_()
+            gev[i][0].record(stream)
+            run_gqa()
+            gev[i][1].record(stream)
+    stream.synchronize()
+    gqa_ms = sum(e[0].elapsed_time(e[1]) for e in gev) / kg
+    del dg, gout
+
     # End to end through the C ABI with pinned host buffers.
     hq, hk, hv = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3))
     for h, t in zip((hq, hk, hv), (q, k, v)):
@@ -355,9 +393,9 @@ def gpu_arm(args):
     d2h = o.numel() * 2 + lse.numel() * 4 + out.numel() * 2
 
     if ws > 1:
-        (fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms, bwd_ms), status = \
-            reduce_over_ranks([fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms, bwd_ms],
-                              status, dev)
+        (fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms, bwd_ms, gqa_ms), status = \
+            reduce_over_ranks([fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms, bwd_ms,
+                               gqa_ms], status, dev)
 
     tflops = weak_scaling_rate(flops, ws, fwd_ms, 1e12)
     per_gpu_tflops = weak_scaling_rate(flops, 1, fwd_ms, 1e12)
@@ -421,6 +459,18 @@ def gpu_arm(args):
                          "traffic": recorded_traffic("paged_decode_kernel"),
                          "peak_kind": peak_kind},
         },
+        "decode_gqa": {
+            "workload": "fa_paged_decode_gqa bf16 64 seqs x 32 query heads x 8 key/value heads x "
+                        "head 128, block 16, ctx U[1,4096] (the decode's contexts)",
+            "value": round(weak_scaling_rate(gqa_bytes, ws, gqa_ms, 1e9), 1), "unit": "GB/s",
+            "ms": round(gqa_ms, 4), "bytes_per_launch": gqa_bytes,
+            "roofline": {"bound": "hbm",
+                         "achieved": round(weak_scaling_rate(gqa_bytes, 1, gqa_ms, 1e9), 1),
+                         "peak": peak_h, "unit": "GB/s",
+                         "frac": round(weak_scaling_rate(gqa_bytes, 1, gqa_ms, 1e9) / peak_h, 4),
+                         "traffic": recorded_traffic("paged_decode_gqa_kernel<4>"),
+                         "peak_kind": peak_kind},
+        },
         "roofline": {"bound": "tensor", "achieved": round(per_gpu_tflops, 2), "peak": peak_t,
                      "unit": "TFLOP/s", "frac": round(per_gpu_tflops / peak_t, 4),
                      "traffic": recorded_traffic("fwd_bf16_tc_kernel<128>"),
@@ -432,7 +482,7 @@ def gpu_arm(args):
                 "note": "KV cache resident (serving state); q, K, V, q_decode, block table, "
                         "context lens copied in and O, LSE, out copied back every step"},
         # library kernels inside timed regions (a backward is three launches)
-        "gpu_launches": 2 * K + kl + 3 * kb + 2 * ke,
+        "gpu_launches": 2 * K + kl + 3 * kb + kg + 2 * ke,
         "clocks": clk,
         "device_status": status,
         "wall_s": round(wall, 3),

@@ -17,7 +17,8 @@ import os
 import threading
 
 __all__ = ["fa_forward", "fa_forward_fp32", "fa_paged_decode", "fa_paged_decode_noalloc",
-           "fa_backward", "fa_backward_workspace_bytes", "backward", "fa_status_string",
+           "fa_backward", "fa_backward_workspace_bytes", "backward", "fa_paged_decode_gqa",
+           "fa_status_string",
            "fa_device_status", "fa_release", "forward", "paged_decode", "FattnError",
            "library_path", "load"]
 
@@ -49,6 +50,7 @@ EXPORTS = {
     "fa_forward_fp32": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_paged_decode": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_paged_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
+    "fa_paged_decode_gqa": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_backward_workspace_bytes": ([_i, _i, _i, _i], ctypes.c_ulonglong),
     "fa_backward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp,
                      ctypes.c_ulonglong, _vp], _i),
@@ -101,6 +103,14 @@ def fa_paged_decode(q, k_cache, v_cache, block_tables, context_lens, out, num_se
     return _check("fa_paged_decode", load().fa_paged_decode(
         q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, num_heads, head_size,
         block_size, max_num_blocks_per_seq, scale, stream))
+
+
+def fa_paged_decode_gqa(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs,
+                        num_heads, num_kv_heads, head_size, block_size, max_num_blocks_per_seq,
+                        scale, stream) -> int:
+    return _check("fa_paged_decode_gqa", load().fa_paged_decode_gqa(
+        q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, num_heads, num_kv_heads,
+        head_size, block_size, max_num_blocks_per_seq, scale, stream))
 
 
 def fa_paged_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs,
@@ -216,11 +226,13 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, workspace=None):
 
 
 def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale=None, out=None):
-    """Single-query paged decode on CUDA tensors in the layouts of fattn.h."""
+    """Single-query paged decode on CUDA tensors in the layouts of fattn.h.
+    The caches' second axis is the key/value head count Hk; Hk < H selects
+    the grouped-head decode (fa_paged_decode_gqa)."""
     import torch
     S, H, D = q.shape
     nb, Hk, Dx, bs, x = k_cache.shape
-    if Hk != H or Dx * x != D or tuple(v_cache.shape) != (nb, H, D, bs):
+    if Hk <= 0 or H % Hk != 0 or Dx * x != D or tuple(v_cache.shape) != (nb, Hk, D, bs):
         raise ValueError("inconsistent cache shapes")
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise ValueError("block_tables and context_lens must be int32")
@@ -231,7 +243,12 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale=None, ou
         scale = D ** -0.5
     if out is None:
         out = torch.empty_like(q)
-    fa_paged_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                    _ptr(context_lens), _ptr(out), S, H, D, bs, block_tables.shape[1],
-                    float(scale), _stream(q))
+    if Hk == H:
+        fa_paged_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                        _ptr(context_lens), _ptr(out), S, H, D, bs, block_tables.shape[1],
+                        float(scale), _stream(q))
+    else:
+        fa_paged_decode_gqa(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                            _ptr(context_lens), _ptr(out), S, H, Hk, D, bs,
+                            block_tables.shape[1], float(scale), _stream(q))
     return out

@@ -125,6 +125,53 @@ int check_forward_args(const void *q, const void *k, const void *v, const void *
   return FA_OK;
 }
 
+// Checks shared by the decode entry points; grows the library-owned split-K
+// workspace and counters for (num_seqs, num_heads, max_num_blocks_per_seq).
+int decode_prepare(const void *q, const void *k_cache, const void *v_cache,
+                   const int *block_tables, const int *context_lens, const void *out,
+                   int num_seqs, int num_heads, int head_size, int block_size,
+                   int max_num_blocks_per_seq, float scale, float **ws, int **counters,
+                   int **status) {
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return FA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || num_heads <= 0 || max_num_blocks_per_seq <= 0) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (head_size != fattn::kDecodeHeadSize || block_size != fattn::kDecodeBlockSize)
+    return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return FA_ERR_ALIGNMENT;
+  if (num_heads > 65535 || num_seqs > 65535) return FA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return FA_OK;
+  const int max_parts = fattn::decode_max_parts(max_num_blocks_per_seq);
+  const size_t ws_bytes = fattn::decode_workspace_bytes(num_seqs, num_heads, max_parts);
+  const size_t n_counters = (size_t)num_seqs * num_heads;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0, rc;
+  if ((rc = current_device(&dev)) != FA_OK) return rc;
+  DeviceState &st = g_dev[dev];
+  if (st.decode_ws_bytes < ws_bytes) {
+    if (st.decode_ws) cudaFree(st.decode_ws);  // synchronises: no launch still uses it
+    st.decode_ws = nullptr;
+    st.decode_ws_bytes = 0;
+    if (cudaMalloc(&st.decode_ws, ws_bytes) != cudaSuccess) return FA_ERR_NO_MEMORY;
+    st.decode_ws_bytes = ws_bytes;
+  }
+  if (st.decode_counter_count < n_counters) {
+    if (st.decode_counters) cudaFree(st.decode_counters);
+    st.decode_counters = nullptr;
+    st.decode_counter_count = 0;
+    if (cudaMalloc(&st.decode_counters, n_counters * sizeof(int)) != cudaSuccess)
+      return FA_ERR_NO_MEMORY;
+    if (cudaMemset(st.decode_counters, 0, n_counters * sizeof(int)) != cudaSuccess)
+      return FA_ERR_CUDA;
+    st.decode_counter_count = n_counters;
+  }
+  *ws = st.decode_ws;
+  *counters = st.decode_counters;
+  *status = st.status;
+  return FA_OK;
+}
+
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 }  // namespace
@@ -236,50 +283,42 @@ int fa_paged_decode(const void *q, const void *k_cache, const void *v_cache,
                     const int *block_tables, const int *context_lens, void *out, int num_seqs,
                     int num_heads, int head_size, int block_size, int max_num_blocks_per_seq,
                     float scale, fa_stream_t stream) {
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
-    return FA_ERR_INVALID_ARG;
-  if (num_seqs < 0 || num_heads <= 0 || max_num_blocks_per_seq <= 0) return FA_ERR_INVALID_ARG;
-  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (head_size != fattn::kDecodeHeadSize || block_size != fattn::kDecodeBlockSize)
-    return FA_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-    return FA_ERR_ALIGNMENT;
-  if (num_heads > 65535 || num_seqs > 65535) return FA_ERR_UNSUPPORTED;
-  if (num_seqs == 0) return FA_OK;
-  const int max_parts = fattn::decode_max_parts(max_num_blocks_per_seq);
-  const size_t ws_bytes = fattn::decode_workspace_bytes(num_seqs, num_heads, max_parts);
-  const size_t n_counters = (size_t)num_seqs * num_heads;
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float *ws = nullptr;
-  int *counters = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_mu);
-    int dev = 0, rc;
-    if ((rc = current_device(&dev)) != FA_OK) return rc;
-    DeviceState &st = g_dev[dev];
-    if (st.decode_ws_bytes < ws_bytes) {
-      if (st.decode_ws) cudaFree(st.decode_ws);  // synchronises: no launch still uses it
-      st.decode_ws = nullptr;
-      st.decode_ws_bytes = 0;
-      if (cudaMalloc(&st.decode_ws, ws_bytes) != cudaSuccess) return FA_ERR_NO_MEMORY;
-      st.decode_ws_bytes = ws_bytes;
-    }
-    if (st.decode_counter_count < n_counters) {
-      if (st.decode_counters) cudaFree(st.decode_counters);
-      st.decode_counters = nullptr;
-      st.decode_counter_count = 0;
-      if (cudaMalloc(&st.decode_counters, n_counters * sizeof(int)) != cudaSuccess)
-        return FA_ERR_NO_MEMORY;
-      if (cudaMemset(st.decode_counters, 0, n_counters * sizeof(int)) != cudaSuccess)
-        return FA_ERR_CUDA;
-      st.decode_counter_count = n_counters;
-    }
-    ws = st.decode_ws;
-    counters = st.decode_counters;
-  }
+  int *counters = nullptr, *status = nullptr;
+  const int rc = decode_prepare(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs,
+                                num_heads, head_size, block_size, max_num_blocks_per_seq, scale,
+                                &ws, &counters, &status);
+  if (rc != FA_OK || num_seqs == 0) return rc;
   return cuda_status(fattn::launch_paged_decode(q, k_cache, v_cache, block_tables, context_lens,
                                                 out, num_seqs, num_heads, max_num_blocks_per_seq,
-                                                scale, ws, counters, s));
+                                                scale, ws, counters,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_paged_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
+                        const int *block_tables, const int *context_lens, void *out,
+                        int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                        int block_size, int max_num_blocks_per_seq, float scale,
+                        fa_stream_t stream) {
+  if (num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads != 0)
+    return FA_ERR_INVALID_ARG;
+  const int group = num_heads / num_kv_heads;
+  if (group > 1 && !fattn::decode_gqa_group_supported(group)) return FA_ERR_UNSUPPORTED;
+  float *ws = nullptr;
+  int *counters = nullptr, *status = nullptr;
+  const int rc = decode_prepare(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs,
+                                num_heads, head_size, block_size, max_num_blocks_per_seq, scale,
+                                &ws, &counters, &status);
+  if (rc != FA_OK || num_seqs == 0) return rc;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (group == 1)
+    return cuda_status(fattn::launch_paged_decode(q, k_cache, v_cache, block_tables,
+                                                  context_lens, out, num_seqs, num_heads,
+                                                  max_num_blocks_per_seq, scale, ws, counters, s));
+  return cuda_status(fattn::launch_paged_decode_gqa(q, k_cache, v_cache, block_tables,
+                                                    context_lens, out, num_seqs, num_heads,
+                                                    num_kv_heads, max_num_blocks_per_seq, scale,
+                                                    ws, counters, status, s));
 }
 
 int fa_device_status(void) {

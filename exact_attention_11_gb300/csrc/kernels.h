@@ -50,6 +50,15 @@ cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
                                  cudaStream_t stream);
 
 int decode_max_parts(int max_num_blocks_per_seq);
+// Grouped key/value heads (decode_gqa.cu): group = num_heads / num_kv_heads
+// must be 2 or a multiple of 4.  Same workspace and counters as the one-head
+// decode (counters indexed per (sequence, query-head group of the CTA)).
+bool decode_gqa_group_supported(int group);
+cudaError_t launch_paged_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
+                                    const int *block_tables, const int *context_lens, void *out,
+                                    int num_seqs, int num_heads, int num_kv_heads, int max_blocks,
+                                    float scale, float *workspace, int *counters,
+                                    int *dev_status, cudaStream_t stream);
 // Split-K workspace: per (sequence, head, partition) an unnormalised output
 // row and its (max, sum) pair, in fp32.  `counters` holds one int per
 // (sequence, head); it must be all zero before the first launch and every

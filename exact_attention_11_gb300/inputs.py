@@ -58,8 +58,8 @@ def sample_rows(N: int, count: int, seed: int):
 @dataclass
 class DecodeInputs:
     q: torch.Tensor             # [S, H, D]
-    k_cache: torch.Tensor       # [nb, H, D/x, bs, x]
-    v_cache: torch.Tensor       # [nb, H, D, bs]
+    k_cache: torch.Tensor       # [nb, Hk, D/x, bs, x]  (Hk = key/value heads)
+    v_cache: torch.Tensor       # [nb, Hk, D, bs]
     block_tables: torch.Tensor  # int32 [S, max_blocks]
     context_lens: torch.Tensor  # int32 [S]
     block_size: int
@@ -69,20 +69,28 @@ class DecodeInputs:
     def max_blocks(self) -> int:
         return int(self.block_tables.shape[1])
 
+    @property
+    def num_kv_heads(self) -> int:
+        return int(self.k_cache.shape[1])
+
     def kv_bytes_read(self) -> int:
         """Algorithmic K and V bytes one decode reads: every context token's key
-        and value, for every head."""
+        and value, once for every key/value head."""
         S, H, D = self.q.shape
         es = self.q.element_size()
-        return int(self.context_lens.to(torch.int64).sum().item()) * H * D * es * 2
+        return int(self.context_lens.to(torch.int64).sum().item()) * self.num_kv_heads * D * es * 2
 
 
 def decode_inputs(num_seqs: int, num_heads: int, head_size: int, block_size: int,
                   max_ctx: int, dtype=torch.bfloat16, seed: int = 0, device="cpu",
-                  min_ctx: int = 1, scale: float | None = None) -> DecodeInputs:
+                  min_ctx: int = 1, scale: float | None = None,
+                  num_kv_heads: int | None = None) -> DecodeInputs:
     """Paged-decode inputs.  The caches are drawn on ``device`` (a seeded CUDA
     generator when it is a GPU, in chunks, so multi-GiB caches never pass
-    through host memory); the small tensors always come from a CPU generator."""
+    through host memory); the small tensors always come from a CPU generator.
+    ``num_kv_heads`` (default num_heads) sets the caches' key/value head axis."""
+    if num_kv_heads is None:
+        num_kv_heads = num_heads
     es = torch.tensor([], dtype=dtype).element_size()
     x = 16 // es
     assert head_size % x == 0
@@ -95,9 +103,10 @@ def decode_inputs(num_seqs: int, num_heads: int, head_size: int, block_size: int
     block_tables = torch.randperm(nb, generator=g).view(num_seqs, max_blocks).to(torch.int32)
     dev = torch.device(device)
     gdev = torch.Generator(device=dev).manual_seed(seed + 1000003)
-    k_cache = torch.empty((nb, num_heads, head_size // x, block_size, x), dtype=dtype, device=dev)
-    v_cache = torch.empty((nb, num_heads, head_size, block_size), dtype=dtype, device=dev)
-    chunk = max(1, (1 << 26) // (num_heads * head_size * block_size))  # blocks per chunk
+    k_cache = torch.empty((nb, num_kv_heads, head_size // x, block_size, x), dtype=dtype,
+                          device=dev)
+    v_cache = torch.empty((nb, num_kv_heads, head_size, block_size), dtype=dtype, device=dev)
+    chunk = max(1, (1 << 26) // (num_kv_heads * head_size * block_size))  # blocks per chunk
     for cache in (k_cache, v_cache):
         flat = cache.view(nb, -1)
         for b0 in range(0, nb, chunk):

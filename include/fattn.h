@@ -165,6 +165,31 @@ int fa_paged_decode(const void *q, const void *k_cache, const void *v_cache,
                     int max_num_blocks_per_seq, float scale, fa_stream_t stream);
 
 /*
+ * fa_paged_decode_gqa -- fa_paged_decode with grouped key/value heads:
+ * num_heads query heads share num_kv_heads cached key/value heads.
+ *
+ * The caches carry a key/value head axis of num_kv_heads ("PagedAttention",
+ * data-sketchers.com, section "Inputs": k_cache [num_blocks, num_kv_heads,
+ * head_size/x, block_size, x], v_cache [num_blocks, num_kv_heads, head_size,
+ * block_size]; section "Key" offsets the key pointer by kv_head_idx).  Query
+ * head h attends with key/value head h / (num_heads / num_kv_heads), i.e.
+ * consecutive query heads share one cached head (num_kv_heads = 1 is
+ * multi-query attention).  q and out are [num_seqs, num_heads, head_size].
+ * Each cached block is read once for up to four query heads of its group.
+ *
+ * Arguments and errors as for fa_paged_decode, plus: FA_ERR_INVALID_ARG when
+ * num_kv_heads <= 0 or does not divide num_heads; FA_ERR_UNSUPPORTED when the
+ * group size num_heads / num_kv_heads is not 1, 2 or a multiple of 4.
+ * Group size 1 is exactly fa_paged_decode.  Shares fa_paged_decode's
+ * library-owned workspace.
+ */
+int fa_paged_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
+                        const int *block_tables, const int *context_lens, void *out,
+                        int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                        int block_size, int max_num_blocks_per_seq, float scale,
+                        fa_stream_t stream);
+
+/*
  * fa_paged_decode_noalloc -- fa_paged_decode for callers that cannot allocate
  * device memory during a call.  The attention pages have no counterpart to
  * this entry point; it exists for deployment reasons only.

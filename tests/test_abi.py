@@ -75,6 +75,23 @@ def test_forward_argument_checks(lib, args, expect):
 ])
 def test_decode_argument_checks(lib, args, expect):
     assert lib.fa_paged_decode(*args, None) == expect
+    # the grouped-head entry point with one key/value head per query head
+    S, H = args[6], args[7]
+    gargs = args[:8] + (H,) + args[8:]
+    assert lib.fa_paged_decode_gqa(*gargs, None) == expect
+
+
+@pytest.mark.parametrize("H,Hk,expect", [
+    (8, 0, -1),     # no key/value heads
+    (8, 3, -1),     # does not divide
+    (12, 4, -2),    # group of 3: not built
+    (24, 4, -2),    # group of 6: not built
+    (8, 4, 0),      # group of 2: valid (no sequences: no-op)
+    (32, 4, 0),     # group of 8
+    (64, 1, 0),     # multi-query
+])
+def test_gqa_decode_group_checks(lib, H, Hk, expect):
+    assert lib.fa_paged_decode_gqa(P, P, P, P, P, P, 0, H, Hk, 128, 16, 4, 0.1, None) == expect
 
 
 W = 1 << 20  # a workspace size larger than any case below needs
