@@ -22,7 +22,7 @@
 // key/value head, sub-group) merges the partitions of its query heads.
 // With GC heads the arithmetic per block is GC times the one-head kernel's,
 // so a warp cannot hide the load latency behind a single block's math: each
-// warp keeps a ring of kStages blocks in shared memory, filled by 4 KB bulk
+// warp keeps a ring of kStages blocks in shared memory (three CTAs per SM), filled by 4 KB bulk
 // copies (TMA engine) that complete on an mbarrier, so the next blocks'
 // loads overlap this block's math.
 #include <cuda_runtime.h>
@@ -41,42 +41,16 @@ constexpr int kBlk = kDecodeBlockSize;    // 16 tokens per cache block
 constexpr int kX = 8;                     // bf16 per 16-byte vector
 constexpr int kPartBlocks = kDecodePartitionTokens / kBlk;  // 32
 constexpr int kWarps = 4;
-constexpr int kStages = 3;                          // blocks in flight per warp
+constexpr int kStages = 2;                          // blocks in flight per warp
 constexpr int kSlice = kHead * kBlk * 2;            // bytes of one (block, head) slice: 4 KB
 constexpr int kStageBytes = 2 * kSlice;             // K and V
-constexpr int kRingBytes = kWarps * kStages * kStageBytes;   // 96 KB dynamic shared memory
+constexpr int kRingBytes = kWarps * kStages * kStageBytes;   // 64 KB dynamic shared memory
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// q8 . (8 bf16 in kv), with q8 = two float4 from shared memory; the same
-// evaluation order as the one-head kernel's dot product.
-__device__ __forceinline__ float dot8s(const float4 a, const float4 b, uint4 kv) {
-  float acc = a.x * bf_lo(kv.x);
-  acc = fmaf(a.y, bf_hi(kv.x), acc);
-  acc = fmaf(a.z, bf_lo(kv.y), acc);
-  acc = fmaf(a.w, bf_hi(kv.y), acc);
-  acc = fmaf(b.x, bf_lo(kv.z), acc);
-  acc = fmaf(b.y, bf_hi(kv.z), acc);
-  acc = fmaf(b.z, bf_lo(kv.w), acc);
-  acc = fmaf(b.w, bf_hi(kv.w), acc);
-  return acc;
-}
-
-__device__ __forceinline__ float fma8(const float *p8, uint4 vv, float acc) {
-  acc = fmaf(p8[0], bf_lo(vv.x), acc);
-  acc = fmaf(p8[1], bf_hi(vv.x), acc);
-  acc = fmaf(p8[2], bf_lo(vv.y), acc);
-  acc = fmaf(p8[3], bf_hi(vv.y), acc);
-  acc = fmaf(p8[4], bf_lo(vv.z), acc);
-  acc = fmaf(p8[5], bf_hi(vv.z), acc);
-  acc = fmaf(p8[6], bf_lo(vv.w), acc);
-  acc = fmaf(p8[7], bf_hi(vv.w), acc);
-  return acc;
-}
-
 template <int G>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 3)
     paged_decode_gqa_kernel(const __nv_bfloat16 *__restrict__ q,
                             const __nv_bfloat16 *__restrict__ k_cache,
                             const __nv_bfloat16 *__restrict__ v_cache,
@@ -172,26 +146,29 @@ __global__ void __launch_bounds__(kWarps * 32)
                                          &s_abort)))) break;
     const uint8_t *kb = my_ring + st * kStageBytes;
     const uint8_t *vb = kb + kSlice;
-    uint4 kv[8], vv[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      kv[i] = *reinterpret_cast<const uint4 *>(kb + (((2 * i + kpar) * kBlk + ktok) * kX) * 2);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      vv[j] = *reinterpret_cast<const uint4 *>(vb + ((vrow + 16 * j) * kBlk + 8 * vhalf) * 2);
-    // The stage is in registers: refill it with block k + kStages.
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0 && k + kStages < n_mine) issue(k + kStages);
     const bool tail = b * kBlk + ktok >= ctx;   // this lane's token is past the context
 
+    // Scores: for each head, this lane's token against its 8 key chunks, read
+    // from the ring as needed (the one-head kernel's order: an 8-term chain
+    // per 16-byte chunk, chunks summed in turn).
+    float alpha[G], p8[G][8];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       float t = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
+        const uint4 kv = *reinterpret_cast<const uint4 *>(kb + (((2 * i + kpar) * kBlk + ktok) * kX) * 2);
         const float4 *q4 = reinterpret_cast<const float4 *>(&sq[g][(2 * i + kpar) * kX]);
-        t += dot8s(q4[0], q4[1], kv[i]);
+        const float4 a = q4[0], c = q4[1];
+        float d8 = a.x * bf_lo(kv.x);
+        d8 = fmaf(a.y, bf_hi(kv.x), d8);
+        d8 = fmaf(a.z, bf_lo(kv.y), d8);
+        d8 = fmaf(a.w, bf_hi(kv.y), d8);
+        d8 = fmaf(c.x, bf_lo(kv.z), d8);
+        d8 = fmaf(c.y, bf_hi(kv.z), d8);
+        d8 = fmaf(c.z, bf_lo(kv.w), d8);
+        d8 = fmaf(c.w, bf_hi(kv.w), d8);
+        t += d8;
       }
       t += __shfl_xor_sync(~0u, t, 16);
       if (tail) t = -INFINITY;
@@ -199,19 +176,34 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
       for (int off = 8; off > 0; off >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(~0u, bmax, off));
       const float m_new = fmaxf(m[g], bmax);       // eq. (2); finite: token b*16 < ctx
-      const float alpha = ex2_approx(m[g] - m_new);  // 0 on the first block
+      alpha[g] = ex2_approx(m[g] - m_new);         // 0 on the first block
       const float p = ex2_approx(t - m_new);
       float psum = p;
 #pragma unroll
       for (int off = 8; off > 0; off >>= 1) psum += __shfl_xor_sync(~0u, psum, off);
-      l[g] = l[g] * alpha + psum;                  // eq. (3)
+      l[g] = l[g] * alpha[g] + psum;               // eq. (3)
       m[g] = m_new;
-      float p8[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) p8[e] = __shfl_sync(~0u, p, 8 * vhalf + e);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[g][j] = fma8(p8, vv[j], acc[g][j] * alpha);  // eq. (4)
+      for (int e = 0; e < 8; ++e) p8[g][e] = __shfl_sync(~0u, p, 8 * vhalf + e);
     }
+    // Values: each 16-byte chunk read and widened once, used by all heads (eq. (4)).
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 vv = *reinterpret_cast<const uint4 *>(vb + ((vrow + 16 * j) * kBlk + 8 * vhalf) * 2);
+      const float v8[8] = {bf_lo(vv.x), bf_hi(vv.x), bf_lo(vv.y), bf_hi(vv.y),
+                           bf_lo(vv.z), bf_hi(vv.z), bf_lo(vv.w), bf_hi(vv.w)};
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float a = acc[g][j] * alpha[g];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a = fmaf(p8[g][e], v8[e], a);
+        acc[g][j] = a;
+      }
+    }
+    // The stage has been read: refill it with block k + kStages.
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && k + kStages < n_mine) issue(k + kStages);
   }
   if (!ok) {
     // A copy did not arrive in time: wait (bounded) for the ones in flight,
