@@ -62,11 +62,11 @@ constexpr int BM = 128;             // query rows per tile (MMA M)
 constexpr int BN = 128;             // keys per tile (MMA N of QK^T, K of PV)
 constexpr int kThreads = 384;       // 12 warps = 3 warpgroups
 // Register split (setmaxnreg): the launch gives every thread 168 registers
-// (65536 / 384, rounded to 8); the producer warpgroup drops to 72 and the two
-// softmax warpgroups rise to 216, so each SM sub-partition, which hosts one
-// warp of every warpgroup, needs 72 + 216 + 216 = 3 * 168 registers per lane.
+// (65536 / 384, rounded to 8); the producer warpgroup drops to 88 and the two
+// softmax warpgroups rise to 208, so each SM sub-partition, which hosts one
+// warp of every warpgroup, needs 88 + 208 + 208 = 3 * 168 registers per lane.
 // The build checks that ptxas gives this kernel exactly 168 at launch.
-constexpr uint32_t kRegsProducer = 72, kRegsSoftmax = 216;
+constexpr uint32_t kRegsProducer = 88, kRegsSoftmax = 208;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -89,11 +89,13 @@ struct Cfg {
 
 // Barrier slots (8 bytes each).
 enum : int {
-  kBarQFull = 0,
-  kBarQEmpty = 1,
+  kBarQFullA = 0,      // query tile A of the current item
+  kBarQEmptyA = 1,
   kBarSFull = 2,       // +tile (A, B)
   kBarPReady = 4,      // +2 * tile + half: the first / second 64 columns of P
   kBarODone = 8,       // +tile
+  kBarQFullB = 10,     // query tile B
+  kBarQEmptyB = 11,
   kBarDrain = 12,
   kBarItemFull = 13,   // +ring slot (2)
   kBarItemEmpty = 32,  // +ring slot (2)
@@ -172,8 +174,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarQEmpty), 1);
+    mbar_init(bar(kBarQFullA), 1);
+    mbar_init(bar(kBarQEmptyA), 1);
+    mbar_init(bar(kBarQFullB), 1);
+    mbar_init(bar(kBarQEmptyB), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(kBarSFull + t), 1);
       mbar_init(bar(kBarPReady + 2 * t), 4);      // one arrival per softmax warp
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int it = 0, kv = 0, nk = 0, nv = 0, nq = 0;
+      int it = 0, kv = 0, nk = 0, nv = 0, nqa = 0, nqb = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
         // Claim the next item and publish it to the other roles.
@@ -224,14 +228,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w >= n_items) break;
         int q0, bh, n_a, n_b;
         sch.decode(w, q0, bh, n_a, n_b);
-        if (!(ok = mbar_wait(bar(kBarQEmpty), (it & 1) ^ 1, abort_flag))) break;
-        mbar_arrive_expect_tx(bar(kBarQFull), 2 * C::kTileBytes);
-        for (int t = 0; t < 2; ++t)
+        // Query tile t of this item, once the previous item's last QK_t has
+        // read the buffer.  Tile A goes first: the MMA warp starts it during
+        // the previous item's last step.  Tile B follows the first key tile.
+        auto load_q = [&](int t) -> bool {
+          if (!mbar_wait(bar(t ? kBarQEmptyB : kBarQEmptyA), (it & 1) ^ 1, abort_flag))
+            return false;
+          const uint32_t full = bar(t ? kBarQFullB : kBarQFullA);
+          mbar_arrive_expect_tx(full, C::kTileBytes);
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(s_base + C::kQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, b * 64,
-                        q0 + t * BM, bh, bar(kBarQFull));
-        ++nq;
+                        q0 + t * BM, bh, full);
+          return true;
+        };
+        if (!(ok = load_q(0))) break;
+        ++nqa;
         if (static_cast<int>(blockIdx.x) == fault_cta) {
+          if ((ok = load_q(1))) ++nqb;
           // Failure-path test: stop here, as if the key-tile copies were lost;
           // the MMA warp's bounded wait for them runs out.
           ok = false;
@@ -246,6 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(s_base + C::kK0 + st * C::kTileBytes + b * C::kBoxBytes, &tm_k, b * 64,
                         j * BN, bh, bar(kBarKFull + st));
           nk = kv + 1;
+          if (j == 0) {
+            if (!(ok = load_q(1))) break;
+            ++nqb;
+          }
           if (!(ok = mbar_wait(bar(kBarVEmpty + st), ph ^ 1, abort_flag))) break;
           mbar_arrive_expect_tx(bar(kBarVFull + st), C::kTileBytes);
           for (int b = 0; b < C::kBoxes; ++b)
@@ -257,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         // Let the copies in flight land before the CTA exits.
-        if (nq > 0) drain_wait(bar(kBarQFull), (nq - 1) & 1);
+        if (nqa > 0) drain_wait(bar(kBarQFullA), (nqa - 1) & 1);
+        if (nqb > 0) drain_wait(bar(kBarQFullB), (nqb - 1) & 1);
         for (int i = (nk > S ? nk - S : 0); i < nk; ++i)
           drain_wait(bar(kBarKFull + i % S), (i / S) & 1);
         for (int i = (nv > S ? nv - S : 0); i < nv; ++i)
@@ -270,29 +288,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Shared-memory descriptors are built once; moving an operand by `off`
       // bytes adds off >> 4 to the start-address field, which cannot carry
       // out of its 14 bits for addresses inside the 228 KB shared window.
-      const uint64_t dq = smem_desc_sw128(s_base + C::kQ, 16, 1024);
-      const uint64_t dk = smem_desc_sw128(s_base + C::kK0, 16, 1024);
-      const uint64_t dv = smem_desc_sw128(s_base + C::kV0, C::kBoxBytes, 1024);
+      // Descriptors as their low 32-bit words (start address, leading offset);
+      // the high word is the same for all three operands.
+      const uint32_t dq = sdesc_lo(s_base + C::kQ, 16);
+      const uint32_t dk = sdesc_lo(s_base + C::kK0, 16);
+      const uint32_t dv = sdesc_lo(s_base + C::kV0, C::kBoxBytes);
       auto qk = [&](int t, int kvi) {
-        const uint64_t a = dq + ((t * C::kTileBytes) >> 4);
-        const uint64_t b = dk + (((kvi % S) * C::kTileBytes) >> 4);
+        const uint32_t a = dq + ((t * C::kTileBytes) >> 4);
+        const uint32_t b = dk + (((kvi % S) * C::kTileBytes) >> 4);
         const uint32_t s_col = tmem + (t ? C::kColS1 : C::kColS0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(s_col, a + off, b + off, idesc_qk, kk > 0 ? 1u : 0u);
+          mma_ss_lo(s_col, a + off, b + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(kBarSFull + t));
       };
       // Half h of O_T += P_T V: keys 64h .. 64h+63 of the tile.
       auto pv = [&](int t, int kvi, bool first, int h) {
-        const uint64_t b = dv + (((kvi % S) * C::kTileBytes) >> 4);
+        const uint32_t b = dv + (((kvi % S) * C::kTileBytes) >> 4);
         const uint32_t s_col = tmem + (t ? C::kColS1 : C::kColS0);
         const uint32_t o_col = tmem + (t ? C::kColO1 : C::kColO0);
 #pragma unroll
         for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
-          mma_ts(o_col, s_col + kk * 8, b + ((kk * 2048) >> 4), idesc_pv,
-                 (!first || kk > 0) ? 1u : 0u);
+          mma_ts_lo(o_col, s_col + kk * 8, b + ((kk * 2048) >> 4), idesc_pv,
+                    (!first || kk > 0) ? 1u : 0u);
       };
       auto wait_p = [&](int t, int h, int cnt) {
         return mbar_wait(bar(kBarPReady + 2 * t + h), cnt & 1, abort_flag);
@@ -302,17 +322,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int it = 0, kv = 0, cnt_a = 0, cnt_b = 0;
       bool ok = true;
-      for (int k = 0; ok; ++k) {
-        int w;
-        if (!(ok = fetch_item(k, w, false)) || w >= n_items) break;
+      // The next item's QK_A(0) is issued during this item's last step, before
+      // the wait for tile B's last P, so that tile A's softmax of the next item
+      // overlaps tile B's tail instead of following it.
+      int w = 0;
+      bool a0_issued = false;
+      ok = fetch_item(0, w, false);
+      for (int k = 0; ok && w < n_items; ++k) {
         int q0, bh, n_a, n_b;
         sch.decode(w, q0, bh, n_a, n_b);
-        if (!(ok = mbar_wait(bar(kBarQFull), it & 1, abort_flag) && wait_k(kv))) break;
+        if (!a0_issued) {
+          if (!(ok = mbar_wait(bar(kBarQFullA), it & 1, abort_flag) && wait_k(kv))) break;
+          tc_fence_after();
+          qk(0, kv);
+          if (n_a == 1) mma_commit(bar(kBarQEmptyA));
+        }
+        a0_issued = false;
+        if (!(ok = mbar_wait(bar(kBarQFullB), it & 1, abort_flag) && wait_k(kv))) break;
         tc_fence_after();
-        qk(0, kv);
         qk(1, kv);
         mma_commit(bar(kBarKEmpty + kv % S));
-        if (n_b == 1) mma_commit(bar(kBarQEmpty));
+        if (n_b == 1) mma_commit(bar(kBarQEmptyB));
+        int w_next = n_items;
+        bool fetched = false;
         for (int j = 0; j < n_b; ++j) {
           const int kvj = kv + j;
           const int st = kvj % S;
@@ -332,6 +364,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               k_next_ready = true;
               tc_fence_after();
               qk(0, kvj + 1);
+              if (j + 2 == n_a) mma_commit(bar(kBarQEmptyA));  // last QK_A of the item
+            }
+          }
+          if (j == n_b - 1) {
+            // S_A is free (its last PV was issued above or at an earlier step):
+            // start the next item's tile A now.
+            if (!(ok = fetch_item(k + 1, w_next, false))) break;
+            fetched = true;
+            if (w_next < n_items) {
+              int nq0, nbh, nn_a, nn_b;
+              sch.decode(w_next, nq0, nbh, nn_a, nn_b);
+              if (!(ok = mbar_wait(bar(kBarQFullA), (it + 1) & 1, abort_flag) &&
+                         wait_k(kv + n_b)))
+                break;
+              tc_fence_after();
+              qk(0, kv + n_b);
+              if (nn_a == 1) mma_commit(bar(kBarQEmptyA));
+              a0_issued = true;
             }
           }
           if (!(ok = wait_p(1, 0, cnt_b))) break;
@@ -348,11 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             qk(1, kvj + 1);
             mma_commit(bar(kBarKEmpty + (kvj + 1) % S));
-            if (j + 2 == n_b) mma_commit(bar(kBarQEmpty));  // last QK of the item
+            if (j + 2 == n_b) mma_commit(bar(kBarQEmptyB));  // last QK_B of the item
           }
         }
+        if (!ok) break;
         kv += n_b;
         ++it;
+        if (!fetched && !(ok = fetch_item(k + 1, w_next, false))) break;
+        w = w_next;
       }
       // Drain: every MMA issued above has completed once this phase does.
       mma_commit(bar(kBarDrain));
