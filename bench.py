@@ -5,8 +5,9 @@ bf16 workload (fa_forward) + one paged decode over the 64-sequence x 32-head
 x head 128 workload with contexts uniform in [1, 4096] (fa_paged_decode):
 every row of the hot path.  Inputs are seeded synthetic draws, resident in
 device memory before timing starts.  Each kernel launch is bracketed by CUDA
-events on the stream it runs on; L2 is flushed (a 512 MiB write) before each
-launch, outside the events.
+events on the stream it runs on.  L2 is flushed (a 512 MiB write) before each
+forward and backward launch, outside the events; the decodes read more than L2
+holds (2.2 GB and 0.55 GB per launch) and are not flushed.
 
 Printed JSON line (rank 0):
   value          forward TFLOP/s, FLOPs = 4*B*H*N^2*d/2 (causal)
@@ -18,7 +19,8 @@ Printed JSON line (rank 0):
   decode_gqa     fa_paged_decode_gqa on the decode's sequences with 8 key/value
                  heads for the 32 query heads, GB/s and HBM roofline
   e2e            the same metrics through the C ABI with pinned host buffers,
-                 host<->device copies inside the timed region
+                 host<->device copies inside the timed region (copy-in, compute
+                 and copy-out of consecutive steps overlap on three streams)
   cpu_baseline   the float64 CPU oracle on the host cores, on a sample
 --impl reference times that oracle alone (the reference arm of this build).
 Multi-GPU (torchrun): each rank runs an independent replica (weak scaling).
@@ -221,7 +223,6 @@ def gpu_arm(args):
         for _ in range(args.warmup):
             flush.zero_()
             run_fwd()
-            flush.zero_()
             run_dec()
     stream.synchronize()
 
@@ -236,11 +237,12 @@ def gpu_arm(args):
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(K):
-            flush.zero_()
+            flush.zero_()   # the forward's inputs (100 MB) fit in L2
             evs[i][0].record(stream)
             run_fwd()
             evs[i][1].record(stream)
-            flush.zero_()
+            # the decode reads 2.2 GB per launch, far more than L2 holds: no flush
+            # (a flush write would leave 126 MB of dirty lines for it to evict)
             evs[i][2].record(stream)
             run_dec()
             evs[i][3].record(stream)
@@ -334,10 +336,8 @@ def gpu_arm(args):
     gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(kg)]
     with torch.cuda.stream(stream):
         for _ in range(3):
-            flush.zero_()
             run_gqa()
-        for i in range(kg):
-            flush.zero_()
+        for i in range(kg):   # 0.55 GB read per launch, larger than L2: no flush
             gev[i][0].record(stream)
             run_gqa()
             gev[i][1].record(stream)
@@ -345,50 +345,97 @@ def gpu_arm(args):
     gqa_ms = sum(e[0].elapsed_time(e[1]) for e in gev) / kg
     del dg, gout
 
-    # End to end through the C ABI with pinned host buffers.
+    # End to end through the C ABI with pinned host buffers: every step copies
+    # its inputs host -> device, runs the call and copies its results back.
+    # The three stages run on their own streams over two device slots, as a
+    # serving loop overlaps them (step i+1's inputs arrive while step i
+    # computes); the timed region runs from the first copy in to the last copy
+    # out, so every step's transfers are inside it.
+    ke = max(3, min(K, 50))
+
+    def pipeline(h2d, compute, d2h):
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+
+        def run(n, first):
+            for i in range(first, first + n):
+                sl = i % 2
+                if i >= 2:
+                    s_in.wait_event(ev_out[sl])      # the slot's previous results are out
+                with torch.cuda.stream(s_in):
+                    h2d(sl)
+                ev_in[sl].record(s_in)
+                stream.wait_event(ev_in[sl])
+                compute(sl)
+                ev_comp[sl].record(stream)
+                s_out.wait_event(ev_comp[sl])
+                with torch.cuda.stream(s_out):
+                    d2h(sl)
+                ev_out[sl].record(s_out)
+
+        run(2, 0)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(s_in)
+        run(ke, 2)
+        t1.record(s_out)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / ke
+
     hq, hk, hv = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3))
     for h, t in zip((hq, hk, hv), (q, k, v)):
         h.copy_(t)
-    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    ho = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
+    hl = [torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True) for _ in range(2)]
+    dqkv = [[torch.empty_like(q) for _ in range(3)] for _ in range(2)]
+    do_ = [torch.empty_like(o) for _ in range(2)]
+    dl = [torch.empty_like(lse) for _ in range(2)]
+
+    def fwd_h2d(sl):
+        for dst, src in zip(dqkv[sl], (hq, hk, hv)):
+            dst.copy_(src, non_blocking=True)
+
+    def fwd_compute(sl):
+        a, b_, c = dqkv[sl]
+        fa.fa_forward(a.data_ptr(), b_.data_ptr(), c.data_ptr(), do_[sl].data_ptr(),
+                      dl[sl].data_ptr(), B, H, N, d, scale, causal, sptr)
+
+    def fwd_d2h(sl):
+        ho[sl].copy_(do_[sl], non_blocking=True)
+        hl[sl].copy_(dl[sl], non_blocking=True)
+
+    e2e_fwd_ms = pipeline(fwd_h2d, fwd_compute, fwd_d2h)
+    del dqkv, do_, dl
+
     hdq = torch.empty(di.q.shape, dtype=di.q.dtype, pin_memory=True)
     hdq.copy_(di.q)
     hbt = torch.empty(di.block_tables.shape, dtype=torch.int32, pin_memory=True)
     hbt.copy_(di.block_tables)
     hcl = torch.empty(di.context_lens.shape, dtype=torch.int32, pin_memory=True)
     hcl.copy_(di.context_lens)
-    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    dbt, dcl, ddq = (torch.empty_like(di.block_tables), torch.empty_like(di.context_lens),
-                     torch.empty_like(di.q))
-    ke = max(3, min(K, 50))
-    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(ke)]
-    with torch.cuda.stream(stream):
-        for i in range(ke + 2):
-            rec = i >= 2
-            if rec:
-                e2e_ev[i - 2][0].record(stream)
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            fa.fa_forward(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o.data_ptr(),
-                          lse.data_ptr(), B, H, N, d, scale, causal, sptr)
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
-            if rec:
-                e2e_ev[i - 2][1].record(stream)
-            ddq.copy_(hdq, non_blocking=True)
-            dbt.copy_(hbt, non_blocking=True)
-            dcl.copy_(hcl, non_blocking=True)
-            fa.fa_paged_decode(ddq.data_ptr(), di.k_cache.data_ptr(), di.v_cache.data_ptr(),
-                               dbt.data_ptr(), dcl.data_ptr(), out.data_ptr(), S, Hd, D,
-                               di.block_size, di.max_blocks, di.scale, sptr)
-            hout.copy_(out, non_blocking=True)
-            if rec:
-                e2e_ev[i - 2][2].record(stream)
-    stream.synchronize()
-    e2e_fwd_ms = sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / ke
-    e2e_dec_ms = sum(e[1].elapsed_time(e[2]) for e in e2e_ev) / ke
+    hout = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+    ddec = [(torch.empty_like(di.q), torch.empty_like(di.block_tables),
+             torch.empty_like(di.context_lens), torch.empty_like(out)) for _ in range(2)]
+
+    def dec_h2d(sl):
+        ddq, dbt, dcl, _ = ddec[sl]
+        ddq.copy_(hdq, non_blocking=True)
+        dbt.copy_(hbt, non_blocking=True)
+        dcl.copy_(hcl, non_blocking=True)
+
+    def dec_compute(sl):
+        ddq, dbt, dcl, dout_ = ddec[sl]
+        fa.fa_paged_decode(ddq.data_ptr(), di.k_cache.data_ptr(), di.v_cache.data_ptr(),
+                           dbt.data_ptr(), dcl.data_ptr(), dout_.data_ptr(), S, Hd, D,
+                           di.block_size, di.max_blocks, di.scale, sptr)
+
+    def dec_d2h(sl):
+        hout[sl].copy_(ddec[sl][3], non_blocking=True)
+
+    e2e_dec_ms = pipeline(dec_h2d, dec_compute, dec_d2h)
+    del ddec
     h2d = 3 * q.numel() * 2 + di.q.numel() * 2 + di.block_tables.numel() * 4 + S * 4
     d2h = o.numel() * 2 + lse.numel() * 4 + out.numel() * 2
 
@@ -422,7 +469,9 @@ def gpu_arm(args):
             "fwd": {k_: v_ for k_, v_ in FWD.items() if k_ != "seed"},
             "decode": {k_: v_ for k_, v_ in DEC.items() if k_ != "seed"},
             "decode_sum_ctx": int(ctx.sum()),
-            "l2": "flushed (512 MiB write) before every timed launch",
+            "l2": "forward, 16K forward and backward: flushed (512 MiB write) before every "
+                  "timed launch; decode (2.2 GB read per launch) and grouped decode "
+                  "(0.55 GB): inputs larger than L2, not flushed",
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
             "sms": torch.cuda.get_device_properties(dev).multi_processor_count,
         },
@@ -480,9 +529,11 @@ def gpu_arm(args):
                 "decode_gbs": round(weak_scaling_rate(dec_bytes, ws, e2e_dec_ms, 1e9), 1),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "KV cache resident (serving state); q, K, V, q_decode, block table, "
-                        "context lens copied in and O, LSE, out copied back every step"},
+                        "context lens copied in and O, LSE, out copied back every step; copies "
+                        "in, compute and copies out on three streams over two device slots "
+                        "(step i+1's inputs arrive while step i computes)"},
         # library kernels inside timed regions (a backward is three launches)
-        "gpu_launches": 2 * K + kl + 3 * kb + kg + 2 * ke,
+        "gpu_launches": 2 * K + kl + 3 * kb + kg + 2 * ke,  # e2e: ke forwards + ke decodes
         "clocks": clk,
         "device_status": status,
         "wall_s": round(wall, 3),
