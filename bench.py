@@ -14,6 +14,7 @@ Printed JSON line (rank 0):
   decode         decode GB/s over the algorithmic bytes (K/V of every context
                  token, q, block table entries read, out)
   roofline       the forward (dominant kernel) against the measured bf16 peak
+  fwd_f16        fa_forward_f16 on the forward workload in fp16 (same FLOPs)
   backward       fa_backward (dQ, dK, dV) of the forward workload, TFLOP/s with
                  FLOPs = 2.5 x the forward's, and its own roofline
   decode_gqa     fa_paged_decode_gqa on the decode's sequences with 8 key/value
@@ -284,6 +285,31 @@ def gpu_arm(args):
     long_ms = sum(e[0].elapsed_time(e[1]) for e in lev) / kl
     del lq, lk, lv, lo, llse
 
+    # The fp16 forward on the same workload, timed the same way, as "fwd_f16".
+    hq16, hk16, hv16 = (t.to(torch.float16) for t in inputs.forward_inputs(
+        B, H, N, d, torch.float32, seed=FWD["seed"] + 1000 * rank))
+    q16, k16, v16 = (t.to(dev) for t in (hq16, hk16, hv16))
+    o16 = torch.empty_like(q16)
+
+    def run_f16():
+        fa.fa_forward_f16(q16.data_ptr(), k16.data_ptr(), v16.data_ptr(), o16.data_ptr(),
+                          lse.data_ptr(), B, H, N, d, scale, causal, sptr)
+
+    kf = max(3, min(K // 4, 100))
+    fev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(kf)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush.zero_()
+            run_f16()
+        for i in range(kf):
+            flush.zero_()
+            fev[i][0].record(stream)
+            run_f16()
+            fev[i][1].record(stream)
+    stream.synchronize()
+    f16_ms = sum(e[0].elapsed_time(e[1]) for e in fev) / kf
+    del q16, k16, v16, o16, hq16, hk16, hv16
+
     # The backward (dQ, dK, dV) of the main forward workload, timed the same
     # way on the forward's own O and LSE, reported as "backward".
     g_out = inputs.grad_output(B, H, N, d, torch.bfloat16, seed=FWD["seed"] + 1000 * rank).to(dev)
@@ -440,9 +466,10 @@ def gpu_arm(args):
     d2h = o.numel() * 2 + lse.numel() * 4 + out.numel() * 2
 
     if ws > 1:
-        (fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms, bwd_ms, gqa_ms), status = \
-            reduce_over_ranks([fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms, bwd_ms,
-                               gqa_ms], status, dev)
+        (fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms, bwd_ms, gqa_ms,
+         f16_ms), status = reduce_over_ranks(
+            [fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms, bwd_ms, gqa_ms, f16_ms],
+            status, dev)
 
     tflops = weak_scaling_rate(flops, ws, fwd_ms, 1e12)
     per_gpu_tflops = weak_scaling_rate(flops, 1, fwd_ms, 1e12)
@@ -483,6 +510,14 @@ def gpu_arm(args):
             "unit": "TFLOP/s",
             "frac_of_bf16_peak": round(fwd_flops(**FWD_LONG) / (long_ms * 1e-3) / 1e12
                                        / peaks["bf16_tflops"], 4),
+        },
+        "fwd_f16": {
+            "workload": "fa_forward_f16 fp16 B=2 H=16 N=4096 d=128 causal (the forward's inputs "
+                        "rounded to fp16)",
+            "ms": round(f16_ms, 4),
+            "value": round(weak_scaling_rate(flops, ws, f16_ms, 1e12), 2),
+            "unit": "TFLOP/s",
+            "frac_of_bf16_peak": round(flops / (f16_ms * 1e-3) / 1e12 / peak_t, 4),
         },
         "backward": {
             "workload": "fa_backward bf16 B=2 H=16 N=4096 d=128 causal (dQ, dK, dV of the "
@@ -533,7 +568,7 @@ def gpu_arm(args):
                         "in, compute and copies out on three streams over two device slots "
                         "(step i+1's inputs arrive while step i computes)"},
         # library kernels inside timed regions (a backward is three launches)
-        "gpu_launches": 2 * K + kl + 3 * kb + kg + 2 * ke,  # e2e: ke forwards + ke decodes
+        "gpu_launches": 2 * K + kl + kf + 3 * kb + kg + 2 * ke,  # e2e: ke forwards + ke decodes
         "clocks": clk,
         "device_status": status,
         "wall_s": round(wall, 3),

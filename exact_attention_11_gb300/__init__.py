@@ -16,7 +16,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["fa_forward", "fa_forward_fp32", "fa_paged_decode", "fa_paged_decode_noalloc",
+__all__ = ["fa_forward", "fa_forward_f16", "fa_forward_fp32", "fa_paged_decode", "fa_paged_decode_noalloc",
            "fa_backward", "fa_backward_workspace_bytes", "backward", "fa_paged_decode_gqa",
            "fa_status_string",
            "fa_device_status", "fa_release", "forward", "paged_decode", "FattnError",
@@ -48,6 +48,7 @@ _vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 EXPORTS = {
     "fa_forward": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_forward_fp32": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "fa_forward_f16": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_paged_decode": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_paged_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_paged_decode_gqa": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp], _i),
@@ -91,6 +92,11 @@ def _check(name: str, rc: int) -> int:
 def fa_forward(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     return _check("fa_forward", load().fa_forward(q, k, v, o, lse, B, H, N, d, scale,
                                                   int(causal), stream))
+
+
+def fa_forward_f16(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
+    return _check("fa_forward_f16", load().fa_forward_f16(q, k, v, o, lse, B, H, N, d, scale,
+                                                          int(causal), stream))
 
 
 def fa_forward_fp32(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
@@ -171,7 +177,7 @@ def _stream(t):
 
 
 def forward(q, k, v, scale=None, causal=False, out=None, lse=None, want_lse=True):
-    """Exact attention on [B,H,N,d] CUDA tensors (bf16 or fp32, contiguous).
+    """Exact attention on [B,H,N,d] CUDA tensors (bf16, fp16 or fp32, contiguous).
 
     Returns (O, LSE) with O in the input dtype and LSE fp32 [B,H,N] (None when
     ``want_lse`` is False).  Runs on the current torch stream."""
@@ -180,8 +186,9 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, want_lse=True
         raise ValueError("q, k, v must share one [B,H,N,d] shape")
     if not (q.is_cuda and q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous CUDA tensors")
-    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
-        raise ValueError("q, k, v must all be bf16 or all fp32")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float16,
+                                                                torch.float32):
+        raise ValueError("q, k, v must all be bf16, all fp16 or all fp32")
     B, H, N, d = q.shape
     if scale is None:
         scale = d ** -0.5
@@ -189,7 +196,8 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, want_lse=True
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fn = fa_forward if q.dtype == torch.bfloat16 else fa_forward_fp32
+    fn = {torch.bfloat16: fa_forward, torch.float16: fa_forward_f16,
+          torch.float32: fa_forward_fp32}[q.dtype]
     fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, float(scale), bool(causal),
        _stream(q))
     return out, lse

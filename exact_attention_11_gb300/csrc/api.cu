@@ -84,12 +84,13 @@ int get_encoder() {
 // 3-D bf16 view {d, N, BH} of a [BH, N, d] tensor; boxes of 64 x box_rows x 1
 // (one 128-byte row segment per box row) with the 128-byte swizzle.  Rows
 // past N read as zero.
-int encode_qkv_map(CUtensorMap *m, const void *base, int BH, int N, int d, int box_rows = 128) {
+int encode_qkv_map(CUtensorMap *m, const void *base, int BH, int N, int d, int box_rows = 128,
+                   CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
   const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+  const CUresult r = g_encode(m, dtype, 3, const_cast<void *>(base), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -194,8 +195,10 @@ const char *fa_status_string(int status) {
   }
 }
 
-int fa_forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
-               int N, int d, float scale, int causal, fa_stream_t stream) {
+namespace {
+// fa_forward and fa_forward_f16: the tensor-core forward for 16-bit inputs.
+int forward16(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+              int N, int d, float scale, int causal, fa_stream_t stream, bool f16) {
   int rc = check_forward_args(q, k, v, o, lse, B, H, N, d, scale);
   if (rc != FA_OK) return rc;
   const int BH = B * H;
@@ -212,12 +215,25 @@ int fa_forward(const void *q, const void *k, const void *v, void *o, float *lse,
     fault_cta = st.inject_fault ? 0 : -1;
     st.inject_fault = 0;
   }
-  if ((rc = encode_qkv_map(&tq, q, BH, N, d)) != FA_OK) return rc;
-  if ((rc = encode_qkv_map(&tk, k, BH, N, d)) != FA_OK) return rc;
-  if ((rc = encode_qkv_map(&tv, v, BH, N, d)) != FA_OK) return rc;
+  const CUtensorMapDataType dt =
+      f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if ((rc = encode_qkv_map(&tq, q, BH, N, d, 128, dt)) != FA_OK) return rc;
+  if ((rc = encode_qkv_map(&tk, k, BH, N, d, 128, dt)) != FA_OK) return rc;
+  if ((rc = encode_qkv_map(&tv, v, BH, N, d, 128, dt)) != FA_OK) return rc;
   return cuda_status(launch_fwd_bf16(tq, tk, tv, o, lse, BH, N, d, scale, causal ? 1 : 0, sched,
                                      g_dev[dev].status, fault_cta,
-                                     reinterpret_cast<cudaStream_t>(stream)));
+                                     reinterpret_cast<cudaStream_t>(stream), f16));
+}
+}  // namespace
+
+int fa_forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+               int N, int d, float scale, int causal, fa_stream_t stream) {
+  return forward16(q, k, v, o, lse, B, H, N, d, scale, causal, stream, false);
+}
+
+int fa_forward_f16(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                   int H, int N, int d, float scale, int causal, fa_stream_t stream) {
+  return forward16(q, k, v, o, lse, B, H, N, d, scale, causal, stream, true);
 }
 
 int fa_forward_fp32(const float *q, const float *k, const float *v, float *o, float *lse, int B,

@@ -87,6 +87,23 @@ struct Cfg {
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
 };
 
+// 16-bit element type of Q, K, V, P and O: bf16 (F16 = false) or fp16.  The
+// instruction descriptor's A and B type fields (bits 7-9, 10-12) are 1 for
+// bf16 and 0 for fp16; both operands of every MMA share the type.
+template <bool F16>
+__device__ __forceinline__ constexpr uint32_t idesc16(uint32_t bf16_desc) {
+  return F16 ? (bf16_desc & ~((1u << 7) | (1u << 10))) : bf16_desc;
+}
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if (F16) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+  }
+  return pack_bf16x2(lo, hi);
+}
+
 // Barrier slots (8 bytes each).
 enum : int {
   kBarQFullA = 0,      // query tile A of the current item
@@ -135,11 +152,11 @@ struct ItemDecoder {
   }
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ o,
+                       const __grid_constant__ CUtensorMap tm_v, uint16_t *__restrict__ o,
                        float *__restrict__ lse, int N, int BH, int n_qblocks, float scale_log2,
                        int causal, int *__restrict__ sched, int *__restrict__ dev_status,
                        int fault_cta) {
@@ -283,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 1 && elect_one()) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
+      constexpr uint32_t idesc_qk = idesc16<F16>(idesc_bf16_f32(BM, BN, false));
+      constexpr uint32_t idesc_pv = idesc16<F16>(idesc_bf16_f32(BM, D, true));
       // Shared-memory descriptors are built once; moving an operand by `off`
       // bytes adds off >> 4 to the start-address field, which cannot carry
       // out of its 14 bits for addresses inside the 228 KB shared window.
@@ -493,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 x = f2_split(x2);
             const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
             sum2[(e >> 1) & 1] = fadd2(sum2[(e >> 1) & 1], f2(p.x, p.y));
-            pk[e >> 1] = pack_bf16x2(p.x, p.y);
+            pk[e >> 1] = pack2<F16>(p.x, p.y);
           }
           tmem_st16(s_tmem + c * 16, pk);
           if (c & 1) {
@@ -513,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait(bar(kBarODone + t), it & 1, abort_flag))) break;
       tc_fence_after();
       const float inv_l = 1.f / l;
-      __nv_bfloat16 *orow = o + (static_cast<int64_t>(bh) * N + row) * D;
+      uint16_t *orow = o + (static_cast<int64_t>(bh) * N + row) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
@@ -524,13 +541,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv_l,
+            v.x = pack2<F16>(__uint_as_float(ov[8 * e + 0]) * inv_l,
                               __uint_as_float(ov[8 * e + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv_l,
+            v.y = pack2<F16>(__uint_as_float(ov[8 * e + 2]) * inv_l,
                               __uint_as_float(ov[8 * e + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv_l,
+            v.z = pack2<F16>(__uint_as_float(ov[8 * e + 4]) * inv_l,
                               __uint_as_float(ov[8 * e + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv_l,
+            v.w = pack2<F16>(__uint_as_float(ov[8 * e + 6]) * inv_l,
                               __uint_as_float(ov[8 * e + 7]) * inv_l);
             dst[e] = v;
           }
@@ -563,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int g_num_sms[64] = {};
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, void *o,
                      float *lse, int BH, int N, float scale, int causal, int *sched,
                      int *dev_status, int fault_cta, cudaStream_t stream) {
@@ -578,15 +595,15 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
     if (e != cudaSuccess) return e;
     g_num_sms[dev] = n;
   }
-  e = cudaFuncSetAttribute(fwd_bf16_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kAlloc);
+  e = cudaFuncSetAttribute(fwd_bf16_tc_kernel<D, F16>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_qblocks = (N + 2 * BM - 1) / (2 * BM);
   const long long n_items = static_cast<long long>(n_qblocks) * BH;
   const int grid = static_cast<int>(n_items < g_num_sms[dev] ? n_items : g_num_sms[dev]);
   const float scale_log2 = scale * 1.4426950408889634f;
-  fwd_bf16_tc_kernel<D><<<grid, kThreads, C::kAlloc, stream>>>(
-      tq, tk, tv, reinterpret_cast<__nv_bfloat16 *>(o), lse, N, BH, n_qblocks, scale_log2, causal,
+  fwd_bf16_tc_kernel<D, F16><<<grid, kThreads, C::kAlloc, stream>>>(
+      tq, tk, tv, reinterpret_cast<uint16_t *>(o), lse, N, BH, n_qblocks, scale_log2, causal,
       sched, dev_status, fault_cta);
   return cudaGetLastError();
 }
@@ -595,12 +612,17 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
 
 cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             void *o, float *lse, int BH, int N, int d, float scale, int causal,
-                            int *sched, int *dev_status, int fault_cta, cudaStream_t stream) {
+                            int *sched, int *dev_status, int fault_cta, cudaStream_t stream,
+                            bool f16) {
   if (d == 64)
-    return launch_d<64>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status, fault_cta,
-                        stream);
-  return launch_d<128>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status, fault_cta,
-                       stream);
+    return f16 ? launch_d<64, true>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status,
+                                    fault_cta, stream)
+               : launch_d<64, false>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status,
+                                     fault_cta, stream);
+  return f16 ? launch_d<128, true>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status,
+                                   fault_cta, stream)
+             : launch_d<128, false>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status,
+                                    fault_cta, stream);
 }
 
 }  // namespace fattn

@@ -76,6 +76,16 @@ int fa_forward(const void *q, const void *k, const void *v, void *o, float *lse,
                fa_stream_t stream);
 
 /*
+ * fa_forward_f16 -- fa_forward with IEEE fp16 q, k, v and o (1 sign, 5
+ * exponent, 10 mantissa bits): the same operation, layouts, lse and errors.
+ * The softmax weights are rounded to fp16 before they multiply V, and o is
+ * rounded to nearest even fp16; inputs must be finite and |o| below 65504.
+ */
+int fa_forward_f16(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int B, int H, int N, int d, float scale, int causal,
+                   fa_stream_t stream);
+
+/*
  * fa_forward_fp32 -- the same operation and contract as fa_forward with fp32
  * q, k, v and o (every product and sum in fp32 on the CUDA cores, no reduced
  * precision anywhere).  d is 64 or 128.

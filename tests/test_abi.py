@@ -60,7 +60,7 @@ P = 4096  # a 16-byte-aligned fake address: never dereferenced on these paths
     ((P, P, P, P, NULL, 1, 1, 0, 64, 0.125, 0), 0),           # N = 0: no-op
 ])
 def test_forward_argument_checks(lib, args, expect):
-    for fn in (lib.fa_forward, lib.fa_forward_fp32):
+    for fn in (lib.fa_forward, lib.fa_forward_f16, lib.fa_forward_fp32):
         assert fn(*args, None) == expect
 
 
