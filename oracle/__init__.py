@@ -66,9 +66,13 @@ def _bind(lib):
         ctypes.c_long] * 8 + [ctypes.c_double, ctypes.c_int]
     lib.oracle_backward.argtypes = [_dp] * 7 + [ctypes.c_long] * 4 + [ctypes.c_double, ctypes.c_int,
                                                                      ctypes.c_int]
+    lib.oracle_forward_masked_rows.argtypes = [_dp, _dp, _dp, ctypes.c_void_p, ctypes.c_long, _lp,
+                                               ctypes.c_long, _dp, _dp] + [ctypes.c_long] * 4 + [
+        ctypes.c_double, ctypes.c_int]
     lib.oracle_max_threads.argtypes = []
     for f in (lib.oracle_forward, lib.oracle_forward_rows, lib.oracle_probs_row,
               lib.oracle_paged_decode, lib.oracle_paged_decode_gqa, lib.oracle_backward,
+              lib.oracle_forward_masked_rows,
               lib.oracle_max_threads):
         f.restype = ctypes.c_int
     return lib
@@ -200,6 +204,39 @@ def attention_backward(q, k, v, dout, scale: float, causal: bool, nthreads: int 
     if rc != 0:
         raise ValueError("oracle_backward rejected its arguments")
     return dq, dk, dv
+
+
+def attention_forward_masked(q, k, v, mask, scale: float, rows=None, nthreads: int = 0):
+    """Forward with a boolean mask (nonzero = the key is visible).  q, k, v are
+    [B,H,N,d]; mask is [N,N] (shared by every head) or [B,H,N,N] / [B*H,N,N].
+    Returns (O [B,H,R,d], LSE [B,H,R]) for the query rows `rows` (default all);
+    a row with no visible key gives O = 0, LSE = -inf."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim != 4 or not (k.shape == v.shape == q.shape):
+        raise ValueError("q, k, v must share one [B,H,N,d] shape")
+    B, H, N, d = q.shape
+    if hasattr(mask, "detach"):
+        mask = mask.detach().cpu().numpy()
+    m = np.ascontiguousarray(np.asarray(mask) != 0, dtype=np.uint8)
+    if m.shape == (N, N):
+        stride = 0
+    elif m.size == B * H * N * N and m.shape[-2:] == (N, N):
+        stride = N * N
+    else:
+        raise ValueError("mask must be [N,N] or one [N,N] per head")
+    if rows is None:
+        rows = np.arange(N)
+    rr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    R = rr.shape[0]
+    o = np.zeros((B, H, R, d))
+    lse = np.zeros((B, H, R))
+    rc = _load().oracle_forward_masked_rows(_ptr(q), _ptr(k), _ptr(v),
+                                            m.ctypes.data_as(ctypes.c_void_p), stride,
+                                            _ptr(rr, _lp), R, _ptr(o), _ptr(lse), B, H, N, d,
+                                            float(scale), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_forward_masked_rows rejected its arguments")
+    return o, lse
 
 
 def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,

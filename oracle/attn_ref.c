@@ -146,6 +146,60 @@ int oracle_forward(const double *q, const double *k, const double *v, double *o,
     return rc;
 }
 
+/* Forward with a boolean attention mask ("FlashAttention: GPU 메모리 계층을
+ * 활용한 어텐션 최적화 분석", youngju.dev, section 11.3: a custom boolean
+ * attn_mask, True = the key takes part): for row i of head bh the visible keys
+ * are the j with mask[bh * mask_bh_stride + i * N + j] != 0 (mask_bh_stride = 0
+ * shares one [N, N] mask across heads).  The visible keys and values are
+ * gathered in order and the row definition applied to them; a row with no
+ * visible key gives O = 0 and LSE = -inf. */
+int oracle_forward_masked_rows(const double *q, const double *k, const double *v,
+                               const unsigned char *mask, long mask_bh_stride,
+                               const long *rows, long nrows, double *o_rows,
+                               double *lse_rows, long B, long H, long N, long d,
+                               double scale, int nthreads)
+{
+    if (B < 0 || H < 0 || N < 0 || d <= 0 || nrows < 0 || mask_bh_stride < 0) return -1;
+    for (long r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= N) return -1;
+    set_threads(nthreads);
+    const long BH = B * H;
+    int failed = 0;
+#pragma omp parallel
+    {
+        const size_t n1 = (size_t)(N > 0 ? N : 1);
+        double *scores = (double *)malloc(sizeof(double) * n1);
+        double *kv = (double *)malloc(sizeof(double) * n1 * (size_t)d);
+        double *vv = (double *)malloc(sizeof(double) * n1 * (size_t)d);
+        if (!scores || !kv || !vv) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (long t = 0; t < BH * nrows; ++t) {
+                const long bh = t / nrows, r = t % nrows;
+                const long i = rows[r];
+                const double *qh = q + bh * N * d, *kh = k + bh * N * d, *vh = v + bh * N * d;
+                const unsigned char *mrow = mask + bh * mask_bh_stride + i * N;
+                long n_vis = 0;
+                for (long j = 0; j < N; ++j) {
+                    if (mrow[j] != 0) {
+                        for (long c = 0; c < d; ++c) {
+                            kv[n_vis * d + c] = kh[j * d + c];
+                            vv[n_vis * d + c] = vh[j * d + c];
+                        }
+                        ++n_vis;
+                    }
+                }
+                attend_row(qh + i * d, kv, vv, n_vis, d, scale, scores,
+                           o_rows + (bh * nrows + r) * d, lse_rows + bh * nrows + r, NULL);
+            }
+        }
+        free(scores); free(kv); free(vv);
+    }
+    return failed ? -1 : 0;
+}
+
 /* The normalised softmax row P[i, 0..N) of one head (q,k are [N,d]); entries
  * of masked keys are written as 0.  Used to check that rows sum to one. */
 int oracle_probs_row(const double *q, const double *k, long N, long d, long i,

@@ -353,6 +353,70 @@ ALL_CHECKS = [check_hand_examples, check_brute_force_tiny, check_library_sdpa,
               check_layout_fixture, check_decode_matches_gathered_forward,
               check_decode_one_hot, check_gqa_decode_matches_replicated_heads,
               check_gqa_decode_head_groups]
+# (the mask checks are appended below, after their definitions)
+
+
+# --------------------------------------------------------------------------
+# Boolean attention mask ("FlashAttention: GPU 메모리 계층을 활용한 어텐션 최적화
+# 분석", youngju.dev, section 11.3: attn_mask = tril(ones) as a custom mask)
+
+def check_mask_special_cases():
+    """tril(ones) reproduces the causal forward and ones the full forward, bit
+    for bit (the same keys in the same order); one visible key per row selects
+    its value row exactly with LSE = its score; an all-False row gives O = 0
+    and LSE = -inf."""
+    r = _rng(41)
+    B, H, N, d, scale = 1, 2, 23, 8, 0.4
+    q, k, v = (r.standard_normal((B, H, N, d)) for _ in range(3))
+    tril = np.tril(np.ones((N, N), dtype=np.uint8))
+    o_m, l_m = oracle.attention_forward_masked(q, k, v, tril, scale)
+    o_c, l_c = oracle.attention_forward(q, k, v, scale, True)
+    np.testing.assert_array_equal(o_m, o_c)
+    np.testing.assert_array_equal(l_m, l_c)
+    o_m, l_m = oracle.attention_forward_masked(q, k, v, np.ones((N, N), dtype=np.uint8), scale)
+    o_f, l_f = oracle.attention_forward(q, k, v, scale, False)
+    np.testing.assert_array_equal(o_m, o_f)
+    np.testing.assert_array_equal(l_m, l_f)
+    pick = r.integers(0, N, size=N)
+    one = np.zeros((N, N), dtype=np.uint8)
+    one[np.arange(N), pick] = 1
+    one[5] = 0                                   # row 5: nothing visible
+    o1, l1 = oracle.attention_forward_masked(q, k, v, one, scale)
+    for i in range(N):
+        if i == 5:
+            np.testing.assert_array_equal(o1[:, :, i], 0.0)
+            assert np.all(np.isneginf(l1[:, :, i]))
+            continue
+        np.testing.assert_array_equal(o1[:, :, i], v[:, :, pick[i]])
+        np.testing.assert_allclose(l1[:, :, i],
+                                   scale * np.einsum("bhc,bhc->bh", q[:, :, i], k[:, :, pick[i]]),
+                                   rtol=0, atol=1e-13)
+
+
+def check_mask_brute_force():
+    """Random masks on tiny heads against a pure-Python softmax over the visible
+    keys, including a different mask per head."""
+    r = _rng(43)
+    B, H, N, d, scale = 2, 2, 6, 3, 0.7
+    q, k, v = (r.standard_normal((B, H, N, d)) for _ in range(3))
+    masks = (r.random((B, H, N, N)) < 0.5).astype(np.uint8)
+    masks[0, 1, 2] = 0
+    o, lse = oracle.attention_forward_masked(q, k, v, masks, scale)
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                vis = [j for j in range(N) if masks[b, h, i, j]]
+                if not vis:
+                    assert np.all(o[b, h, i] == 0) and np.isneginf(lse[b, h, i])
+                    continue
+                sc = [scale * sum(q[b, h, i, c] * k[b, h, j, c] for c in range(d)) for j in vis]
+                mx = max(sc)
+                e = [math.exp(x - mx) for x in sc]
+                tot = sum(e)
+                for c in range(d):
+                    want = sum(e[t] / tot * v[b, h, j, c] for t, j in enumerate(vis))
+                    assert abs(o[b, h, i, c] - want) <= 1e-12
+                assert abs(lse[b, h, i] - (mx + math.log(tot))) <= 1e-12
 
 
 # --------------------------------------------------------------------------
@@ -429,5 +493,6 @@ def check_backward_invariants():
     np.testing.assert_allclose(dk, 0, atol=1e-12)
 
 
+ALL_CHECKS += [check_mask_special_cases, check_mask_brute_force]
 ALL_CHECKS += [check_backward_hand_example, check_backward_finite_differences,
                check_backward_library_autograd, check_backward_invariants]

@@ -31,6 +31,9 @@ MUTANTS = [
      "V[tok * D + c] = vb[off * D + c];"),
     ("block_table_index_mod", "block_tables[s * max_blocks + tok / block_size]",
      "block_tables[s * max_blocks + tok % block_size]"),
+    ("mask_inverted", "if (mrow[j] != 0) {", "if (mrow[j] == 0) {"),
+    ("mask_transposed", "const unsigned char *mrow = mask + bh * mask_bh_stride + i * N;\n                long n_vis = 0;\n                for (long j = 0; j < N; ++j) {\n                    if (mrow[j] != 0) {",
+     "const unsigned char *mrow = mask + bh * mask_bh_stride + i;\n                long n_vis = 0;\n                for (long j = 0; j < N; ++j) {\n                    if (mrow[j * N] != 0) {"),
     ("gqa_heads_interleaved", "const long kvh = h / group;", "const long kvh = h % num_kv_heads;"),
     ("bwd_D_sign", "const double ds = p[j] * (dp[j] - D);", "const double ds = p[j] * (dp[j] + D);"),
     ("bwd_dq_no_scale", "dqh[i * d + c] += scale * ds * kh[j * d + c];",
