@@ -15,6 +15,7 @@ Printed JSON line (rank 0):
                  token, q, block table entries read, out)
   roofline       the forward (dominant kernel) against the measured bf16 peak
   fwd_f16        fa_forward_f16 on the forward workload in fp16 (same FLOPs)
+  fwd_masked     fa_forward_masked with the tril mask on the forward workload
   backward       fa_backward (dQ, dK, dV) of the forward workload, TFLOP/s with
                  FLOPs = 2.5 x the forward's, and its own roofline
   decode_gqa     fa_paged_decode_gqa on the decode's sequences with 8 key/value
@@ -310,6 +311,31 @@ def gpu_arm(args):
     f16_ms = sum(e[0].elapsed_time(e[1]) for e in fev) / kf
     del q16, k16, v16, o16, hq16, hk16, hv16
 
+    # The forward with a boolean mask (tril, the causal pattern as an explicit
+    # [N, N] mask), timed the same way, as "fwd_masked".
+    tril = torch.tril(torch.ones(N, N, dtype=torch.uint8, device=dev))
+
+    def run_masked():
+        fa.fa_forward_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                             lse.data_ptr(), tril.data_ptr(), 0, B, H, N, d, scale, sptr)
+
+    km = max(3, min(K // 4, 100))
+    mev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(km)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush.zero_()
+            run_masked()
+        for i in range(km):
+            flush.zero_()
+            mev[i][0].record(stream)
+            run_masked()
+            mev[i][1].record(stream)
+    stream.synchronize()
+    masked_ms = sum(e[0].elapsed_time(e[1]) for e in mev) / km
+    del tril
+    with torch.cuda.stream(stream):
+        run_fwd()   # o, lse of the causal forward again (the backward uses them)
+
     # The backward (dQ, dK, dV) of the main forward workload, timed the same
     # way on the forward's own O and LSE, reported as "backward".
     g_out = inputs.grad_output(B, H, N, d, torch.bfloat16, seed=FWD["seed"] + 1000 * rank).to(dev)
@@ -467,9 +493,9 @@ def gpu_arm(args):
 
     if ws > 1:
         (fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms, bwd_ms, gqa_ms,
-         f16_ms), status = reduce_over_ranks(
-            [fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms, bwd_ms, gqa_ms, f16_ms],
-            status, dev)
+         f16_ms, masked_ms), status = reduce_over_ranks(
+            [fwd_ms, dec_ms, e2e_fwd_ms, e2e_dec_ms, wall, long_ms, bwd_ms, gqa_ms, f16_ms,
+             masked_ms], status, dev)
 
     tflops = weak_scaling_rate(flops, ws, fwd_ms, 1e12)
     per_gpu_tflops = weak_scaling_rate(flops, 1, fwd_ms, 1e12)
@@ -518,6 +544,14 @@ def gpu_arm(args):
             "value": round(weak_scaling_rate(flops, ws, f16_ms, 1e12), 2),
             "unit": "TFLOP/s",
             "frac_of_bf16_peak": round(flops / (f16_ms * 1e-3) / 1e12 / peak_t, 4),
+        },
+        "fwd_masked": {
+            "workload": "fa_forward_masked bf16 B=2 H=16 N=4096 d=128 with the [N,N] tril mask "
+                        "(every key tile computed; FLOPs counted for the visible half)",
+            "ms": round(masked_ms, 4),
+            "value": round(weak_scaling_rate(flops, ws, masked_ms, 1e12), 2),
+            "unit": "TFLOP/s",
+            "frac_of_bf16_peak": round(flops / (masked_ms * 1e-3) / 1e12 / peak_t, 4),
         },
         "backward": {
             "workload": "fa_backward bf16 B=2 H=16 N=4096 d=128 causal (dQ, dK, dV of the "
@@ -568,7 +602,7 @@ def gpu_arm(args):
                         "in, compute and copies out on three streams over two device slots "
                         "(step i+1's inputs arrive while step i computes)"},
         # library kernels inside timed regions (a backward is three launches)
-        "gpu_launches": 2 * K + kl + kf + 3 * kb + kg + 2 * ke,  # e2e: ke forwards + ke decodes
+        "gpu_launches": 2 * K + kl + kf + km + 3 * kb + kg + 2 * ke,  # e2e: ke fwd + ke decodes
         "clocks": clk,
         "device_status": status,
         "wall_s": round(wall, 3),

@@ -16,7 +16,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["fa_forward", "fa_forward_f16", "fa_forward_fp32", "fa_paged_decode", "fa_paged_decode_noalloc",
+__all__ = ["fa_forward", "fa_forward_f16", "fa_forward_masked", "forward_masked", "fa_forward_fp32", "fa_paged_decode", "fa_paged_decode_noalloc",
            "fa_backward", "fa_backward_workspace_bytes", "backward", "fa_paged_decode_gqa",
            "fa_status_string",
            "fa_device_status", "fa_release", "forward", "paged_decode", "FattnError",
@@ -49,6 +49,8 @@ EXPORTS = {
     "fa_forward": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_forward_fp32": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_forward_f16": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "fa_forward_masked": ([_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_longlong, _i, _i, _i, _i, _f,
+                           _vp], _i),
     "fa_paged_decode": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_paged_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp], _i),
     "fa_paged_decode_gqa": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp], _i),
@@ -97,6 +99,11 @@ def fa_forward(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
 def fa_forward_f16(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     return _check("fa_forward_f16", load().fa_forward_f16(q, k, v, o, lse, B, H, N, d, scale,
                                                           int(causal), stream))
+
+
+def fa_forward_masked(q, k, v, o, lse, mask, mask_bh_stride, B, H, N, d, scale, stream) -> int:
+    return _check("fa_forward_masked", load().fa_forward_masked(
+        q, k, v, o, lse, mask, mask_bh_stride, B, H, N, d, scale, stream))
 
 
 def fa_forward_fp32(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
@@ -200,6 +207,38 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, want_lse=True
           torch.float32: fa_forward_fp32}[q.dtype]
     fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, float(scale), bool(causal),
        _stream(q))
+    return out, lse
+
+
+def forward_masked(q, k, v, mask, scale=None, out=None, lse=None):
+    """Exact attention with a boolean mask on bf16 [B,H,N,d] CUDA tensors.
+    mask: bool or uint8 CUDA tensor, [N,N] (shared) or [B,H,N,N] (nonzero =
+    visible).  Returns (O, LSE); rows with no visible key give O = 0,
+    LSE = -inf."""
+    import torch
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B,H,N,d] shape")
+    for t in (q, k, v):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16):
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    B, H, N, d = q.shape
+    m = mask.to(torch.uint8) if mask.dtype == torch.bool else mask
+    if not (m.is_cuda and m.is_contiguous() and m.dtype == torch.uint8):
+        raise ValueError("mask must be a contiguous bool or uint8 CUDA tensor")
+    if tuple(m.shape) == (N, N):
+        stride = 0
+    elif tuple(m.shape) == (B, H, N, N):
+        stride = N * N
+    else:
+        raise ValueError("mask must be [N,N] or [B,H,N,N]")
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_forward_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(m), stride, B, H, N,
+                      d, float(scale), _stream(q))
     return out, lse
 
 

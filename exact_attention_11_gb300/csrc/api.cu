@@ -196,9 +196,11 @@ const char *fa_status_string(int status) {
 }
 
 namespace {
-// fa_forward and fa_forward_f16: the tensor-core forward for 16-bit inputs.
+// fa_forward, fa_forward_f16 and fa_forward_masked: the tensor-core forward
+// for 16-bit inputs.
 int forward16(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
-              int N, int d, float scale, int causal, fa_stream_t stream, bool f16) {
+              int N, int d, float scale, int causal, fa_stream_t stream, bool f16,
+              const uint8_t *mask = nullptr, long long mask_bh_stride = 0) {
   int rc = check_forward_args(q, k, v, o, lse, B, H, N, d, scale);
   if (rc != FA_OK) return rc;
   const int BH = B * H;
@@ -222,7 +224,8 @@ int forward16(const void *q, const void *k, const void *v, void *o, float *lse, 
   if ((rc = encode_qkv_map(&tv, v, BH, N, d, 128, dt)) != FA_OK) return rc;
   return cuda_status(launch_fwd_bf16(tq, tk, tv, o, lse, BH, N, d, scale, causal ? 1 : 0, sched,
                                      g_dev[dev].status, fault_cta,
-                                     reinterpret_cast<cudaStream_t>(stream), f16));
+                                     reinterpret_cast<cudaStream_t>(stream), f16, mask,
+                                     static_cast<int64_t>(mask_bh_stride)));
 }
 }  // namespace
 
@@ -234,6 +237,16 @@ int fa_forward(const void *q, const void *k, const void *v, void *o, float *lse,
 int fa_forward_f16(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                    int H, int N, int d, float scale, int causal, fa_stream_t stream) {
   return forward16(q, k, v, o, lse, B, H, N, d, scale, causal, stream, true);
+}
+
+int fa_forward_masked(const void *q, const void *k, const void *v, void *o, float *lse,
+                      const void *mask, long long mask_bh_stride, int B, int H, int N, int d,
+                      float scale, fa_stream_t stream) {
+  if (!mask || mask_bh_stride < 0) return FA_ERR_INVALID_ARG;
+  if (!aligned16(mask) || mask_bh_stride % 16 != 0) return FA_ERR_ALIGNMENT;
+  if (N % 16 != 0) return FA_ERR_UNSUPPORTED;
+  return forward16(q, k, v, o, lse, B, H, N, d, scale, 0, stream, false,
+                   static_cast<const uint8_t *>(mask), mask_bh_stride);
 }
 
 int fa_forward_fp32(const float *q, const float *k, const float *v, float *o, float *lse, int B,

@@ -152,14 +152,18 @@ struct ItemDecoder {
   }
 };
 
-template <int D, bool F16>
+// MASK: a boolean mask decides visibility -- key j is visible to query row i
+// of head bh iff mask[bh * mask_bh_stride + i * N + j] != 0 (N a multiple of 16;
+// causal is then 0).  A row that sees no key gets O = 0 and LSE = -inf.
+template <int D, bool F16, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, uint16_t *__restrict__ o,
                        float *__restrict__ lse, int N, int BH, int n_qblocks, float scale_log2,
                        int causal, int *__restrict__ sched, int *__restrict__ dev_status,
-                       int fault_cta) {
+                       int fault_cta, const uint8_t *__restrict__ mask,
+                       int64_t mask_bh_stride) {
   using C = Cfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -449,6 +453,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_mine = t ? n_b : n_a;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < n_mine; ++j, ++sc) {
+        // MASK: this row's 128 mask bytes for key tile j, fetched before the
+        // wait for the scores (chunks past N read as "not visible").
+        uint4 mk[8];
+        if (MASK) {
+          const int kb0 = j * BN;
+          const uint8_t *mr = mask + static_cast<int64_t>(bh) * mask_bh_stride +
+                              static_cast<int64_t>(min(row, N - 1)) * N + kb0;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            mk[c] = (kb0 + 16 * c < N) ? *reinterpret_cast<const uint4 *>(mr + 16 * c)
+                                       : make_uint4(0u, 0u, 0u, 0u);
+        }
         if (!(ok = mbar_wait(bar(kBarSFull + t), sc & 1, abort_flag))) break;
         tc_fence_after();
         uint32_t sv[4][32];
@@ -457,7 +473,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_wait_ld(sv[c]);
 #define S_(c) sv[(c) >> 5][(c) & 31]
-        if (j == n_mine - 1) {
+        if (MASK) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) {
+            const uint32_t w = (&mk[c >> 4].x)[(c >> 2) & 3];
+            if (((w >> (8 * (c & 3))) & 0xffu) == 0u) S_(c) = __float_as_uint(-INFINITY);
+          }
+        } else if (j == n_mine - 1) {
           // Keys past the sequence end, and (causal) keys after the query row.
           const int lim = (causal ? min(N, row + 1) : N) - j * BN;
 #pragma unroll
@@ -498,7 +520,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(o_tmem + c * 32, ov);
           }
         }
-        const uint64_t nm2 = f2(-m, -m);
+        // While a masked row has seen no visible key, m is -inf: use 0 so that
+        // the (all masked) scores give p = 0 rather than NaN.
+        const float mref = (MASK && m == -INFINITY) ? 0.f : m;
+        const uint64_t nm2 = f2(-mref, -mref);
         uint64_t sum2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -529,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Epilogue: O_T / l as bf16 rows and the LSE, once the last PV_T is done.
       if (!(ok = mbar_wait(bar(kBarODone + t), it & 1, abort_flag))) break;
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = (MASK && l == 0.f) ? 0.f : 1.f / l;
       uint16_t *orow = o + (static_cast<int64_t>(bh) * N + row) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -554,7 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (lse != nullptr && row < N)
-        lse[static_cast<int64_t>(bh) * N + row] = (m + __log2f(l)) * 0.6931471805599453f;
+        lse[static_cast<int64_t>(bh) * N + row] =
+            (MASK && l == 0.f) ? -INFINITY : (m + __log2f(l)) * 0.6931471805599453f;
       ++it;
     }
   }
@@ -580,10 +606,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int g_num_sms[64] = {};
 
-template <int D, bool F16>
+template <int D, bool F16, bool MASK>
 cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, void *o,
                      float *lse, int BH, int N, float scale, int causal, int *sched,
-                     int *dev_status, int fault_cta, cudaStream_t stream) {
+                     int *dev_status, int fault_cta, cudaStream_t stream, const uint8_t *mask,
+                     int64_t mask_bh_stride) {
   using C = Cfg<D>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -595,16 +622,16 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
     if (e != cudaSuccess) return e;
     g_num_sms[dev] = n;
   }
-  e = cudaFuncSetAttribute(fwd_bf16_tc_kernel<D, F16>,
+  e = cudaFuncSetAttribute(fwd_bf16_tc_kernel<D, F16, MASK>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_qblocks = (N + 2 * BM - 1) / (2 * BM);
   const long long n_items = static_cast<long long>(n_qblocks) * BH;
   const int grid = static_cast<int>(n_items < g_num_sms[dev] ? n_items : g_num_sms[dev]);
   const float scale_log2 = scale * 1.4426950408889634f;
-  fwd_bf16_tc_kernel<D, F16><<<grid, kThreads, C::kAlloc, stream>>>(
+  fwd_bf16_tc_kernel<D, F16, MASK><<<grid, kThreads, C::kAlloc, stream>>>(
       tq, tk, tv, reinterpret_cast<uint16_t *>(o), lse, N, BH, n_qblocks, scale_log2, causal,
-      sched, dev_status, fault_cta);
+      sched, dev_status, fault_cta, mask, mask_bh_stride);
   return cudaGetLastError();
 }
 
@@ -613,16 +640,21 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
 cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             void *o, float *lse, int BH, int N, int d, float scale, int causal,
                             int *sched, int *dev_status, int fault_cta, cudaStream_t stream,
-                            bool f16) {
+                            bool f16, const uint8_t *mask, int64_t mask_bh_stride) {
+#define FATTN_FWD_ARGS \
+  tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status, fault_cta, stream, mask, \
+      mask_bh_stride
+  if (mask != nullptr) {
+    if (f16) return cudaErrorInvalidValue;   // masks are served for bf16 only
+    return d == 64 ? launch_d<64, false, true>(FATTN_FWD_ARGS)
+                   : launch_d<128, false, true>(FATTN_FWD_ARGS);
+  }
   if (d == 64)
-    return f16 ? launch_d<64, true>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status,
-                                    fault_cta, stream)
-               : launch_d<64, false>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status,
-                                     fault_cta, stream);
-  return f16 ? launch_d<128, true>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status,
-                                   fault_cta, stream)
-             : launch_d<128, false>(tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status,
-                                    fault_cta, stream);
+    return f16 ? launch_d<64, true, false>(FATTN_FWD_ARGS)
+               : launch_d<64, false, false>(FATTN_FWD_ARGS);
+  return f16 ? launch_d<128, true, false>(FATTN_FWD_ARGS)
+             : launch_d<128, false, false>(FATTN_FWD_ARGS);
+#undef FATTN_FWD_ARGS
 }
 
 }  // namespace fattn

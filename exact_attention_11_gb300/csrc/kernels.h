@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstddef>
+#include <cstdint>
 
 namespace fattn {
 
@@ -24,10 +25,13 @@ constexpr int kFwdSchedSlots = 64;
 // fault_cta >= 0 makes that CTA's producer stop after its first Q loads (the
 // failure-path test); -1 in normal use.
 // f16 selects fp16 Q, K, V, O (tensor maps of CU_TENSOR_MAP_DATA_TYPE_FLOAT16).
+// mask (bf16 only, causal 0, N a multiple of 16): uint8, key j visible to row i
+// of head bh iff mask[bh * mask_bh_stride + i * N + j] != 0.
 cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             void *o, float *lse, int BH, int N, int d, float scale, int causal,
                             int *sched, int *dev_status, int fault_cta, cudaStream_t stream,
-                            bool f16 = false);
+                            bool f16 = false, const uint8_t *mask = nullptr,
+                            int64_t mask_bh_stride = 0);
 
 // Backward: workspace = fp32 dQ accumulator (row-major [BH][N][d] inside
 // B*H*Npad*d floats, Npad = N rounded up to 128), then [-LSE2 | -D] (2 x 128

@@ -86,6 +86,23 @@ int fa_forward_f16(const void *q, const void *k, const void *v, void *o, float *
                    fa_stream_t stream);
 
 /*
+ * fa_forward_masked -- fa_forward with a boolean attention mask in place of
+ * the causal flag ("FlashAttention: GPU 메모리 계층을 활용한 어텐션 최적화 분석",
+ * youngju.dev, section 11.3: a custom boolean attn_mask, True = the key takes
+ * part).  Key j is visible to query row i of head bh = b * H + h iff
+ *     mask[bh * mask_bh_stride + i * N + j] != 0;
+ * mask_bh_stride = 0 shares one [N, N] mask across batch and heads, N * N
+ * gives every head its own.  mask is uint8, 16-byte aligned, N must be a
+ * multiple of 16 (else FA_ERR_UNSUPPORTED) and mask_bh_stride a multiple of
+ * 16 (else FA_ERR_ALIGNMENT).  A row with no visible key gets o = 0 and
+ * lse = -inf.  Every key tile is computed (no tile is skipped for being fully
+ * masked).  Other arguments, layouts and errors as for fa_forward (bf16).
+ */
+int fa_forward_masked(const void *q, const void *k, const void *v, void *o, float *lse,
+                      const void *mask, long long mask_bh_stride, int B, int H, int N, int d,
+                      float scale, fa_stream_t stream);
+
+/*
  * fa_forward_fp32 -- the same operation and contract as fa_forward with fp32
  * q, k, v and o (every product and sum in fp32 on the CUDA cores, no reduced
  * precision anywhere).  d is 64 or 128.

@@ -125,6 +125,18 @@ def test_backward_workspace_size(lib):
     assert fa.fa_backward_workspace_bytes(0, 4, 64, 64) == 0
 
 
+@pytest.mark.parametrize("mask,stride,N,expect", [
+    (NULL, 0, 64, -1),       # no mask
+    (P, -16, 64, -1),        # negative stride
+    (P + 8, 0, 64, -3),      # misaligned mask
+    (P, 8, 64, -3),          # stride not a multiple of 16
+    (P, 0, 40, -2),          # N not a multiple of 16
+    (P, 0, 0, 0),            # N = 0: no-op
+])
+def test_masked_forward_argument_checks(lib, mask, stride, N, expect):
+    assert lib.fa_forward_masked(P, P, P, P, NULL, mask, stride, 1, 1, N, 64, 0.125, None) == expect
+
+
 def test_valid_call_without_gpu_fails_loudly(lib):
     import torch
     if torch.cuda.is_available():
