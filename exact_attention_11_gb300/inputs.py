@@ -9,6 +9,9 @@ Recipes (one per workload shape used by the library's tests and benchmark):
 
 * forward: Q, K, V drawn in that order, iid N(0, 1) scaled by ``amp`` in fp32,
   shape [B, H, N, d].
+* forward with outliers: as above, then a seeded 0.1% of the entries of each
+  tensor multiplied by 10 (the pages give no recipe for outlier inputs).
+* rotation signs: d iid fair signs, fp32 +-1.
 * paged decode: q [S, H, D] ~ N(0,1); k_cache [nb, H, D/x, bs, x] and v_cache
   [nb, H, D, bs] ~ N(0,1); context_lens ~ U{1..max_ctx}; block_tables is a
   random permutation of the nb = S * max_blocks physical blocks, viewed as
@@ -46,6 +49,29 @@ def grad_output(B: int, H: int, N: int, d: int, dtype=torch.bfloat16, seed: int 
     to ``dtype`` (drawn from its own seed stream, distinct from Q, K, V)."""
     g = torch.Generator(device="cpu").manual_seed(seed + 0x5EED)
     return _randn((B, H, N, d), g).to(dtype).to(device)
+
+
+def outlier_inputs(B: int, H: int, N: int, d: int, dtype=torch.bfloat16, seed: int = 0,
+                   frac: float = 1e-3, amp: float = 10.0, device="cpu"):
+    """Q, K, V like :func:`forward_inputs`, with a seeded fraction ``frac`` of
+    the entries of each scaled by ``amp``: the few large-magnitude values that
+    hurt a per-block 8-bit scale."""
+    g = torch.Generator(device="cpu").manual_seed(seed + 0x0F7)
+    out = []
+    for _ in range(3):
+        t = _randn((B, H, N, d), g)
+        sel = torch.rand((B, H, N, d), generator=g) < frac
+        t = torch.where(sel, t * amp, t)
+        out.append(t.to(dtype).to(device))
+    return tuple(out)
+
+
+def rotation_signs(d: int, seed: int = 0, device="cpu"):
+    """d random signs (+1.0 / -1.0, fp32): the diagonal of the random
+    orthogonal transform used before FP8 quantization."""
+    g = torch.Generator(device="cpu").manual_seed(seed + 0x51C)
+    bits = torch.randint(0, 2, (d,), generator=g)
+    return (1.0 - 2.0 * bits.to(torch.float32)).to(device)
 
 
 def sample_rows(N: int, count: int, seed: int):

@@ -15,6 +15,8 @@ Parity status: the forward definition is pinned by brute force, by a library
 special case (PyTorch's float64 math SDPA) and by closed-form invariants; the
 paged decode gather is pinned by an independent scatter and by the worked
 layout numbers of the PagedAttention page.  See ``tests/test_oracle_pins.py``.
+The FP8 quantization and the FP8 forward's reference live in ``fp8.py``, pinned
+by ``tests/test_oracle_fp8.py``.
 """
 from __future__ import annotations
 

@@ -1,0 +1,198 @@
+"""Checks that pin the FP8 part of the oracle (``oracle/fp8.py``) to facts
+outside itself.
+
+Every ``check_*`` takes the module under test, so that
+``test_oracle_fp8.py`` can run the same checks on the oracle and on copies of
+it with a plausible mistake planted in them.  The facts used:
+
+* the E4M3 format, from its definition and from PyTorch's own float32 ->
+  float8_e4m3fn conversion (a library routine that rounds to nearest even);
+* values worked out by hand from that definition;
+* the Sylvester-Hadamard matrix as SciPy builds it, and the orthogonality of
+  diag(sigma) H / sqrt(d);
+* closed-form properties of per-block scaling (the largest value of a block
+  maps to +-448, every value is reproduced within half an E4M3 step);
+* the error of E4M3 softmax weights, simulated directly, against the bound the
+  oracle reports;
+* the claim of "FlashAttention: GPU 메모리 계층을 활용한 어텐션 최적화 분석"
+  (youngju.dev, section 9.2, item 3) that the random orthogonal transform
+  lowers the FP8 error when the inputs have outliers.
+"""
+from __future__ import annotations
+
+import numpy as np
+import scipy.linalg
+import torch
+
+import oracle
+from exact_attention_11_gb300 import inputs
+
+
+def _e4m3_torch(x) -> np.ndarray:
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).to(torch.float32).double().numpy()
+
+
+def _codebook() -> np.ndarray:
+    c = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().double().numpy()
+    return c
+
+
+def check_e4m3_codebook(f):
+    """Every finite E4M3 value is its own rounding; there are 126 positive
+    ones, the largest 448 and the smallest 2^-9; values above 448 saturate."""
+    c = _codebook()
+    fin = c[np.isfinite(c)]
+    assert np.array_equal(f.e4m3_round(fin), fin)
+    pos = np.unique(fin[fin > 0])
+    assert len(pos) == 126 and pos.max() == 448.0 and pos.min() == 2.0 ** -9
+    assert np.array_equal(f.e4m3_round([449.0, 463.9, 500.0, 1e6, -1e6]),
+                          [448.0, 448.0, 448.0, 448.0, -448.0])
+
+
+def check_e4m3_ties_to_even(f):
+    """The midpoint of two neighbouring E4M3 values rounds to the one whose
+    code has an even last bit."""
+    c = _codebook()
+    codes = np.arange(1, 0x7E)            # positive finite codes, consecutive values
+    lo, hi = c[codes], c[codes + 1]
+    mid = (lo + hi) / 2.0
+    want = np.where(codes % 2 == 0, lo, hi)
+    assert np.array_equal(f.e4m3_round(mid), want)
+    assert np.array_equal(f.e4m3_round(-mid), -want)
+
+
+def check_e4m3_matches_library(f):
+    """Random fp32 values of every magnitude in (-448, 448): the same values as
+    PyTorch's conversion to float8_e4m3fn."""
+    r = np.random.default_rng(3)
+    x = (r.standard_normal(20000) * np.exp2(r.uniform(-14, 8.7, 20000))).astype(np.float32)
+    x = x[np.abs(x) < 448]
+    assert np.array_equal(f.e4m3_round(x), _e4m3_torch(x))
+
+
+def check_e4m3_hand_values(f):
+    """Worked by hand: 17 is halfway between 16 and 18 (step 2) and goes to
+    16 (even code); 0.3 lies in [0.25, 0.5) where the step is 1/32, and
+    0.3 * 32 = 9.6 rounds to 10: 0.3125; -5.5 is exact (step 1/2 in [4, 8));
+    2^-10 is halfway between 0 and 2^-9 and goes to 0; 1.5 * 2^-10 goes to
+    2^-9; 0.1 = 1.6 * 2^-4, 1.6 * 8 = 12.8 -> 13: 13/8 * 2^-4 = 0.1015625."""
+    got = f.e4m3_round([17.0, 0.3, -5.5, 2.0 ** -10, 1.5 * 2.0 ** -10, 0.1])
+    assert np.array_equal(got, [16.0, 0.3125, -5.5, 0.0, 2.0 ** -9, 0.1015625])
+
+
+def check_hadamard_is_sylvester_product(f):
+    """The butterfly equals (x * sigma) @ H with SciPy's Sylvester-Hadamard
+    matrix; small integers keep every fp32 sum exact."""
+    r = np.random.default_rng(4)
+    for d in (2, 4, 8, 64, 128):
+        x = r.integers(-8, 9, size=(3, 5, d)).astype(np.float32)
+        sig = inputs.rotation_signs(d, seed=d).numpy()
+        want = (x.astype(np.float64) * sig) @ scipy.linalg.hadamard(d)
+        assert np.array_equal(f.hadamard_rows(x, sig).astype(np.float64), want)
+
+
+def check_block_scales_closed_form(f):
+    """Per 128-row block: scale = fp32(amax / 448) (computed here with
+    PyTorch's fp32 division), the block's largest entry maps to +-448, every
+    entry is reproduced within half an E4M3 step, and a block of zeros gets
+    scale 1 and zero codes.  N = 300 has a ragged third block."""
+    B, H, N, d = 2, 3, 300, 64
+    q, _, _ = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=12)
+    q = q.float()
+    q[1, 2, 128:256] = 0.0
+    codes, scales = f.quantize_rows(q.numpy())
+    assert scales.shape == (B, H, 3) and scales.dtype == np.float32
+    for blk, sl in enumerate((slice(0, 128), slice(128, 256), slice(256, 300))):
+        amax = q[:, :, sl].abs().amax(dim=(2, 3))
+        want = torch.where(amax == 0, torch.ones_like(amax), amax / torch.tensor(448.0))
+        assert np.array_equal(scales[:, :, blk], want.numpy())
+        blk_codes = codes[:, :, sl]
+        top = np.abs(blk_codes).reshape(B, H, -1).max(axis=2)
+        assert np.all((top == 448.0) | (amax.numpy() == 0))
+    deq = f.dequantize_rows(codes, scales)
+    x = q.double().numpy()
+    s = scales[:, :, np.arange(N) // 128][..., None].astype(np.float64)
+    assert np.all(np.abs(deq - x) <= 2.0 ** -4 * np.abs(x) + 2.0 ** -10 * s)
+    assert np.all(codes[1, 2, 128:256] == 0) and scales[1, 2, 1] == 1.0
+    vc, vs = f.quantize_heads(q.numpy())
+    amax = q.abs().amax(dim=(2, 3))
+    assert vs.shape == (B, H) and np.array_equal(vs, (amax / torch.tensor(448.0)).numpy())
+
+
+def check_rotation_is_orthogonal_transform(f):
+    """With signs, codes times scales reproduce the rows of Q diag(sigma) H /
+    sqrt(d) (computed here in float64 from SciPy's matrix) within half an E4M3
+    step; V is not rotated and keeps one scale per head."""
+    B, H, N, d = 1, 2, 200, 128
+    q, k, v = (t.float().numpy() for t in inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=13))
+    sig = inputs.rotation_signs(d, seed=1).numpy()
+    M = np.diag(sig.astype(np.float64)) @ scipy.linalg.hadamard(d) / np.sqrt(d)
+    assert np.allclose(M @ M.T, np.eye(d), atol=1e-14)
+    qd, kd, vd = f.dequantized(q, k, v, sig)
+    for x, xd in ((q, qd), (k, kd)):
+        xm = x.astype(np.float64) @ M
+        s = np.abs(xm).reshape(B, H, -1).max(axis=2)[..., None, None] / 448.0
+        assert np.all(np.abs(xd - xm) <= 2.0 ** -4 * np.abs(xm) + 2.0 ** -10 * s * 1.001)
+    _, _, vd_plain = f.dequantized(q, k, v, None)
+    assert np.array_equal(vd, vd_plain)
+    # V: one scale per head, fp32(amax / 448): vd / scale is on the E4M3 grid.
+    vs = (torch.as_tensor(v).abs().amax(dim=(2, 3)) / torch.tensor(448.0)).double().numpy()
+    vc = vd / vs[:, :, None, None]
+    assert np.array_equal(f.e4m3_round(vc), vc)
+    assert np.all(np.abs(vc).reshape(B, H, -1).max(axis=2) == 448.0)
+
+
+def check_weight_rounding_within_bound(f):
+    """Simulate the kernel's E4M3 softmax weights (p * 2^4, rounded) on the
+    dequantized inputs: the error against exact attention stays inside the
+    reported bound everywhere, and its typical size matches ``sigma``."""
+    B, H, N, d = 1, 2, 384, 64
+    q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=14)
+    scale = d ** -0.5
+    o, lse, bound, sigma = f.forward_fp8_reference(q, k, v, scale, True)
+    qd, kd, vd = f.dequantized(q, k, v)
+    sim = np.zeros_like(o)
+    for h in range(H):
+        s = scale * (qd[0, h] @ kd[0, h].T)
+        s = np.where(np.tril(np.ones((N, N), dtype=bool)), s, -np.inf)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        pr = f.e4m3_round(p * 16.0) / 16.0
+        sim[0, h] = (pr @ vd[0, h]) / p.sum(axis=1, keepdims=True)
+    err = np.abs(sim - o)
+    assert np.all(err <= bound)
+    ratio = np.sqrt(np.mean((err / sigma) ** 2))
+    assert 0.2 < ratio < 1.0, ratio
+    ro, rl = oracle.attention_forward(qd, kd, vd, scale, True)
+    assert np.array_equal(o, ro) and np.array_equal(lse, rl)
+
+
+def check_incoherent_processing_helps_with_outliers(f):
+    """Inputs with a few large entries: FP8 with the random orthogonal
+    transform is closer to exact attention on the unquantized inputs than FP8
+    without it.  The page reports a 2.6x lower error without giving its input
+    distribution or its baseline; on these inputs (0.1% of entries x10) the
+    gain is about 1.4x, and the margin asked here is 1.2x."""
+    B, H, N, d = 1, 2, 512, 128
+    q, k, v = inputs.outlier_inputs(B, H, N, d, torch.bfloat16, seed=15)
+    scale = d ** -0.5
+    exact, _ = oracle.attention_forward(q, k, v, scale, False)
+    sig = inputs.rotation_signs(d, seed=2).numpy()
+    o_plain, _, _, _ = f.forward_fp8_reference(q, k, v, scale, False)
+    o_rot, _, _, _ = f.forward_fp8_reference(q, k, v, scale, False, signs=sig)
+    e_plain = np.sqrt(np.mean((o_plain - exact) ** 2))
+    e_rot = np.sqrt(np.mean((o_rot - exact) ** 2))
+    assert e_plain > 1.2 * e_rot, (e_plain, e_rot)
+
+
+ALL_CHECKS = [
+    check_e4m3_codebook,
+    check_e4m3_ties_to_even,
+    check_e4m3_matches_library,
+    check_e4m3_hand_values,
+    check_hadamard_is_sylvester_product,
+    check_block_scales_closed_form,
+    check_rotation_is_orthogonal_transform,
+    check_weight_rounding_within_bound,
+    check_incoherent_processing_helps_with_outliers,
+]
