@@ -16,6 +16,8 @@ Printed JSON line (rank 0):
   roofline       the forward (dominant kernel) against the measured bf16 peak
   fwd_f16        fa_forward_f16 on the forward workload in fp16 (same FLOPs)
   fwd_masked     fa_forward_masked with the tril mask on the forward workload
+  fwd_fp8        fa_forward_fp8 on the forward workload quantized to E4M3 by
+                 fa_quantize_fp8 (timed separately), against 2x the bf16 peak
   backward       fa_backward (dQ, dK, dV) of the forward workload, TFLOP/s with
                  FLOPs = 2.5 x the forward's, and its own roofline
   decode_gqa     fa_paged_decode_gqa on the decode's sequences with 8 key/value
@@ -333,6 +335,46 @@ def gpu_arm(args):
     stream.synchronize()
     masked_ms = sum(e[0].elapsed_time(e[1]) for e in mev) / km
     del tril
+
+    # The FP8 forward on the same workload: the inputs are block-quantized to
+    # E4M3 once (fa_quantize_fp8), then fa_forward_fp8 is timed the same way,
+    # and the quantization on its own; reported as "fwd_fp8".
+    x8 = fa.quantize_fp8(q, k, v)
+    qws = torch.empty((max(fa.fa_quantize_fp8_workspace_bytes(B, H, N, d), 16),),
+                      dtype=torch.uint8, device=dev)
+
+    def run_fp8():
+        fa.fa_forward_fp8(x8.q8.data_ptr(), x8.k8.data_ptr(), x8.vt8.data_ptr(),
+                          x8.q_scale.data_ptr(), x8.k_scale.data_ptr(), x8.v_scale.data_ptr(),
+                          o.data_ptr(), lse.data_ptr(), B, H, N, d, scale, causal, sptr)
+
+    def run_quant():
+        fa.fa_quantize_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), None, x8.q8.data_ptr(),
+                           x8.k8.data_ptr(), x8.vt8.data_ptr(), x8.q_scale.data_ptr(),
+                           x8.k_scale.data_ptr(), x8.v_scale.data_ptr(), B, H, N, d,
+                           qws.data_ptr(), qws.numel(), sptr)
+
+    kq = max(3, min(K // 4, 100))
+    qev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(kq)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush.zero_()
+            run_quant()
+            flush.zero_()
+            run_fp8()
+        for i in range(kq):
+            flush.zero_()
+            qev[i][0].record(stream)
+            run_fp8()
+            qev[i][1].record(stream)
+            flush.zero_()
+            qev[i][2].record(stream)
+            run_quant()
+            qev[i][3].record(stream)
+    stream.synchronize()
+    fp8_ms = sum(e[0].elapsed_time(e[1]) for e in qev) / kq
+    quant_ms = sum(e[2].elapsed_time(e[3]) for e in qev) / kq
+    del x8, qws
     with torch.cuda.stream(stream):
         run_fwd()   # o, lse of the causal forward again (the backward uses them)
 
@@ -553,6 +595,23 @@ def gpu_arm(args):
             "unit": "TFLOP/s",
             "frac_of_bf16_peak": round(flops / (masked_ms * 1e-3) / 1e12 / peak_t, 4),
         },
+        "fwd_fp8": {
+            "workload": "fa_forward_fp8 on the forward workload block-quantized to E4M3 "
+                        "(fa_quantize_fp8: 128-row blocks for Q and K, per-head V; no "
+                        "transform), bf16 output",
+            "ms": round(fp8_ms, 4),
+            "value": round(weak_scaling_rate(flops, ws, fp8_ms, 1e12), 2),
+            "unit": "TFLOP/s",
+            "quantize_ms": round(quant_ms, 4),
+            "value_with_quantize": round(weak_scaling_rate(flops, ws, fp8_ms + quant_ms, 1e12), 2),
+            "roofline": {"bound": "tensor",
+                         "achieved": round(weak_scaling_rate(flops, 1, fp8_ms, 1e12), 2),
+                         "peak": round(2 * peak_t, 1), "unit": "TFLOP/s",
+                         "frac": round(weak_scaling_rate(flops, 1, fp8_ms, 1e12) / (2 * peak_t), 4),
+                         "traffic": None,
+                         "peak_kind": f"{peak_kind} bf16 burst x 2 (nominal fp8/bf16 ratio)",
+                         "kernel": "fwd_bf16_tc_kernel<128,0,0,1> (E4M3)"},
+        },
         "backward": {
             "workload": "fa_backward bf16 B=2 H=16 N=4096 d=128 causal (dQ, dK, dV of the "
                         "forward workload, upstream gradient N(0,1))",
@@ -602,7 +661,8 @@ def gpu_arm(args):
                         "in, compute and copies out on three streams over two device slots "
                         "(step i+1's inputs arrive while step i computes)"},
         # library kernels inside timed regions (a backward is three launches)
-        "gpu_launches": 2 * K + kl + kf + km + 3 * kb + kg + 2 * ke,  # e2e: ke fwd + ke decodes
+        # fwd_fp8: kq forwards + kq quantizations of two launches each
+        "gpu_launches": 2 * K + kl + kf + km + 3 * kq + 3 * kb + kg + 2 * ke,
         "clocks": clk,
         "device_status": status,
         "wall_s": round(wall, 3),

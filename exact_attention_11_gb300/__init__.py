@@ -18,7 +18,8 @@ import threading
 
 __all__ = ["fa_forward", "fa_forward_f16", "fa_forward_masked", "forward_masked", "fa_forward_fp32", "fa_paged_decode", "fa_paged_decode_noalloc",
            "fa_backward", "fa_backward_workspace_bytes", "backward", "fa_paged_decode_gqa",
-           "fa_status_string",
+           "fa_status_string", "fa_quantize_fp8", "fa_quantize_fp8_workspace_bytes",
+           "fa_fp8_vt_stride", "fa_forward_fp8", "quantize_fp8", "forward_fp8", "Fp8Inputs",
            "fa_device_status", "fa_release", "forward", "paged_decode", "FattnError",
            "library_path", "load"]
 
@@ -57,6 +58,10 @@ EXPORTS = {
     "fa_backward_workspace_bytes": ([_i, _i, _i, _i], ctypes.c_ulonglong),
     "fa_backward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp,
                      ctypes.c_ulonglong, _vp], _i),
+    "fa_quantize_fp8_workspace_bytes": ([_i, _i, _i, _i], ctypes.c_ulonglong),
+    "fa_fp8_vt_stride": ([_i], ctypes.c_longlong),
+    "fa_quantize_fp8": ([_vp] * 10 + [_i, _i, _i, _i, _vp, ctypes.c_ulonglong, _vp], _i),
+    "fa_forward_fp8": ([_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_status_string": ([_i], ctypes.c_char_p),
     "fa_device_status": ([], _i),
     "fa_release": ([], None),
@@ -150,6 +155,27 @@ def fa_backward(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, wo
     return _check("fa_backward", load().fa_backward(
         q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, int(causal), workspace,
         workspace_bytes, stream))
+
+
+def fa_quantize_fp8_workspace_bytes(B, H, N, d) -> int:
+    return int(load().fa_quantize_fp8_workspace_bytes(B, H, N, d))
+
+
+def fa_fp8_vt_stride(N) -> int:
+    return int(load().fa_fp8_vt_stride(N))
+
+
+def fa_quantize_fp8(q, k, v, signs, q8, k8, vt8, q_scale, k_scale, v_scale, B, H, N, d,
+                    workspace, workspace_bytes, stream) -> int:
+    return _check("fa_quantize_fp8", load().fa_quantize_fp8(
+        q, k, v, signs, q8, k8, vt8, q_scale, k_scale, v_scale, B, H, N, d, workspace,
+        workspace_bytes, stream))
+
+
+def fa_forward_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, B, H, N, d, scale, causal,
+                   stream) -> int:
+    return _check("fa_forward_fp8", load().fa_forward_fp8(
+        q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, B, H, N, d, scale, int(causal), stream))
 
 
 def fa_status_string(status: int) -> str:
@@ -299,3 +325,70 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale=None, ou
                             _ptr(context_lens), _ptr(out), S, H, Hk, D, bs,
                             block_tables.shape[1], float(scale), _stream(q))
     return out
+
+
+class Fp8Inputs:
+    """E4M3 codes and dequantization scales of one attention problem, in the
+    layouts of fa_quantize_fp8: q8, k8 uint8 [B,H,N,d]; vt8 uint8 [B,H,d,Npad]
+    (V transposed); q_scale, k_scale fp32 [B,H,ceil(N/128)]; v_scale fp32
+    [B,H]."""
+
+    def __init__(self, q8, k8, vt8, q_scale, k_scale, v_scale, shape):
+        self.q8, self.k8, self.vt8 = q8, k8, vt8
+        self.q_scale, self.k_scale, self.v_scale = q_scale, k_scale, v_scale
+        self.shape = tuple(shape)
+
+
+def quantize_fp8(q, k, v, signs=None, workspace=None, out=None):
+    """Block-quantizes bf16 [B,H,N,128] CUDA tensors to E4M3 (fa_quantize_fp8).
+    ``signs``: optional fp32 CUDA tensor of 128 values +-1 for the random
+    orthogonal transform of q and k.  ``out``: an Fp8Inputs of the same shape
+    to write into.  Returns an Fp8Inputs.  Runs on the current torch stream."""
+    import torch
+    for t in (q, k, v):
+        if t.dim() != 4 or t.shape != q.shape:
+            raise ValueError("q, k, v must share one [B,H,N,d] shape")
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16):
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    B, H, N, d = q.shape
+    if signs is not None and not (signs.is_cuda and signs.is_contiguous()
+                                  and signs.dtype == torch.float32 and signs.numel() == d):
+        raise ValueError("signs must be a contiguous fp32 CUDA tensor of d values")
+    if out is None:
+        dev = q.device
+        nblk = (N + 127) // 128
+        npad = fa_fp8_vt_stride(N)
+        out = Fp8Inputs(torch.empty((B, H, N, d), dtype=torch.uint8, device=dev),
+                        torch.empty((B, H, N, d), dtype=torch.uint8, device=dev),
+                        torch.empty((B, H, d, npad), dtype=torch.uint8, device=dev),
+                        torch.empty((B, H, nblk), dtype=torch.float32, device=dev),
+                        torch.empty((B, H, nblk), dtype=torch.float32, device=dev),
+                        torch.empty((B, H), dtype=torch.float32, device=dev), q.shape)
+    elif out.shape != tuple(q.shape):
+        raise ValueError("out was made for another shape")
+    nbytes = fa_quantize_fp8_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=q.device)
+    fa_quantize_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(signs), _ptr(out.q8), _ptr(out.k8),
+                    _ptr(out.vt8), _ptr(out.q_scale), _ptr(out.k_scale), _ptr(out.v_scale),
+                    B, H, N, d, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                    _stream(q))
+    return out
+
+
+def forward_fp8(x, scale=None, causal=False, out=None, lse=None, want_lse=True):
+    """The FP8 forward (fa_forward_fp8) on an Fp8Inputs.  Returns (O bf16
+    [B,H,N,d], LSE fp32 [B,H,N] or None).  Runs on the current torch stream."""
+    import torch
+    B, H, N, d = x.shape
+    if scale is None:
+        scale = d ** -0.5
+    dev = x.q8.device
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    fa_forward_fp8(_ptr(x.q8), _ptr(x.k8), _ptr(x.vt8), _ptr(x.q_scale), _ptr(x.k_scale),
+                   _ptr(x.v_scale), _ptr(out), _ptr(lse), B, H, N, d, float(scale),
+                   bool(causal), _stream(x.q8))
+    return out, lse

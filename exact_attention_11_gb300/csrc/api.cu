@@ -97,6 +97,24 @@ int encode_qkv_map(CUtensorMap *m, const void *base, int BH, int N, int d, int b
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// 3-D E4M3 view {inner, rows, BH} of a [BH, rows, inner] byte tensor (inner
+// = 128 codes of a row of Q or K, or Npad keys of a row of V^T), boxes of
+// 128 x 128 x 1 with the 128-byte swizzle.  Reads past the extents give zero.
+int encode_e4m3_map(CUtensorMap *m, const void *base, int BH, int rows, int inner) {
+  const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)inner, (cuuint64_t)rows * inner};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// Keys per row of the transposed FP8 V: N rounded up to 16.
+long long fp8_vt_stride(int N) { return ((long long)N + 15) / 16 * 16; }
+
 // 3-D fp32 view {d, N, BH} of the backward's row-major dQ accumulator, boxes
 // of 32 x 32 x 1 (128-byte rows, 128-byte swizzle) for the TMA reduce-add.
 int encode_dq_acc_map(CUtensorMap *m, void *base, int BH, int N, int d) {
@@ -262,6 +280,69 @@ int fa_forward_fp32(const float *q, const float *k, const float *v, float *o, fl
     if ((rc = current_device(&dev)) != FA_OK) return rc;
   }
   return cuda_status(fattn::launch_fwd_f32(q, k, v, o, lse, BH, N, d, scale, causal ? 1 : 0,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+unsigned long long fa_quantize_fp8_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 0 || H < 0 || N < 0 || d < 0) return 0;
+  return static_cast<unsigned long long>(
+      fattn::fp8_quant_workspace_bytes(static_cast<int>((long long)B * H), N));
+}
+
+long long fa_fp8_vt_stride(int N) { return N < 0 ? 0 : fp8_vt_stride(N); }
+
+int fa_quantize_fp8(const void *q, const void *k, const void *v, const float *signs, void *q8,
+                    void *k8, void *vt8, float *q_scale, float *k_scale, float *v_scale, int B,
+                    int H, int N, int d, void *workspace, unsigned long long workspace_bytes,
+                    fa_stream_t stream) {
+  if (!q || !k || !v || !q8 || !k8 || !vt8 || !q_scale || !k_scale || !v_scale)
+    return FA_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q8) || !aligned16(k8) ||
+      !aligned16(vt8) || (signs && !aligned16(signs)))
+    return FA_ERR_ALIGNMENT;
+  const long long BH = (long long)B * H;
+  if (BH > 65535 || N > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  if (BH == 0 || N == 0) return FA_OK;
+  if (!workspace) return FA_ERR_INVALID_ARG;
+  if (workspace_bytes < fattn::fp8_quant_workspace_bytes((int)BH, N)) return FA_ERR_INVALID_ARG;
+  int dev = 0, rc;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if ((rc = current_device(&dev)) != FA_OK) return rc;
+  }
+  // The transform's 1/sqrt(d), rounded once to fp32, multiplies the scales.
+  const float rot_factor = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  return cuda_status(fattn::launch_fp8_quantize(
+      q, k, v, signs, q8, k8, vt8, q_scale, k_scale, v_scale, static_cast<float *>(workspace),
+      (int)BH, N, (int)fp8_vt_stride(N), rot_factor, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_forward_fp8(const void *q8, const void *k8, const void *vt8, const float *q_scale,
+                   const float *k_scale, const float *v_scale, void *o, float *lse, int B, int H,
+                   int N, int d, float scale, int causal, fa_stream_t stream) {
+  if (!q_scale || !k_scale || !v_scale) return FA_ERR_INVALID_ARG;
+  int rc = check_forward_args(q8, k8, vt8, o, lse, B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  const int BH = B * H;
+  if (BH == 0 || N == 0) return FA_OK;
+  int dev = 0;
+  int *sched = nullptr;
+  CUtensorMap tq, tk, tvt;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if ((rc = current_device(&dev)) != FA_OK) return rc;
+    if ((rc = get_encoder()) != FA_OK) return rc;
+    DeviceState &st = g_dev[dev];
+    sched = st.fwd_sched + 2 * (st.fwd_sched_next++ % fattn::kFwdSchedSlots);
+  }
+  if ((rc = encode_e4m3_map(&tq, q8, BH, N, d)) != FA_OK) return rc;
+  if ((rc = encode_e4m3_map(&tk, k8, BH, N, d)) != FA_OK) return rc;
+  if ((rc = encode_e4m3_map(&tvt, vt8, BH, d, (int)fp8_vt_stride(N))) != FA_OK) return rc;
+  return cuda_status(fattn::launch_fwd_fp8(tq, tk, tvt, q_scale, k_scale, v_scale, o, lse, BH, N,
+                                           scale, causal ? 1 : 0, sched, g_dev[dev].status,
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 

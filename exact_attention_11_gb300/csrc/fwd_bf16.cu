@@ -54,6 +54,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "ptx_f8.cuh"
 
 namespace fattn {
 namespace {
@@ -68,14 +69,25 @@ constexpr int kThreads = 384;       // 12 warps = 3 warpgroups
 // The build checks that ptxas gives this kernel exactly 168 at launch.
 constexpr uint32_t kRegsProducer = 88, kRegsSoftmax = 208;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+// FP8 (E4M3) variant: Q and K arrive as E4M3 codes with one scale per 128-row
+// block, V as E4M3 codes transposed to [d][keys] with one scale per head.  The
+// softmax weights are carried as E4M3 of 2^4 * exp2(x - m_ref): with the
+// output rescale skipped while the row max has grown by at most 4 (instead of
+// 8), every weight stays at or below 2^8 < 448, and weights down to 2^-10 of
+// the row max keep E4M3's full 3-bit mantissa.
+template <bool FP8>
+struct SoftmaxCfg {
+  static constexpr float kRescaleThreshold = FP8 ? 4.0f : 8.0f;  // log2 units
+  static constexpr float kPOffset = FP8 ? 4.0f : 0.0f;           // log2 of the weight scale
+};
 
-template <int D>
+template <int D, bool FP8 = false>
 struct Cfg {
-  static constexpr int kStages = D == 64 ? 4 : 2;   // K and V ring depth
-  static constexpr int kBoxes = D / 64;             // 64-column (128-byte) boxes per row
-  static constexpr int kTileBytes = BM * D * 2;     // one 128 x D bf16 tile
+  static constexpr int kElemBytes = FP8 ? 1 : 2;
+  static constexpr int kStages = (D == 64 || FP8) ? 4 : 2;   // K and V ring depth
+  static constexpr int kBoxes = D * kElemBytes / 128;        // 128-byte boxes per row
+  static constexpr int kTileBytes = BM * D * kElemBytes;     // one 128 x D tile
   static constexpr int kBoxBytes = BM * 128;        // 16 KB
   static constexpr int kQ = 0;                      // Q_A, Q_B
   static constexpr int kK0 = kQ + 2 * kTileBytes;
@@ -155,7 +167,10 @@ struct ItemDecoder {
 // MASK: a boolean mask decides visibility -- key j is visible to query row i
 // of head bh iff mask[bh * mask_bh_stride + i * N + j] != 0 (N a multiple of 16;
 // causal is then 0).  A row that sees no key gets O = 0 and LSE = -inf.
-template <int D, bool F16, bool MASK>
+// FP8: E4M3 inputs (tm_v then maps V^T, [BH][d][Npad]); q_scale and k_scale
+// hold one dequantization scale per 128-row block of each head (n_sblk per
+// head), v_scale one per head.  The output is bf16.
+template <int D, bool F16, bool MASK, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -163,8 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                        float *__restrict__ lse, int N, int BH, int n_qblocks, float scale_log2,
                        int causal, int *__restrict__ sched, int *__restrict__ dev_status,
                        int fault_cta, const uint8_t *__restrict__ mask,
-                       int64_t mask_bh_stride) {
-  using C = Cfg<D>;
+                       int64_t mask_bh_stride, const float *__restrict__ q_scale,
+                       const float *__restrict__ k_scale, const float *__restrict__ v_scale,
+                       int n_sblk) {
+  using C = Cfg<D, FP8>;
+  using SC = SoftmaxCfg<FP8>;
+  static_assert(!FP8 || (D == 128 && !F16 && !MASK), "the FP8 variant is d = 128, unmasked");
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -286,9 +305,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!(ok = mbar_wait(bar(kBarVEmpty + st), ph ^ 1, abort_flag))) break;
           mbar_arrive_expect_tx(bar(kBarVFull + st), C::kTileBytes);
-          for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(s_base + C::kV0 + st * C::kTileBytes + b * C::kBoxBytes, &tm_v, b * 64,
-                        j * BN, bh, bar(kBarVFull + st));
+          if (FP8)   // V^T: rows are the d coordinates, keys run along x
+            tma_load_3d(s_base + C::kV0 + st * C::kTileBytes, &tm_v, j * BN, 0, bh,
+                        bar(kBarVFull + st));
+          else
+            for (int b = 0; b < C::kBoxes; ++b)
+              tma_load_3d(s_base + C::kV0 + st * C::kTileBytes + b * C::kBoxBytes, &tm_v, b * 64,
+                          j * BN, bh, bar(kBarVFull + st));
           nv = kv + 1;
         }
         ++it;
@@ -304,8 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 1 && elect_one()) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc_qk = idesc16<F16>(idesc_bf16_f32(BM, BN, false));
-      constexpr uint32_t idesc_pv = idesc16<F16>(idesc_bf16_f32(BM, D, true));
+      constexpr uint32_t idesc_qk =
+          FP8 ? idesc_e4m3_f32(BM, BN) : idesc16<F16>(idesc_bf16_f32(BM, BN, false));
+      constexpr uint32_t idesc_pv =
+          FP8 ? idesc_e4m3_f32(BM, D) : idesc16<F16>(idesc_bf16_f32(BM, D, true));
       // Shared-memory descriptors are built once; moving an operand by `off`
       // bytes adds off >> 4 to the start-address field, which cannot carry
       // out of its 14 bits for addresses inside the 228 KB shared window.
@@ -313,15 +338,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the high word is the same for all three operands.
       const uint32_t dq = sdesc_lo(s_base + C::kQ, 16);
       const uint32_t dk = sdesc_lo(s_base + C::kK0, 16);
-      const uint32_t dv = sdesc_lo(s_base + C::kV0, C::kBoxBytes);
+      // V (16-bit) is read N-major: its leading offset is the box stride.
+      // V^T (FP8) is K-major like Q and K.
+      const uint32_t dv = sdesc_lo(s_base + C::kV0, FP8 ? 16 : C::kBoxBytes);
       auto qk = [&](int t, int kvi) {
         const uint32_t a = dq + ((t * C::kTileBytes) >> 4);
         const uint32_t b = dk + (((kvi % S) * C::kTileBytes) >> 4);
         const uint32_t s_col = tmem + (t ? C::kColS1 : C::kColS0);
+        if (FP8) {
+          // K = 32 codes (32 bytes) per MMA.
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss_lo(s_col, a + off, b + off, idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 32; ++kk)
+            mma_f8_ss_lo(s_col, a + kk * 2, b + kk * 2, idesc_qk, kk > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+            mma_ss_lo(s_col, a + off, b + off, idesc_qk, kk > 0 ? 1u : 0u);
+          }
         }
         mma_commit(bar(kBarSFull + t));
       };
@@ -330,10 +364,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b = dv + (((kvi % S) * C::kTileBytes) >> 4);
         const uint32_t s_col = tmem + (t ? C::kColS1 : C::kColS0);
         const uint32_t o_col = tmem + (t ? C::kColO1 : C::kColO0);
+        if (FP8) {
+          // P_T holds four codes per TMEM column: 32 keys = 8 columns.
 #pragma unroll
-        for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
-          mma_ts_lo(o_col, s_col + kk * 8, b + ((kk * 2048) >> 4), idesc_pv,
-                    (!first || kk > 0) ? 1u : 0u);
+          for (int kk = 2 * h; kk < 2 * h + 2; ++kk)
+            mma_f8_ts_lo(o_col, s_col + kk * 8, b + kk * 2, idesc_pv,
+                         (!first || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+            mma_ts_lo(o_col, s_col + kk * 8, b + ((kk * 2048) >> 4), idesc_pv,
+                      (!first || kk > 0) ? 1u : 0u);
+        }
       };
       auto wait_p = [&](int t, int h, int cnt) {
         return mbar_wait(bar(kBarPReady + 2 * t + h), cnt & 1, abort_flag);
@@ -441,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_tmem = tmem + lane_off + (t ? C::kColS1 : C::kColS0);
     const uint32_t o_tmem = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
-    const uint64_t c2 = f2(scale_log2, scale_log2);
+    uint64_t c2 = f2(scale_log2, scale_log2);
     int it = 0, sc = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -451,8 +493,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       sch.decode(w, q0, bh, n_a, n_b);
       const int row = q0 + t * BM + r_local;
       const int n_mine = t ? n_b : n_a;
+      // FP8: the scores are raw code products; this tile's Q block scale (a
+      // tile past the last block has no rows to keep) times each key tile's
+      // scale turns them into scale * q.k.
+      float q_fac = scale_log2;
+      if (FP8) {
+        const int qblk = q0 / BM + t;
+        if (qblk < n_sblk) q_fac *= q_scale[static_cast<int64_t>(bh) * n_sblk + qblk];
+      }
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < n_mine; ++j, ++sc) {
+        float c_tile = scale_log2;
+        if (FP8) {
+          c_tile = q_fac * k_scale[static_cast<int64_t>(bh) * n_sblk + j];
+          c2 = f2(c_tile, c_tile);
+        }
         // MASK: this row's 128 mask bytes for key tile j, fetched before the
         // wait for the scores (chunks past N read as "not visible").
         uint4 mk[8];
@@ -495,9 +550,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int a = 0; a < 4; ++a)
             mx[a] = fmax3(mx[a], __uint_as_float(S_(c + 2 * a)), __uint_as_float(S_(c + 2 * a + 1)));
-        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c_tile;
         float alpha = 1.f;
-        if (tmax > m + kRescaleThreshold) {  // also true while m = -inf
+        if (tmax > m + SC::kRescaleThreshold) {  // also true while m = -inf
           alpha = ex2_approx(m - tmax);
           m = tmax;
         }
@@ -523,21 +578,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         // While a masked row has seen no visible key, m is -inf: use 0 so that
         // the (all masked) scores give p = 0 rather than NaN.
         const float mref = (MASK && m == -INFINITY) ? 0.f : m;
-        const uint64_t nm2 = f2(-mref, -mref);
+        const float nmv = SC::kPOffset - mref;
+        const uint64_t nm2 = f2(nmv, nmv);
         uint64_t sum2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+        uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const uint64_t x2 =
+          for (int e = 0; e < 32; e += 4) {
+            const uint64_t xa =
                 ffma2(f2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), c2, nm2);
-            const float2 x = f2_split(x2);
+            const uint64_t xb =
+                ffma2(f2(__uint_as_float(sv[c][e + 2]), __uint_as_float(sv[c][e + 3])), c2, nm2);
+            const float2 x = f2_split(xa), y = f2_split(xb);
             const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            sum2[(e >> 1) & 1] = fadd2(sum2[(e >> 1) & 1], f2(p.x, p.y));
-            pk[e >> 1] = pack2<F16>(p.x, p.y);
+            const float2 r = make_float2(ex2_approx(y.x), ex2_approx(y.y));
+            sum2[0] = fadd2(sum2[0], f2(p.x, p.y));
+            sum2[1] = fadd2(sum2[1], f2(r.x, r.y));
+            if (FP8) {
+              // Four codes per column; columns 8(c & 1) .. 8(c & 1) + 7 of
+              // this 64-key half.
+              pk[(c & 1) * 8 + (e >> 2)] = pack_e4m3x4(p.x, p.y, r.x, r.y);
+            } else {
+              pk[e >> 1] = pack2<F16>(p.x, p.y);
+              pk[(e >> 1) + 1] = pack2<F16>(r.x, r.y);
+            }
           }
-          tmem_st16(s_tmem + c * 16, pk);
+          if (FP8) {
+            if (c & 1) tmem_st16(s_tmem + (c >> 1) * 16, pk);
+          } else {
+            tmem_st16(s_tmem + c * 16, pk);
+          }
           if (c & 1) {
             // Columns 0-63 (then 64-127) of P are in TMEM: let PV_T use them.
             tmem_wait_st();
@@ -554,7 +625,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Epilogue: O_T / l as bf16 rows and the LSE, once the last PV_T is done.
       if (!(ok = mbar_wait(bar(kBarODone + t), it & 1, abort_flag))) break;
       tc_fence_after();
-      const float inv_l = (MASK && l == 0.f) ? 0.f : 1.f / l;
+      float inv_l = (MASK && l == 0.f) ? 0.f : 1.f / l;
+      if (FP8) inv_l *= v_scale[bh];
       uint16_t *orow = o + (static_cast<int64_t>(bh) * N + row) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -580,7 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (lse != nullptr && row < N)
         lse[static_cast<int64_t>(bh) * N + row] =
-            (MASK && l == 0.f) ? -INFINITY : (m + __log2f(l)) * 0.6931471805599453f;
+            (MASK && l == 0.f) ? -INFINITY
+                               : (m - SC::kPOffset + __log2f(l)) * 0.6931471805599453f;
       ++it;
     }
   }
@@ -606,12 +679,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int g_num_sms[64] = {};
 
-template <int D, bool F16, bool MASK>
+template <int D, bool F16, bool MASK, bool FP8 = false>
 cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, void *o,
                      float *lse, int BH, int N, float scale, int causal, int *sched,
                      int *dev_status, int fault_cta, cudaStream_t stream, const uint8_t *mask,
-                     int64_t mask_bh_stride) {
-  using C = Cfg<D>;
+                     int64_t mask_bh_stride, const float *q_scale = nullptr,
+                     const float *k_scale = nullptr, const float *v_scale = nullptr) {
+  using C = Cfg<D, FP8>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -622,16 +696,17 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
     if (e != cudaSuccess) return e;
     g_num_sms[dev] = n;
   }
-  e = cudaFuncSetAttribute(fwd_bf16_tc_kernel<D, F16, MASK>,
+  e = cudaFuncSetAttribute(fwd_bf16_tc_kernel<D, F16, MASK, FP8>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_qblocks = (N + 2 * BM - 1) / (2 * BM);
   const long long n_items = static_cast<long long>(n_qblocks) * BH;
   const int grid = static_cast<int>(n_items < g_num_sms[dev] ? n_items : g_num_sms[dev]);
   const float scale_log2 = scale * 1.4426950408889634f;
-  fwd_bf16_tc_kernel<D, F16, MASK><<<grid, kThreads, C::kAlloc, stream>>>(
+  const int n_sblk = (N + BM - 1) / BM;
+  fwd_bf16_tc_kernel<D, F16, MASK, FP8><<<grid, kThreads, C::kAlloc, stream>>>(
       tq, tk, tv, reinterpret_cast<uint16_t *>(o), lse, N, BH, n_qblocks, scale_log2, causal,
-      sched, dev_status, fault_cta, mask, mask_bh_stride);
+      sched, dev_status, fault_cta, mask, mask_bh_stride, q_scale, k_scale, v_scale, n_sblk);
   return cudaGetLastError();
 }
 
@@ -655,6 +730,15 @@ cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const 
   return f16 ? launch_d<128, true, false>(FATTN_FWD_ARGS)
              : launch_d<128, false, false>(FATTN_FWD_ARGS);
 #undef FATTN_FWD_ARGS
+}
+
+cudaError_t launch_fwd_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tvt,
+                           const float *q_scale, const float *k_scale, const float *v_scale,
+                           void *o, float *lse, int BH, int N, float scale, int causal,
+                           int *sched, int *dev_status, cudaStream_t stream) {
+  return launch_d<128, false, false, true>(tq, tk, tvt, o, lse, BH, N, scale, causal, sched,
+                                           dev_status, -1, stream, nullptr, 0, q_scale, k_scale,
+                                           v_scale);
 }
 
 }  // namespace fattn

@@ -33,6 +33,23 @@ cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             bool f16 = false, const uint8_t *mask = nullptr,
                             int64_t mask_bh_stride = 0);
 
+// FP8 forward (fwd_bf16.cu, d = 128): tq, tk are E4M3 maps {128, N, B*H}
+// with 128 x 128 x 1 boxes, tvt the E4M3 map {Npad, 128, B*H} of V^T, same
+// boxes; all with the 128-byte swizzle.  q_scale, k_scale: one fp32 per
+// 128-row block of each head; v_scale: one per head.  o is bf16.
+cudaError_t launch_fwd_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tvt,
+                           const float *q_scale, const float *k_scale, const float *v_scale,
+                           void *o, float *lse, int BH, int N, float scale, int causal,
+                           int *sched, int *dev_status, cudaStream_t stream);
+
+// FP8 block quantization (fp8_quant.cu, d = 128); v_amax: the workspace of
+// fp8_quant_workspace_bytes(BH, N) bytes; signs: 128 fp32 +-1 values or null.
+size_t fp8_quant_workspace_bytes(int BH, int N);
+cudaError_t launch_fp8_quantize(const void *q, const void *k, const void *v, const float *signs,
+                                void *q8, void *k8, void *vt8, float *q_scale, float *k_scale,
+                                float *v_scale, float *v_amax, int BH, int N, int n_pad,
+                                float rot_factor, cudaStream_t stream);
+
 // Backward: workspace = fp32 dQ accumulator (row-major [BH][N][d] inside
 // B*H*Npad*d floats, Npad = N rounded up to 128), then [-LSE2 | -D] (2 x 128
 // fp32) per 128-query block: 4 * B*H*Npad*(d + 2) bytes.  tq and tdo (the map

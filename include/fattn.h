@@ -103,6 +103,62 @@ int fa_forward_masked(const void *q, const void *k, const void *v, void *o, floa
                       float scale, fa_stream_t stream);
 
 /*
+ * FP8 forward ("FlashAttention: GPU 메모리 계층을 활용한 어텐션 최적화 분석",
+ * youngju.dev, section 9.2, item 3: FP8 low-precision support with block
+ * quantization and incoherent processing).  Two calls: fa_quantize_fp8 codes
+ * bf16 Q, K, V as E4M3 with per-block scales, fa_forward_fp8 runs the forward
+ * on the codes.  d must be 128 (else FA_ERR_UNSUPPORTED).  E4M3: 1 sign, 4
+ * exponent (bias 7) and 3 mantissa bits, largest finite value 448, byte
+ * 0x7F/0xFF is NaN and is never written.
+ *
+ * fa_quantize_fp8_workspace_bytes -- bytes of device workspace that
+ * fa_quantize_fp8 needs: 4 * B*H*ceil(N/128).  0 for negative sizes.
+ *
+ * fa_fp8_vt_stride -- Npad, the number of keys per row of the transposed V
+ * codes: N rounded up to a multiple of 16.  0 for negative N.
+ *
+ * fa_quantize_fp8 -- in: q, k, v bf16 [B, H, N, 128] (contiguous, 16-byte
+ * aligned); signs: null, or 128 fp32 values each +1 or -1 (device, 16-byte
+ * aligned), the diagonal of the random orthogonal transform
+ * M = diag(signs) H / sqrt(128) (H the Sylvester-Hadamard matrix) applied to
+ * the rows of q and k (not v) before quantization; q M (k M)^T = q k^T.
+ * out (device, caller-allocated):
+ *   q8, k8    E4M3 [B, H, N, 128] (16-byte aligned);
+ *   vt8       E4M3 [B, H, 128, Npad], V transposed (16-byte aligned), codes
+ *             past N are zero;
+ *   q_scale, k_scale  fp32 [B, H, ceil(N/128)]: one dequantization scale per
+ *             block of 128 rows;  v_scale  fp32 [B, H]: one per head.
+ * Per block, s = amax / 448 in fp32 (1 for an all-zero block) and a value x
+ * (a row of q M or k M when signs are given, the fp32 butterfly
+ * (x * signs) H without the 1/sqrt(128)) is coded as E4M3 of x * (1/s),
+ * rounded to nearest even and saturated to +-448; the stored scale is s, or
+ * s * fp32(1/sqrt(128)) with signs, so that code * scale stands for the
+ * value.  workspace: at least fa_quantize_fp8_workspace_bytes bytes of device
+ * memory, used during the call only.  Errors: FA_ERR_INVALID_ARG (null
+ * pointer, negative size, workspace too small), FA_ERR_ALIGNMENT,
+ * FA_ERR_UNSUPPORTED (d != 128, B*H > 65535 or N > 2^30), FA_ERR_CUDA.
+ * Asynchronous on `stream`; B*H = 0 or N = 0 does nothing.
+ *
+ * fa_forward_fp8 -- o = softmax(scale * Qd Kd^T [+ causal mask]) Vd and lse
+ * as in fa_forward, where Qd, Kd, Vd are the dequantized inputs (codes times
+ * scales, with the buffers and layouts fa_quantize_fp8 writes).  Q Kd^T is
+ * formed by E4M3 tensor-core products accumulated in fp32; the softmax
+ * weights are rounded to E4M3 (relative error <= 2^-4, absolute <= 2^-14 of
+ * the row maximum) before the product with V; lse is computed from the
+ * unrounded weights.  o is bf16 [B, H, N, 128], lse fp32 [B, H, N] (may be
+ * null).  Errors and the async contract as for fa_forward.
+ */
+unsigned long long fa_quantize_fp8_workspace_bytes(int B, int H, int N, int d);
+long long fa_fp8_vt_stride(int N);
+int fa_quantize_fp8(const void *q, const void *k, const void *v, const float *signs, void *q8,
+                    void *k8, void *vt8, float *q_scale, float *k_scale, float *v_scale, int B,
+                    int H, int N, int d, void *workspace, unsigned long long workspace_bytes,
+                    fa_stream_t stream);
+int fa_forward_fp8(const void *q8, const void *k8, const void *vt8, const float *q_scale,
+                   const float *k_scale, const float *v_scale, void *o, float *lse, int B, int H,
+                   int N, int d, float scale, int causal, fa_stream_t stream);
+
+/*
  * fa_forward_fp32 -- the same operation and contract as fa_forward with fp32
  * q, k, v and o (every product and sum in fp32 on the CUDA cores, no reduced
  * precision anywhere).  d is 64 or 128.

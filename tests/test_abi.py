@@ -137,6 +137,44 @@ def test_masked_forward_argument_checks(lib, mask, stride, N, expect):
     assert lib.fa_forward_masked(P, P, P, P, NULL, mask, stride, 1, 1, N, 64, 0.125, None) == expect
 
 
+QW = 4 * 2 * 3          # workspace of fa_quantize_fp8 for B=2, H=3, N <= 128
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((NULL, P, P, NULL, P, P, P, P, P, P, 2, 3, 100, 128, P, QW), -1),    # null q
+    ((P, P, P, NULL, P, P, NULL, P, P, P, 2, 3, 100, 128, P, QW), -1),    # null vt8
+    ((P, P, P, NULL, P, P, P, P, P, NULL, 2, 3, 100, 128, P, QW), -1),    # null v_scale
+    ((P, P, P, NULL, P, P, P, P, P, P, 2, 3, 100, 64, P, QW), -2),        # d = 64
+    ((P, P, P, P + 4, P, P, P, P, P, P, 2, 3, 100, 128, P, QW), -3),      # misaligned signs
+    ((P, P, P, NULL, P + 8, P, P, P, P, P, 2, 3, 100, 128, P, QW), -3),   # misaligned q8
+    ((P, P, P, NULL, P, P, P, P, P, P, 2, 3, 100, 128, NULL, QW), -1),    # no workspace
+    ((P, P, P, NULL, P, P, P, P, P, P, 2, 3, 100, 128, P, QW - 1), -1),   # one byte short
+    ((P, P, P, NULL, P, P, P, P, P, P, 300, 300, 100, 128, P, 1 << 40), -2),  # B*H > 65535
+    ((P, P, P, NULL, P, P, P, P, P, P, -1, 3, 100, 128, P, QW), -1),      # negative B
+    ((P, P, P, NULL, P, P, P, P, P, P, 0, 3, 100, 128, NULL, 0), 0),      # empty: no-op
+])
+def test_quantize_fp8_argument_checks(lib, args, expect):
+    assert lib.fa_quantize_fp8(*args, None) == expect
+
+
+def test_quantize_fp8_sizes(lib):
+    assert lib.fa_quantize_fp8_workspace_bytes(2, 3, 100, 128) == 4 * 2 * 3
+    assert lib.fa_quantize_fp8_workspace_bytes(2, 3, 129, 128) == 4 * 2 * 3 * 2
+    assert lib.fa_quantize_fp8_workspace_bytes(-1, 3, 100, 128) == 0
+    assert [lib.fa_fp8_vt_stride(n) for n in (1, 16, 17, 4096, -3)] == [16, 16, 32, 4096, 0]
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((P, P, P, NULL, P, P, P, NULL, 1, 1, 64, 128, 0.1, 0), -1),          # null q_scale
+    ((P, P, P, P, P, P, P, NULL, 1, 1, 64, 64, 0.1, 0), -2),              # d = 64
+    ((P, P, P + 8, P, P, P, P, NULL, 1, 1, 64, 128, 0.1, 0), -3),         # misaligned vt8
+    ((P, P, P, P, P, P, P, NULL, 1, 1, 64, 128, 0.0, 0), -1),             # zero scale
+    ((P, P, P, P, P, P, P, NULL, 1, 1, 0, 128, 0.1, 1), 0),               # N = 0: no-op
+])
+def test_forward_fp8_argument_checks(lib, args, expect):
+    assert lib.fa_forward_fp8(*args, None) == expect
+
+
 def test_valid_call_without_gpu_fails_loudly(lib):
     import torch
     if torch.cuda.is_available():
@@ -147,6 +185,8 @@ def test_valid_call_without_gpu_fails_loudly(lib):
         fa.fa_forward(P, P, P, P, None, 1, 1, 64, 64, 0.125, 0, None)
     rc = lib.fa_backward(P, P, P, P, P, P, P, P, P, 1, 1, 64, 64, 0.125, 0, P, W, None)
     assert rc == -7
+    assert lib.fa_quantize_fp8(P, P, P, NULL, P, P, P, P, P, P, 1, 1, 64, 128, P, 4, None) == -7
+    assert lib.fa_forward_fp8(P, P, P, P, P, P, P, NULL, 1, 1, 64, 128, 0.1, 0, None) == -7
 
 
 def test_missing_library_raises(monkeypatch, tmp_path):

@@ -1,0 +1,148 @@
+"""FP8 forward: block quantization (fa_quantize_fp8) and the E4M3 forward
+(fa_forward_fp8) against the oracle ("FlashAttention: GPU 메모리 계층을 활용한
+어텐션 최적화 분석", youngju.dev, section 9.2, item 3).
+
+Quantization is compared bit for bit: codes and scales are fixed by fp32
+operations and round-to-nearest-even conversions that both sides perform.
+The forward is compared with exact float64 attention on the dequantized
+inputs, inside the per-element bound that the E4M3 softmax weights and the
+bf16 output allow (``oracle.fp8.forward_fp8_reference``), with the typical
+error checked against the bound's statistical scale (rms of error / sigma
+below 1).  LSE comes from fp32 sums of unrounded weights: within 2e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle.fp8 as ofp8
+import exact_attention_11_gb300 as fa
+from exact_attention_11_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+TOL_LSE = 2e-3
+
+
+def _e4m3_bytes(values) -> np.ndarray:
+    t = torch.as_tensor(np.asarray(values, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _quantize(q, k, v, signs=None):
+    s = None if signs is None else signs.to(DEV)
+    x = fa.quantize_fp8(q.to(DEV), k.to(DEV), v.to(DEV), s)
+    torch.cuda.synchronize()
+    return x
+
+
+@pytest.mark.parametrize("B,H,N,rot", [
+    (1, 2, 128, False),
+    (2, 3, 300, False),      # ragged last block, V^T padding
+    (1, 1, 1, False),        # a single row
+    (2, 2, 513, True),       # with the random orthogonal transform
+    (1, 3, 1000, True),
+])
+def test_quantize_codes_and_scales_bit_exact(B, H, N, rot):
+    d = 128
+    q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=N + 7 * B)
+    signs = inputs.rotation_signs(d, seed=N) if rot else None
+    x = _quantize(q, k, v, signs)
+    sg = None if signs is None else signs.numpy()
+    for got, got_s, src in ((x.q8, x.q_scale, q), (x.k8, x.k_scale, k)):
+        codes, scales = ofp8.quantize_rows(src, sg)
+        assert np.array_equal(got.cpu().numpy(), _e4m3_bytes(codes))
+        assert np.array_equal(got_s.cpu().numpy(), scales)
+    vcodes, vscales = ofp8.quantize_heads(v)
+    npad = fa.fa_fp8_vt_stride(N)
+    vt = x.vt8.cpu().numpy()
+    assert vt.shape == (B, H, d, npad)
+    assert np.array_equal(vt[..., :N], _e4m3_bytes(vcodes).transpose(0, 1, 3, 2))
+    assert np.all(vt[..., N:] == 0)
+    assert np.array_equal(x.v_scale.cpu().numpy(), vscales)
+
+
+def test_quantize_zero_block_and_outliers():
+    """A block of zeros (scale 1, zero codes) and inputs with large entries."""
+    B, H, N, d = 1, 2, 384, 128
+    q, k, v = inputs.outlier_inputs(B, H, N, d, torch.bfloat16, seed=3, amp=300.0)
+    q[0, 1, 128:256] = 0
+    v[0, 0] = 0
+    x = _quantize(q, k, v)
+    codes, scales = ofp8.quantize_rows(q)
+    assert np.array_equal(x.q8.cpu().numpy(), _e4m3_bytes(codes))
+    assert x.q_scale[0, 1, 1].item() == 1.0
+    assert x.v_scale[0, 0].item() == 1.0 and int(x.vt8[0, 0].sum()) == 0
+
+
+def _check_forward(q, k, v, causal, signs=None, rows=None):
+    B, H, N, d = q.shape
+    x = _quantize(q, k, v, signs)
+    o, lse = fa.forward_fp8(x, causal=causal)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    sg = None if signs is None else signs.numpy()
+    ro, rl, bound, sigma = ofp8.forward_fp8_reference(q, k, v, d ** -0.5, causal, sg, rows)
+    o = o.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    if rows is not None:
+        o, lse = o[:, :, rows], lse[:, :, rows]
+    err = np.abs(o - ro)
+    assert np.isfinite(o).all()
+    assert np.all(err <= bound), float((err / bound).max())
+    assert np.sqrt(np.mean((err / sigma) ** 2)) <= 1.0
+    assert np.abs(lse - rl).max() <= TOL_LSE
+    return o, ro
+
+
+@pytest.mark.parametrize("B,H,N,causal", [
+    (1, 2, 256, True),
+    (2, 2, 333, False),      # ragged key and query tails
+    (1, 1, 1, True),
+    (1, 2, 1000, True),
+    (1, 4, 640, False),
+])
+def test_fp8_forward_matches_oracle(B, H, N, causal):
+    q, k, v = inputs.forward_inputs(B, H, N, 128, torch.bfloat16, seed=N + B)
+    _check_forward(q, k, v, causal)
+
+
+def test_fp8_forward_with_transform_on_outliers():
+    """With outliers the transform must lower the error against exact
+    attention on the unquantized inputs, on the GPU as in the oracle."""
+    B, H, N, d = 1, 2, 512, 128
+    q, k, v = inputs.outlier_inputs(B, H, N, d, torch.bfloat16, seed=15)
+    signs = inputs.rotation_signs(d, seed=2)
+    o_rot, _ = _check_forward(q, k, v, False, signs)
+    o_plain, _ = _check_forward(q, k, v, False)
+    exact, _ = oracle.attention_forward(q, k, v, d ** -0.5, False)
+    e_rot = np.sqrt(np.mean((o_rot - exact) ** 2))
+    e_plain = np.sqrt(np.mean((o_plain - exact) ** 2))
+    assert e_plain > 1.2 * e_rot, (e_plain, e_rot)
+
+
+def test_fp8_forward_benchmark_shape_sampled_rows():
+    """2 x 16 x 4096 x 128 causal, the benchmark's forward shape; 48 sampled
+    rows per head plus the first and last are checked."""
+    B, H, N, d = 2, 16, 4096, 128
+    q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=3)
+    rows = sorted(set(inputs.sample_rows(N, 48, seed=N).tolist()) | {0, N - 1})
+    _check_forward(q, k, v, True, rows=np.asarray(rows))
+
+
+def test_fp8_distance_from_bf16_is_the_quantization_error():
+    """The FP8 output differs from the bf16 forward of the same inputs by about
+    what quantizing the inputs alone explains: the rms of (FP8 - bf16) on the
+    GPU lies within [0.8, 1.5] x the rms of (FP8 reference - exact) in the
+    oracle (the GPU side adds E4M3 weights and bf16 roundings)."""
+    B, H, N, d = 1, 2, 512, 128
+    q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=77)
+    x = _quantize(q, k, v)
+    o8, _ = fa.forward_fp8(x, causal=True)
+    o16, _ = fa.forward(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
+    torch.cuda.synchronize()
+    r_gpu = (o8.float() - o16.float()).pow(2).mean().sqrt().item()
+    exact, _ = oracle.attention_forward(q, k, v, d ** -0.5, True)
+    ref8, _, _, _ = ofp8.forward_fp8_reference(q, k, v, d ** -0.5, True)
+    r_ref = float(np.sqrt(np.mean((ref8 - exact) ** 2)))
+    assert 0.8 * r_ref < r_gpu < 1.5 * r_ref, (r_gpu, r_ref)
