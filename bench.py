@@ -608,7 +608,7 @@ def gpu_arm(args):
                          "achieved": round(weak_scaling_rate(flops, 1, fp8_ms, 1e12), 2),
                          "peak": round(2 * peak_t, 1), "unit": "TFLOP/s",
                          "frac": round(weak_scaling_rate(flops, 1, fp8_ms, 1e12) / (2 * peak_t), 4),
-                         "traffic": None,
+                         "traffic": recorded_traffic("fwd_bf16_tc_kernel<128,0,0,1>"),
                          "peak_kind": f"{peak_kind} bf16 burst x 2 (nominal fp8/bf16 ratio)",
                          "kernel": "fwd_bf16_tc_kernel<128,0,0,1> (E4M3)"},
         },

@@ -82,45 +82,6 @@ struct SoftmaxCfg {
   static constexpr float kPOffset = FP8 ? 4.0f : 0.0f;           // log2 of the weight scale
 };
 
-// FP8: the E4M3 products run twice as fast as bf16 ones, which leaves the
-// multi-function unit (16 exponentials per clock per SM) as the limit of the
-// softmax.  One pair of weights in every kFp8EmuPeriod groups of four is
-// therefore evaluated on the FMA and integer pipes instead (exp2_fma_x2);
-// 0 disables this.
-#ifndef FATTN_FP8_EMU_PERIOD
-#define FATTN_FP8_EMU_PERIOD 2
-#endif
-constexpr int kFp8EmuPeriod = FATTN_FP8_EMU_PERIOD;
-
-// 2^x for a pair of fp32 values without the multi-function unit.  x = n + f
-// with n = round(x), found by adding 1.5 * 2^23 (the sum's low mantissa bits
-// then hold n in two's complement), and f in [-1/2, 1/2]; 2^f comes from a
-// cubic whose coefficients minimise the largest relative error on that
-// interval (a Remez fit, fit_exp2_poly.py beside this file: 7.5e-5 with fp32
-// Horner evaluation), and 2^n is applied by adding n to the exponent field.
-// Inputs are clamped at -126 first (2^f has exponent field 126 or 127, so the
-// sum cannot leave the field's range for x <= 127); -inf gives a value below
-// 2^-126.
-__device__ __forceinline__ uint64_t exp2_fma_x2(uint64_t x2) {
-  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-  constexpr float c0 = 0x1.fff692p-1f, c1 = 0x1.62f31ap-1f, c2 = 0x1.f0de1ap-3f,
-                  c3 = 0x1.c3f76p-5f;
-  float2 x = f2_split(x2);
-  x.x = fmaxf(x.x, -126.f);
-  x.y = fmaxf(x.y, -126.f);
-  const uint64_t xv = f2(x.x, x.y);
-  const uint64_t j = fadd2(xv, f2(kRound, kRound));
-  const uint64_t n = fadd2(j, f2(-kRound, -kRound));
-  const uint64_t f = ffma2(n, f2(-1.f, -1.f), xv);
-  uint64_t p = ffma2(f2(c3, c3), f, f2(c2, c2));
-  p = ffma2(p, f, f2(c1, c1));
-  p = ffma2(p, f, f2(c0, c0));
-  const float2 jj = f2_split(j), pp = f2_split(p);
-  const uint32_t r0 = __float_as_uint(jj.x) * (1u << 23) + __float_as_uint(pp.x);
-  const uint32_t r1 = __float_as_uint(jj.y) * (1u << 23) + __float_as_uint(pp.y);
-  return f2(__uint_as_float(r0), __uint_as_float(r1));
-}
-
 template <int D, bool FP8 = false>
 struct Cfg {
   static constexpr int kElemBytes = FP8 ? 1 : 2;
@@ -630,10 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   f2(__uint_as_float(sv[c][e + 2]), __uint_as_float(sv[c][e + 3])), c2t, nm2);
               const float2 x = f2_split(xa), y = f2_split(xb);
               const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-              const bool emu =
-                  kFp8EmuPeriod > 0 && (c * 8 + (e >> 2)) % kFp8EmuPeriod == kFp8EmuPeriod - 1;
-              const float2 r = emu ? f2_split(exp2_fma_x2(xb))
-                                   : make_float2(ex2_approx(y.x), ex2_approx(y.y));
+              const float2 r = make_float2(ex2_approx(y.x), ex2_approx(y.y));
               sum2[0] = fadd2(sum2[0], f2(p.x, p.y));
               sum2[1] = fadd2(sum2[1], f2(r.x, r.y));
               // Four codes per column; columns 8(c & 1) .. 8(c & 1) + 7 of
