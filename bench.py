@@ -16,6 +16,7 @@ Printed JSON line (rank 0):
   roofline       the forward (dominant kernel) against the measured bf16 peak
   fwd_f16        fa_forward_f16 on the forward workload in fp16 (same FLOPs)
   fwd_masked     fa_forward_masked with the tril mask on the forward workload
+  fwd_d256       fa_forward on 2 x 8 x 4096 x 256 causal (head dimension 256)
   fwd_fp8        fa_forward_fp8 on the forward workload quantized to E4M3 by
                  fa_quantize_fp8 (timed separately), against 2x the bf16 peak
   backward       fa_backward (dQ, dK, dV) of the forward workload, TFLOP/s with
@@ -47,6 +48,8 @@ FWD = dict(B=2, H=16, N=4096, d=128, causal=True, seed=3)
 # The long-sequence forward, timed separately and reported nested.
 FWD_LONG = dict(B=1, H=8, N=16384, d=128, causal=True, seed=4, amp=0.5)
 DEC = dict(num_seqs=64, num_heads=32, head_size=128, block_size=16, max_ctx=4096, seed=5)
+# Head dimension 256, timed separately and reported nested.
+FWD_D256 = dict(B=2, H=8, N=4096, d=256, causal=True, seed=6)
 # Grouped key/value heads: the same sequences and contexts, 8 cached heads.
 DEC_GQA = dict(DEC, num_kv_heads=8)
 L2_FLUSH_BYTES = 512 << 20
@@ -336,6 +339,33 @@ def gpu_arm(args):
     masked_ms = sum(e[0].elapsed_time(e[1]) for e in mev) / km
     del tril
 
+    # Head dimension 256 (2 x 8 x 4096 x 256 causal), timed the same way, as
+    # "fwd_d256".
+    DB, DH, DN, Dd = FWD_D256["B"], FWD_D256["H"], FWD_D256["N"], FWD_D256["d"]
+    dq_, dk_, dv_ = (t.to(dev) for t in inputs.forward_inputs(
+        DB, DH, DN, Dd, torch.bfloat16, seed=FWD_D256["seed"] + 1000 * rank))
+    do_ = torch.empty_like(dq_)
+    dlse = torch.empty((DB, DH, DN), dtype=torch.float32, device=dev)
+
+    def run_d256():
+        fa.fa_forward(dq_.data_ptr(), dk_.data_ptr(), dv_.data_ptr(), do_.data_ptr(),
+                      dlse.data_ptr(), DB, DH, DN, Dd, Dd ** -0.5, FWD_D256["causal"], sptr)
+
+    kd = max(3, min(K // 4, 100))
+    dev_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(kd)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush.zero_()
+            run_d256()
+        for i in range(kd):
+            flush.zero_()
+            dev_ev[i][0].record(stream)
+            run_d256()
+            dev_ev[i][1].record(stream)
+    stream.synchronize()
+    d256_ms = sum(e[0].elapsed_time(e[1]) for e in dev_ev) / kd
+    del dq_, dk_, dv_, do_, dlse
+
     # The FP8 forward on the same workload: the inputs are block-quantized to
     # E4M3 once (fa_quantize_fp8), then fa_forward_fp8 is timed the same way,
     # and the quantization on its own; reported as "fwd_fp8".
@@ -564,9 +594,10 @@ def gpu_arm(args):
             "fwd": {k_: v_ for k_, v_ in FWD.items() if k_ != "seed"},
             "decode": {k_: v_ for k_, v_ in DEC.items() if k_ != "seed"},
             "decode_sum_ctx": int(ctx.sum()),
-            "l2": "forward, 16K forward and backward: flushed (512 MiB write) before every "
-                  "timed launch; decode (2.2 GB read per launch) and grouped decode "
-                  "(0.55 GB): inputs larger than L2, not flushed",
+            "l2": "forward, 16K, fp16, masked, d256 and FP8 forwards, FP8 quantization and "
+                  "backward: flushed (512 MiB write) before every timed launch; decode "
+                  "(2.2 GB read per launch) and grouped decode (0.55 GB): inputs larger than "
+                  "L2, not flushed",
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
             "sms": torch.cuda.get_device_properties(dev).multi_processor_count,
         },
@@ -594,6 +625,14 @@ def gpu_arm(args):
             "value": round(weak_scaling_rate(flops, ws, masked_ms, 1e12), 2),
             "unit": "TFLOP/s",
             "frac_of_bf16_peak": round(flops / (masked_ms * 1e-3) / 1e12 / peak_t, 4),
+        },
+        "fwd_d256": {
+            "workload": "fa_forward bf16 B=2 H=8 N=4096 d=256 causal",
+            "ms": round(d256_ms, 4),
+            "value": round(weak_scaling_rate(fwd_flops(**FWD_D256), ws, d256_ms, 1e12), 2),
+            "unit": "TFLOP/s",
+            "frac_of_bf16_peak": round(fwd_flops(**FWD_D256) / (d256_ms * 1e-3) / 1e12 / peak_t,
+                                       4),
         },
         "fwd_fp8": {
             "workload": "fa_forward_fp8 on the forward workload block-quantized to E4M3 "
@@ -662,7 +701,7 @@ def gpu_arm(args):
                         "(step i+1's inputs arrive while step i computes)"},
         # library kernels inside timed regions (a backward is three launches)
         # fwd_fp8: kq forwards + kq quantizations of two launches each
-        "gpu_launches": 2 * K + kl + kf + km + 3 * kq + 3 * kb + kg + 2 * ke,
+        "gpu_launches": 2 * K + kl + kf + km + kd + 3 * kq + 3 * kb + kg + 2 * ke,
         "clocks": clk,
         "device_status": status,
         "wall_s": round(wall, 3),

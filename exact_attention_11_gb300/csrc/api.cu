@@ -130,11 +130,12 @@ int encode_dq_acc_map(CUtensorMap *m, void *base, int BH, int N, int d) {
 }
 
 int check_forward_args(const void *q, const void *k, const void *v, const void *o,
-                       const void *lse, int B, int H, int N, int d, float scale) {
+                       const void *lse, int B, int H, int N, int d, float scale,
+                       bool allow_d256 = false) {
   if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
   if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && !(allow_d256 && d == 256)) return FA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_ALIGNMENT;
   // Grid and tensor-map limits: B*H and the tile count index 32-bit grids.
@@ -219,7 +220,7 @@ namespace {
 int forward16(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
               int N, int d, float scale, int causal, fa_stream_t stream, bool f16,
               const uint8_t *mask = nullptr, long long mask_bh_stride = 0) {
-  int rc = check_forward_args(q, k, v, o, lse, B, H, N, d, scale);
+  int rc = check_forward_args(q, k, v, o, lse, B, H, N, d, scale, mask == nullptr);
   if (rc != FA_OK) return rc;
   const int BH = B * H;
   if (BH == 0 || N == 0) return FA_OK;
@@ -239,6 +240,13 @@ int forward16(const void *q, const void *k, const void *v, void *o, float *lse, 
       f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if ((rc = encode_qkv_map(&tq, q, BH, N, d, 128, dt)) != FA_OK) return rc;
   if ((rc = encode_qkv_map(&tk, k, BH, N, d, 128, dt)) != FA_OK) return rc;
+  if (d == 256) {
+    // One 128-row query tile per CTA; V arrives in 64-key halves.
+    if ((rc = encode_qkv_map(&tv, v, BH, N, d, 64, dt)) != FA_OK) return rc;
+    return cuda_status(fattn::launch_fwd_d256(tq, tk, tv, o, lse, BH, N, scale, causal ? 1 : 0,
+                                              sched, g_dev[dev].status,
+                                              reinterpret_cast<cudaStream_t>(stream), f16));
+  }
   if ((rc = encode_qkv_map(&tv, v, BH, N, d, 128, dt)) != FA_OK) return rc;
   return cuda_status(launch_fwd_bf16(tq, tk, tv, o, lse, BH, N, d, scale, causal ? 1 : 0, sched,
                                      g_dev[dev].status, fault_cta,

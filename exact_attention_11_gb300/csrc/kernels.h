@@ -33,6 +33,12 @@ cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             bool f16 = false, const uint8_t *mask = nullptr,
                             int64_t mask_bh_stride = 0);
 
+// Head dimension 256 (fwd_d256.cu), bf16 or (f16) fp16: tq and tk as for
+// launch_fwd_bf16 (64 x 128 x 1 boxes), tv with 64 x 64 x 1 boxes.
+cudaError_t launch_fwd_d256(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            void *o, float *lse, int BH, int N, float scale, int causal,
+                            int *sched, int *dev_status, cudaStream_t stream, bool f16);
+
 // FP8 forward (fwd_bf16.cu, d = 128): tq, tk are E4M3 maps {128, N, B*H}
 // with 128 x 128 x 1 boxes, tvt the E4M3 map {Npad, 128, B*H} of V^T, same
 // boxes; all with the 128-byte swizzle.  q_scale, k_scale: one fp32 per

@@ -63,7 +63,8 @@ typedef enum {
  *   o        bf16 [B, H, N, d], written (rounded to nearest even).
  *   lse      fp32 [B, H, N] natural-log log-sum-exp of the scaled scores,
  *            written; may be NULL when the caller does not need it.
- *   d        head dimension: 64 or 128 (else FA_ERR_UNSUPPORTED).
+ *   d        head dimension: 64, 128 or 256 (else FA_ERR_UNSUPPORTED; section
+ *            11.4 of the same page serves head dimensions up to 256).
  *   scale    multiplier applied to every score before the softmax (usually
  *            1/sqrt(d)); must be finite and > 0.
  *   causal   0 or non-zero.
@@ -96,7 +97,8 @@ int fa_forward_f16(const void *q, const void *k, const void *v, void *o, float *
  * multiple of 16 (else FA_ERR_UNSUPPORTED) and mask_bh_stride a multiple of
  * 16 (else FA_ERR_ALIGNMENT).  A row with no visible key gets o = 0 and
  * lse = -inf.  Every key tile is computed (no tile is skipped for being fully
- * masked).  Other arguments, layouts and errors as for fa_forward (bf16).
+ * masked).  d is 64 or 128.  Other arguments, layouts and errors as for
+ * fa_forward (bf16).
  */
 int fa_forward_masked(const void *q, const void *k, const void *v, void *o, float *lse,
                       const void *mask, long long mask_bh_stride, int B, int H, int N, int d,

@@ -51,7 +51,8 @@ P = 4096  # a 16-byte-aligned fake address: never dereferenced on these paths
 @pytest.mark.parametrize("args,expect", [
     ((NULL, P, P, P, NULL, 1, 1, 64, 64, 0.125, 0), -1),      # null q
     ((P, P, P, P, NULL, -1, 1, 64, 64, 0.125, 0), -1),        # negative B
-    ((P, P, P, P, NULL, 1, 1, 64, 96, 0.125, 0), -2),         # d not 64/128
+    ((P, P, P, P, NULL, 1, 1, 64, 96, 0.125, 0), -2),         # d not 64/128/256
+    ((P, P, P, P, NULL, 1, 1, 64, 512, 0.125, 0), -2),        # d = 512
     ((P, P, P, P, NULL, 1, 1, 64, 64, 0.0, 0), -1),           # scale 0
     ((P, P, P, P, NULL, 1, 1, 64, 64, float("nan"), 0), -1),  # scale NaN
     ((P + 2, P, P, P, NULL, 1, 1, 64, 64, 0.125, 0), -3),     # misaligned q
@@ -135,6 +136,15 @@ def test_backward_workspace_size(lib):
 ])
 def test_masked_forward_argument_checks(lib, mask, stride, N, expect):
     assert lib.fa_forward_masked(P, P, P, P, NULL, mask, stride, 1, 1, N, 64, 0.125, None) == expect
+
+
+def test_head_dim_256_is_forward_only(lib):
+    """d = 256 is served by fa_forward and fa_forward_f16 only."""
+    assert lib.fa_forward_masked(P, P, P, P, NULL, P, 0, 1, 1, 64, 256, 0.1, None) == -2
+    assert lib.fa_forward_fp32(P, P, P, P, NULL, 1, 1, 64, 256, 0.1, 0, None) == -2
+    assert lib.fa_backward(P, P, P, P, P, P, P, P, P, 1, 1, 64, 256, 0.1, 0, P, 1 << 30,
+                           None) == -2
+    assert lib.fa_forward(P, P, P, P, NULL, 0, 1, 64, 256, 0.1, 1, None) == 0   # empty: no-op
 
 
 QW = 4 * 2 * 3          # workspace of fa_quantize_fp8 for B=2, H=3, N <= 128
