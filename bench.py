@@ -620,7 +620,8 @@ def gpu_arm(args):
         },
         "fwd_masked": {
             "workload": "fa_forward_masked bf16 B=2 H=16 N=4096 d=128 with the [N,N] tril mask "
-                        "(every key tile computed; FLOPs counted for the visible half)",
+                        "(key tiles no row of a work item sees are skipped; FLOPs counted for the "
+                        "visible half; the mask's tile summary is inside the timed call)",
             "ms": round(masked_ms, 4),
             "value": round(weak_scaling_rate(flops, ws, masked_ms, 1e12), 2),
             "unit": "TFLOP/s",

@@ -27,6 +27,8 @@ struct DeviceState {
   size_t decode_counter_count = 0;
   int *fwd_sched = nullptr;       // kFwdSchedSlots pairs of forward work counters, kept at zero
   unsigned fwd_sched_next = 0;    // slot for the next forward launch
+  void *mask_ws = nullptr;        // tile summary of the last mask (fa_forward_masked)
+  size_t mask_ws_bytes = 0;
   int inject_fault = 0;           // fa_debug_inject_fault: armed for the next forward
   int checked = 0;                // 1: sm_103 verified, -1: unsupported
 };
@@ -226,6 +228,9 @@ int forward16(const void *q, const void *k, const void *v, void *o, float *lse, 
   if (BH == 0 || N == 0) return FA_OK;
   int dev = 0, fault_cta = -1;
   int *sched = nullptr;
+  void *mask_ws = nullptr;
+  const int mask_heads = mask_bh_stride != 0 ? BH : 1;
+  if (mask != nullptr && (mask_heads > 65535 || (N + 127) / 128 > 65535)) return FA_ERR_UNSUPPORTED;
   CUtensorMap tq, tk, tv;
   {
     std::lock_guard<std::mutex> lock(g_mu);
@@ -235,6 +240,17 @@ int forward16(const void *q, const void *k, const void *v, void *o, float *lse, 
     sched = st.fwd_sched + 2 * (st.fwd_sched_next++ % fattn::kFwdSchedSlots);
     fault_cta = st.inject_fault ? 0 : -1;
     st.inject_fault = 0;
+    if (mask != nullptr) {
+      const size_t need = fattn::mask_summary_bytes(mask_heads, N);
+      if (st.mask_ws_bytes < need) {
+        if (st.mask_ws) cudaFree(st.mask_ws);  // synchronises: no launch still uses it
+        st.mask_ws = nullptr;
+        st.mask_ws_bytes = 0;
+        if (cudaMalloc(&st.mask_ws, need) != cudaSuccess) return FA_ERR_NO_MEMORY;
+        st.mask_ws_bytes = need;
+      }
+      mask_ws = st.mask_ws;
+    }
   }
   const CUtensorMapDataType dt =
       f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -248,10 +264,17 @@ int forward16(const void *q, const void *k, const void *v, void *o, float *lse, 
                                               reinterpret_cast<cudaStream_t>(stream), f16));
   }
   if ((rc = encode_qkv_map(&tv, v, BH, N, d, 128, dt)) != FA_OK) return rc;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *flags = nullptr;
+  const int2 *ranges = nullptr;
+  if (mask != nullptr &&
+      (rc = cuda_status(fattn::launch_mask_summary(mask, static_cast<int64_t>(mask_bh_stride), N,
+                                                   mask_heads, mask_ws, &flags, &ranges, s))) !=
+          FA_OK)
+    return rc;
   return cuda_status(launch_fwd_bf16(tq, tk, tv, o, lse, BH, N, d, scale, causal ? 1 : 0, sched,
-                                     g_dev[dev].status, fault_cta,
-                                     reinterpret_cast<cudaStream_t>(stream), f16, mask,
-                                     static_cast<int64_t>(mask_bh_stride)));
+                                     g_dev[dev].status, fault_cta, s, f16, mask,
+                                     static_cast<int64_t>(mask_bh_stride), ranges, flags));
 }
 }  // namespace
 
@@ -469,6 +492,7 @@ void fa_release(void) {
   if (st.decode_counters) cudaFree(st.decode_counters);
   if (st.status) cudaFree(st.status);
   if (st.fwd_sched) cudaFree(st.fwd_sched);
+  if (st.mask_ws) cudaFree(st.mask_ws);
   st = DeviceState{};
 }
 

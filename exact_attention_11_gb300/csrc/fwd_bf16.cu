@@ -153,12 +153,26 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t ph) {
 }
 
 // Work item w -> query block, head and the key tiles each query tile needs.
+// With a mask, `ranges` holds per (mask head, item) the first key tile kv0
+// that any of the item's rows can see and the tile counts n_a <= n_b of its
+// query tiles (mask_tiles.cu); key tile j of the item is tile kv0 + j of the
+// sequence.
 struct ItemDecoder {
   int BH, n_qblocks, n_kv_total, causal;
-  __device__ void decode(int w, int &q0, int &bh, int &n_a, int &n_b) const {
+  const int2 *ranges;
+  int mask_shared;
+  __device__ void decode(int w, int &q0, int &bh, int &n_a, int &n_b, int &kv0) const {
     const int qb = n_qblocks - 1 - w / BH;
     bh = w % BH;
     q0 = qb * 2 * BM;
+    kv0 = 0;
+    if (ranges != nullptr) {
+      const int2 r = ranges[static_cast<int64_t>(mask_shared ? 0 : bh) * n_qblocks + qb];
+      kv0 = r.x & 0xffff;
+      n_a = r.x >> 16;
+      n_b = r.y;
+      return;
+    }
     n_a = causal ? min(2 * qb + 1, n_kv_total) : n_kv_total;
     n_b = causal ? min(2 * qb + 2, n_kv_total) : n_kv_total;
   }
@@ -167,6 +181,10 @@ struct ItemDecoder {
 // MASK: a boolean mask decides visibility -- key j is visible to query row i
 // of head bh iff mask[bh * mask_bh_stride + i * N + j] != 0 (N a multiple of 16;
 // causal is then 0).  A row that sees no key gets O = 0 and LSE = -inf.
+// mask_ranges / mask_flags: the per-tile summary of mask_tiles.cu: per item
+// the key tiles its rows can see (the others are skipped), per 128 x 128
+// block a flag (0: nothing visible, 1: partly, 2: everything; a fully
+// visible tile reads no mask bytes).
 // FP8: E4M3 inputs (tm_v then maps V^T, [BH][d][Npad]); q_scale and k_scale
 // hold one dequantization scale per 128-row block of each head (n_sblk per
 // head), v_scale one per head.  The output is bf16.
@@ -180,7 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        int fault_cta, const uint8_t *__restrict__ mask,
                        int64_t mask_bh_stride, const float *__restrict__ q_scale,
                        const float *__restrict__ k_scale, const float *__restrict__ v_scale,
-                       int n_sblk) {
+                       int n_sblk, const int2 *__restrict__ mask_ranges,
+                       const uint8_t *__restrict__ mask_flags) {
   using C = Cfg<D, FP8>;
   using SC = SoftmaxCfg<FP8>;
   static_assert(!FP8 || (D == 128 && !F16 && !MASK), "the FP8 variant is d = 128, unmasked");
@@ -199,6 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   sch.n_qblocks = n_qblocks;
   sch.n_kv_total = (N + BN - 1) / BN;
   sch.causal = causal;
+  sch.ranges = MASK ? mask_ranges : nullptr;
+  sch.mask_shared = mask_bh_stride == 0;
   const int n_items = n_qblocks * BH;
   // Consumer side of the item ring: every lane of the calling warp waits for
   // ring entry k, reads it, and one arrival per warp (or the lone MMA thread)
@@ -266,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         misc->item[slot] = w;
         mbar_arrive(bar(kBarItemFull + slot));
         if (w >= n_items) break;
-        int q0, bh, n_a, n_b;
-        sch.decode(w, q0, bh, n_a, n_b);
+        int q0, bh, n_a, n_b, kv0;
+        sch.decode(w, q0, bh, n_a, n_b, kv0);
         // Query tile t of this item, once the previous item's last QK_t has
         // read the buffer.  Tile A goes first: the MMA warp starts it during
         // the previous item's last step.  Tile B follows the first key tile.
@@ -297,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(kBarKFull + st), C::kTileBytes);
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(s_base + C::kK0 + st * C::kTileBytes + b * C::kBoxBytes, &tm_k, b * 64,
-                        j * BN, bh, bar(kBarKFull + st));
+                        (kv0 + j) * BN, bh, bar(kBarKFull + st));
           nk = kv + 1;
           if (j == 0) {
             if (!(ok = load_q(1))) break;
@@ -306,12 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(bar(kBarVEmpty + st), ph ^ 1, abort_flag))) break;
           mbar_arrive_expect_tx(bar(kBarVFull + st), C::kTileBytes);
           if (FP8)   // V^T: rows are the d coordinates, keys run along x
-            tma_load_3d(s_base + C::kV0 + st * C::kTileBytes, &tm_v, j * BN, 0, bh,
+            tma_load_3d(s_base + C::kV0 + st * C::kTileBytes, &tm_v, (kv0 + j) * BN, 0, bh,
                         bar(kBarVFull + st));
           else
             for (int b = 0; b < C::kBoxes; ++b)
               tma_load_3d(s_base + C::kV0 + st * C::kTileBytes + b * C::kBoxBytes, &tm_v, b * 64,
-                          j * BN, bh, bar(kBarVFull + st));
+                          (kv0 + j) * BN, bh, bar(kBarVFull + st));
           nv = kv + 1;
         }
         ++it;
@@ -392,8 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool a0_issued = false;
       ok = fetch_item(0, w, false);
       for (int k = 0; ok && w < n_items; ++k) {
-        int q0, bh, n_a, n_b;
-        sch.decode(w, q0, bh, n_a, n_b);
+        int q0, bh, n_a, n_b, kv0;
+        sch.decode(w, q0, bh, n_a, n_b, kv0);
         if (!a0_issued) {
           if (!(ok = mbar_wait(bar(kBarQFullA), it & 1, abort_flag) && wait_k(kv))) break;
           tc_fence_after();
@@ -436,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = fetch_item(k + 1, w_next, false))) break;
             fetched = true;
             if (w_next < n_items) {
-              int nq0, nbh, nn_a, nn_b;
-              sch.decode(w_next, nq0, nbh, nn_a, nn_b);
+              int nq0, nbh, nn_a, nn_b, nkv0;
+              sch.decode(w_next, nq0, nbh, nn_a, nn_b, nkv0);
               if (!(ok = mbar_wait(bar(kBarQFullA), (it + 1) & 1, abort_flag) &&
                          wait_k(kv + n_b)))
                 break;
@@ -489,10 +510,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; ok; ++k) {
       int w;
       if (!(ok = fetch_item(k, w, true)) || w >= n_items) break;
-      int q0, bh, n_a, n_b;
-      sch.decode(w, q0, bh, n_a, n_b);
+      int q0, bh, n_a, n_b, kv0;
+      sch.decode(w, q0, bh, n_a, n_b, kv0);
       const int row = q0 + t * BM + r_local;
       const int n_mine = t ? n_b : n_a;
+      // MASK: this query tile's row of the tile summary (a tile past the
+      // sequence end has no rows to keep: treat it as seeing nothing).
+      const int n_t = (N + BM - 1) / BM;
+      const int qt = q0 / BM + t;
+      const uint8_t *flag_row =
+          MASK ? mask_flags + (static_cast<int64_t>(mask_bh_stride ? bh : 0) * n_t + qt) * n_t
+               : nullptr;
       // FP8: the scores are raw code products; this tile's Q block scale (a
       // tile past the last block has no rows to keep) times each key tile's
       // scale turns them into scale * q.k.
@@ -508,14 +536,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // MASK: this row's 128 mask bytes for key tile j, fetched before the
         // wait for the scores (chunks past N read as "not visible").
         uint4 mk[8];
+        int flag = 1;
         if (MASK) {
-          const int kb0 = j * BN;
-          const uint8_t *mr = mask + static_cast<int64_t>(bh) * mask_bh_stride +
-                              static_cast<int64_t>(min(row, N - 1)) * N + kb0;
+          flag = qt < n_t ? flag_row[kv0 + j] : 0;
+          if (flag == 1) {
+            const int kb0 = (kv0 + j) * BN;
+            const uint8_t *mr = mask + static_cast<int64_t>(bh) * mask_bh_stride +
+                                static_cast<int64_t>(min(row, N - 1)) * N + kb0;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            mk[c] = (kb0 + 16 * c < N) ? *reinterpret_cast<const uint4 *>(mr + 16 * c)
-                                       : make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < 8; ++c)
+              mk[c] = (kb0 + 16 * c < N) ? *reinterpret_cast<const uint4 *>(mr + 16 * c)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) mk[c] = make_uint4(0u, 0u, 0u, 0u);   // nothing visible
+          }
         }
         if (!(ok = mbar_wait(bar(kBarSFull + t), sc & 1, abort_flag))) break;
         tc_fence_after();
@@ -526,10 +561,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) tmem_wait_ld(sv[c]);
 #define S_(c) sv[(c) >> 5][(c) & 31]
         if (MASK) {
+          if (flag != 2) {   // a fully visible tile needs no mask
 #pragma unroll
-          for (int c = 0; c < BN; ++c) {
-            const uint32_t w = (&mk[c >> 4].x)[(c >> 2) & 3];
-            if (((w >> (8 * (c & 3))) & 0xffu) == 0u) S_(c) = __float_as_uint(-INFINITY);
+            for (int c = 0; c < BN; ++c) {
+              const uint32_t w = (&mk[c >> 4].x)[(c >> 2) & 3];
+              if (((w >> (8 * (c & 3))) & 0xffu) == 0u) S_(c) = __float_as_uint(-INFINITY);
+            }
           }
         } else if (j == n_mine - 1) {
           // Keys past the sequence end, and (causal) keys after the query row.
@@ -698,7 +735,8 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
                      float *lse, int BH, int N, float scale, int causal, int *sched,
                      int *dev_status, int fault_cta, cudaStream_t stream, const uint8_t *mask,
                      int64_t mask_bh_stride, const float *q_scale = nullptr,
-                     const float *k_scale = nullptr, const float *v_scale = nullptr) {
+                     const float *k_scale = nullptr, const float *v_scale = nullptr,
+                     const int2 *mask_ranges = nullptr, const uint8_t *mask_flags = nullptr) {
   using C = Cfg<D, FP8>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -720,7 +758,8 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
   const int n_sblk = (N + BM - 1) / BM;
   fwd_bf16_tc_kernel<D, F16, MASK, FP8><<<grid, kThreads, C::kAlloc, stream>>>(
       tq, tk, tv, reinterpret_cast<uint16_t *>(o), lse, N, BH, n_qblocks, scale_log2, causal,
-      sched, dev_status, fault_cta, mask, mask_bh_stride, q_scale, k_scale, v_scale, n_sblk);
+      sched, dev_status, fault_cta, mask, mask_bh_stride, q_scale, k_scale, v_scale, n_sblk,
+      mask_ranges, mask_flags);
   return cudaGetLastError();
 }
 
@@ -729,10 +768,11 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
 cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             void *o, float *lse, int BH, int N, int d, float scale, int causal,
                             int *sched, int *dev_status, int fault_cta, cudaStream_t stream,
-                            bool f16, const uint8_t *mask, int64_t mask_bh_stride) {
+                            bool f16, const uint8_t *mask, int64_t mask_bh_stride,
+                            const int2 *mask_ranges, const uint8_t *mask_flags) {
 #define FATTN_FWD_ARGS \
   tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status, fault_cta, stream, mask, \
-      mask_bh_stride
+      mask_bh_stride, nullptr, nullptr, nullptr, mask_ranges, mask_flags
   if (mask != nullptr) {
     if (f16) return cudaErrorInvalidValue;   // masks are served for bf16 only
     return d == 64 ? launch_d<64, false, true>(FATTN_FWD_ARGS)

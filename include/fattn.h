@@ -96,8 +96,11 @@ int fa_forward_f16(const void *q, const void *k, const void *v, void *o, float *
  * gives every head its own.  mask is uint8, 16-byte aligned, N must be a
  * multiple of 16 (else FA_ERR_UNSUPPORTED) and mask_bh_stride a multiple of
  * 16 (else FA_ERR_ALIGNMENT).  A row with no visible key gets o = 0 and
- * lse = -inf.  Every key tile is computed (no tile is skipped for being fully
- * masked).  d is 64 or 128.  Other arguments, layouts and errors as for
+ * lse = -inf.  Each call first summarises the mask per 128 x 128 block (one
+ * read of the mask): key tiles that none of a query block's rows can see are
+ * skipped, and fully visible blocks are not read again.  The summary lives
+ * in a library-owned buffer grown on demand (calls that overlap on the GPU
+ * must not share a device).  d is 64 or 128.  Other arguments, layouts and errors as for
  * fa_forward (bf16).
  */
 int fa_forward_masked(const void *q, const void *k, const void *v, void *o, float *lse,

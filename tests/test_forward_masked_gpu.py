@@ -76,3 +76,42 @@ def test_sliding_window_mask_sampled_rows():
     rows = sorted(set(inputs.sample_rows(N, 48, seed=2).tolist()) | {0, 299, 300, N - 1})
     o, lse, ro, rl = _run(B, H, N, d, mask, seed=2, rows=rows)
     _close(o, lse, ro, rl)
+
+
+def test_block_sparse_mask_skips_tiles():
+    """A mask made of whole 128 x 128 blocks (on or off, per head) plus a
+    ragged N: key tiles that no row of an item sees are skipped, fully visible
+    tiles read no mask bytes, partial ones (the ragged edge) are masked."""
+    B, H, N, d = 1, 3, 720, 128
+    r = np.random.default_rng(11)
+    nt = (N + 127) // 128
+    blocks = r.random((B, H, nt, nt)) < 0.4
+    mask = np.repeat(np.repeat(blocks, 128, axis=2), 128, axis=3)[:, :, :N, :N].astype(np.uint8)
+    mask[0, 2, 300:310] = 0                     # a few rows with nothing visible
+    o, lse, ro, rl = _run(B, H, N, d, mask, seed=12)
+    _close(o, lse, ro, rl)
+
+
+def test_mask_hiding_whole_items():
+    """Rows 0-511 see no key at all (two whole work items of 256 rows): they
+    must still be written as O = 0, LSE = -inf; the other rows see a band."""
+    N, d = 1024, 64
+    i = np.arange(N)
+    mask = ((i[None, :] <= i[:, None]) & (i[None, :] > i[:, None] - 200)).astype(np.uint8)
+    mask[:512] = 0
+    o, lse, ro, rl = _run(2, 2, N, d, mask, seed=13)
+    _close(o, lse, ro, rl)
+    assert np.all(o[:, :, :512] == 0) and np.all(np.isneginf(lse[:, :, :512]))
+
+
+def test_dense_mask_equals_unmasked_forward():
+    """An all-ones mask (every tile fully visible: no mask bytes are read) gives
+    the unmasked non-causal forward."""
+    B, H, N, d = 1, 2, 384, 128
+    mask = np.ones((N, N), dtype=np.uint8)
+    o, lse, ro, rl = _run(B, H, N, d, mask, seed=14)
+    _close(o, lse, ro, rl)
+    q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=14)
+    ou, lu = fa.forward(q.to(DEV), k.to(DEV), v.to(DEV), causal=False)
+    torch.cuda.synchronize()
+    assert np.array_equal(o, ou.float().cpu().numpy())
