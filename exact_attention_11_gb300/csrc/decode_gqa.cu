@@ -103,13 +103,16 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   // Value mapping: lane -> rows d = (lane >> 1) + 16 j, tokens 8 (lane & 1) .. +7.
   const int vrow = lane >> 1, vhalf = lane & 1;
 
-  float m[G], l[G], acc[G][8];
+  // acc2[g][j]: two partial sums (even and odd tokens of the lane's eight)
+  // of output row vrow + 16 j of head g, as one packed fp32 pair.
+  float m[G], l[G];
+  uint64_t acc2[G][8];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     m[g] = -INFINITY;
     l[g] = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[g][j] = 0.f;
+    for (int j = 0; j < 8; ++j) acc2[g][j] = f2(0.f, 0.f);
   }
 
   const int b_begin = part * kPartBlocks;
@@ -148,28 +151,33 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     const uint8_t *vb = kb + kSlice;
     const bool tail = b * kBlk + ktok >= ctx;   // this lane's token is past the context
 
-    // Scores: for each head, this lane's token against its 8 key chunks, read
-    // from the ring as needed (the one-head kernel's order: an 8-term chain
-    // per 16-byte chunk, chunks summed in turn).
+    // Scores: this lane's token against its 8 key chunks (dimensions 8c ..
+    // 8c + 7, c = 2i + parity); each chunk is read and widened once and used
+    // by every head, two dimensions per packed fp32 FMA.
+    uint64_t t2[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) t2[g] = f2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = 2 * i + kpar;
+      const uint4 kv = *reinterpret_cast<const uint4 *>(kb + ((c * kBlk + ktok) * kX) * 2);
+      const uint64_t k01 = f2(bf_lo(kv.x), bf_hi(kv.x)), k23 = f2(bf_lo(kv.y), bf_hi(kv.y));
+      const uint64_t k45 = f2(bf_lo(kv.z), bf_hi(kv.z)), k67 = f2(bf_lo(kv.w), bf_hi(kv.w));
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float4 *q4 = reinterpret_cast<const float4 *>(&sq[g][c * kX]);
+        const float4 a = q4[0], b4 = q4[1];
+        t2[g] = ffma2(f2(a.x, a.y), k01, t2[g]);
+        t2[g] = ffma2(f2(a.z, a.w), k23, t2[g]);
+        t2[g] = ffma2(f2(b4.x, b4.y), k45, t2[g]);
+        t2[g] = ffma2(f2(b4.z, b4.w), k67, t2[g]);
+      }
+    }
     float alpha[G], p8[G][8];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      float t = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 kv = *reinterpret_cast<const uint4 *>(kb + (((2 * i + kpar) * kBlk + ktok) * kX) * 2);
-        const float4 *q4 = reinterpret_cast<const float4 *>(&sq[g][(2 * i + kpar) * kX]);
-        const float4 a = q4[0], c = q4[1];
-        float d8 = a.x * bf_lo(kv.x);
-        d8 = fmaf(a.y, bf_hi(kv.x), d8);
-        d8 = fmaf(a.z, bf_lo(kv.y), d8);
-        d8 = fmaf(a.w, bf_hi(kv.y), d8);
-        d8 = fmaf(c.x, bf_lo(kv.z), d8);
-        d8 = fmaf(c.y, bf_hi(kv.z), d8);
-        d8 = fmaf(c.z, bf_lo(kv.w), d8);
-        d8 = fmaf(c.w, bf_hi(kv.w), d8);
-        t += d8;
-      }
+      const float2 tt = f2_split(t2[g]);
+      float t = tt.x + tt.y;
       t += __shfl_xor_sync(~0u, t, 16);
       if (tail) t = -INFINITY;
       float bmax = t;
@@ -186,18 +194,27 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 #pragma unroll
       for (int e = 0; e < 8; ++e) p8[g][e] = __shfl_sync(~0u, p, 8 * vhalf + e);
     }
-    // Values: each 16-byte chunk read and widened once, used by all heads (eq. (4)).
+    // Values: each 16-byte chunk read and widened once, used by all heads
+    // (eq. (4)), two tokens per packed FMA.
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const uint64_t a2 = f2(alpha[g], alpha[g]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc2[g][j] = fmul2(acc2[g][j], a2);
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint4 vv = *reinterpret_cast<const uint4 *>(vb + ((vrow + 16 * j) * kBlk + 8 * vhalf) * 2);
-      const float v8[8] = {bf_lo(vv.x), bf_hi(vv.x), bf_lo(vv.y), bf_hi(vv.y),
-                           bf_lo(vv.z), bf_hi(vv.z), bf_lo(vv.w), bf_hi(vv.w)};
+      const uint64_t v01 = f2(bf_lo(vv.x), bf_hi(vv.x)), v23 = f2(bf_lo(vv.y), bf_hi(vv.y));
+      const uint64_t v45 = f2(bf_lo(vv.z), bf_hi(vv.z)), v67 = f2(bf_lo(vv.w), bf_hi(vv.w));
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float a = acc[g][j] * alpha[g];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) a = fmaf(p8[g][e], v8[e], a);
-        acc[g][j] = a;
+        uint64_t a = acc2[g][j];
+        a = ffma2(f2(p8[g][0], p8[g][1]), v01, a);
+        a = ffma2(f2(p8[g][2], p8[g][3]), v23, a);
+        a = ffma2(f2(p8[g][4], p8[g][5]), v45, a);
+        a = ffma2(f2(p8[g][6], p8[g][7]), v67, a);
+        acc2[g][j] = a;
       }
     }
     // The stage has been read: refill it with block k + kStages.
@@ -221,11 +238,17 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   // Every warp takes part in the merge; s_abort tells them to stop there.
   __syncthreads();
   if (s_abort) return;
-  // The two lanes of a row hold tokens 0-7 and 8-15: add them.
+  // The two lanes of a row hold tokens 0-7 and 8-15: add them (after the
+  // even and odd halves of each lane's packed sums).
+  float acc[G][8];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[g][j] += __shfl_xor_sync(~0u, acc[g][j], 1);
+    for (int j = 0; j < 8; ++j) {
+      const float2 a = f2_split(acc2[g][j]);
+      acc[g][j] = a.x + a.y;
+      acc[g][j] += __shfl_xor_sync(~0u, acc[g][j], 1);
+    }
     if (lane == 0) {
       s_m[warp][g] = m[g];
       s_l[warp][g] = l[g];

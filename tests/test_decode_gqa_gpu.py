@@ -69,8 +69,9 @@ def test_gqa_decode_benchmark_workload():
 
 def test_gqa_decode_equals_replicated_one_head_decode():
     """The grouped kernel and the one-head kernel on caches whose key/value heads
-    are repeated for their query heads give the same outputs (both compute the
-    same sums; only the order of the per-head work differs)."""
+    are repeated for their query heads give the same outputs up to the order of
+    their fp32 sums (the grouped kernel adds even and odd terms in separate
+    packed lanes): at most one bf16 step apart, and mostly bit-equal."""
     S, H, Hk = 4, 8, 2
     di = inputs.decode_inputs(S, H, 128, 16, 900, seed=11, device=DEV, num_kv_heads=Hk)
     g = fa.paged_decode(di.q, di.k_cache, di.v_cache, di.block_tables, di.context_lens, di.scale)
@@ -78,4 +79,6 @@ def test_gqa_decode_equals_replicated_one_head_decode():
     vc = di.v_cache.repeat_interleave(H // Hk, dim=1).contiguous()
     m = fa.paged_decode(di.q, kc, vc, di.block_tables, di.context_lens, di.scale)
     torch.cuda.synchronize()
-    assert torch.equal(g, m)
+    gf, mf = g.float(), m.float()
+    assert ((gf - mf).abs() <= mf.abs() * 2.0 ** -7 + 1e-6).all()
+    assert (gf == mf).float().mean().item() > 0.8
