@@ -634,6 +634,14 @@ def gpu_arm(args):
             "unit": "TFLOP/s",
             "frac_of_bf16_peak": round(fwd_flops(**FWD_D256) / (d256_ms * 1e-3) / 1e12 / peak_t,
                                        4),
+            "roofline": {"bound": "tensor",
+                         "achieved": round(weak_scaling_rate(fwd_flops(**FWD_D256), 1, d256_ms,
+                                                             1e12), 2),
+                         "peak": peak_t, "unit": "TFLOP/s",
+                         "frac": round(weak_scaling_rate(fwd_flops(**FWD_D256), 1, d256_ms, 1e12)
+                                       / peak_t, 4),
+                         "traffic": recorded_traffic("fwd_d256_kernel<0>"),
+                         "peak_kind": f"{peak_kind} bf16 burst", "kernel": "fwd_d256_kernel<0>"},
         },
         "fwd_fp8": {
             "workload": "fa_forward_fp8 on the forward workload block-quantized to E4M3 "
