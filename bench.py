@@ -626,6 +626,7 @@ def gpu_arm(args):
             "value": round(weak_scaling_rate(flops, ws, masked_ms, 1e12), 2),
             "unit": "TFLOP/s",
             "frac_of_bf16_peak": round(flops / (masked_ms * 1e-3) / 1e12 / peak_t, 4),
+            "traffic_forward_kernel": recorded_traffic("fwd_bf16_tc_kernel<128,0,1,0>"),
         },
         "fwd_d256": {
             "workload": "fa_forward bf16 B=2 H=8 N=4096 d=256 causal",
