@@ -347,7 +347,8 @@ int fa_quantize_fp8(const void *q, const void *k, const void *v, const float *si
   const float rot_factor = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   return cuda_status(fattn::launch_fp8_quantize(
       q, k, v, signs, q8, k8, vt8, q_scale, k_scale, v_scale, static_cast<float *>(workspace),
-      (int)BH, N, (int)fp8_vt_stride(N), rot_factor, reinterpret_cast<cudaStream_t>(stream)));
+      (int)BH, N, (int)fp8_vt_stride(N), rot_factor, g_dev[dev].status,
+      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int fa_forward_fp8(const void *q8, const void *k8, const void *vt8, const float *q_scale,

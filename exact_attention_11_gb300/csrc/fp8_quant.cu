@@ -18,7 +18,9 @@
 //
 // The work is HBM-bound: each kernel reads its 128 x 128 bf16 block once
 // (V twice: once for the head's amax, once to code it) and writes 16 KB of
-// codes.
+// codes.  A CTA stages its block in shared memory with one 32 KB bulk copy,
+// so the bytes in flight per SM are bounded by shared memory (up to seven
+// blocks) rather than by registers.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -33,12 +35,6 @@ constexpr int kD = 128;
 constexpr int kRows = 128;          // rows per quantization block
 constexpr int kThreads = 256;       // 8 warps x 16 rows
 constexpr int kRowsPerWarp = kRows / (kThreads / 32);
-
-__device__ __forceinline__ float4 load_bf16x4(const uint16_t *p) {
-  const uint2 u = *reinterpret_cast<const uint2 *>(p);
-  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-}
 
 // One butterfly stage across lanes: the lane whose `mask` bit is clear keeps
 // a + b, its partner a - b (a the lower-index value, b the higher).
@@ -83,35 +79,84 @@ __device__ __forceinline__ uint32_t code4(float4 v, float inv) {
                      __fmul_rn(v.w, inv));
 }
 
+// Stages rows r0 .. r0 + n_rows - 1 of one head (contiguous, 256 bytes each)
+// in shared memory with one bulk copy; false if the copy did not arrive
+// within the wait limit (then *dev_status is set).
+__device__ __forceinline__ bool stage_rows(const uint16_t *src, uint32_t dst, int n_rows,
+                                           uint32_t bar, volatile int *abort_flag,
+                                           int *dev_status) {
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n_rows) * kD * 2);
+    bulk_load(dst, src, static_cast<uint32_t>(n_rows) * kD * 2, bar);
+  }
+  if (!mbar_wait(bar, 0, abort_flag)) {
+    if (threadIdx.x == 0) atomicExch(dev_status, kDevTimeout);
+    return false;
+  }
+  return true;
+}
+
+// Four values of staged row r (lane's columns 4 lane .. 4 lane + 3); rows past
+// the block's end read as zero.
+__device__ __forceinline__ float4 staged4(const uint8_t *stage, int r, int n_rows, int lane) {
+  if (r >= n_rows) return make_float4(0.f, 0.f, 0.f, 0.f);
+  const uint2 u = *reinterpret_cast<const uint2 *>(stage + r * (kD * 2) + lane * 8);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
 // grid (n_blk, BH, 3): z = 0 codes Q, z = 1 codes K, z = 2 records the
-// block's |V| maximum in v_amax[bh * n_blk + blk].
+// block's |V| maximum in v_amax[bh * n_blk + blk].  The block is staged in
+// shared memory by one bulk copy, then read twice (maximum, then codes), so
+// without the transform the registers hold no block data and seven CTAs fit
+// per SM.
 template <bool ROT>
 __global__ void __launch_bounds__(kThreads)
     fp8_quant_rows_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
                           const uint16_t *__restrict__ v, const float *__restrict__ signs,
                           uint8_t *__restrict__ q8, uint8_t *__restrict__ k8,
                           float *__restrict__ q_scale, float *__restrict__ k_scale,
-                          float *__restrict__ v_amax, int N, int n_blk, float rot_factor) {
+                          float *__restrict__ v_amax, int N, int n_blk, float rot_factor,
+                          int *__restrict__ dev_status) {
+  extern __shared__ __align__(128) uint8_t stage[];   // 128 rows x 256 bytes
   __shared__ float red[kThreads / 32];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
   const int blk = blockIdx.x, bh = blockIdx.y, which = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint16_t *src = which == 0 ? q : which == 1 ? k : v;
   const int64_t head = static_cast<int64_t>(bh) * N;
-  const int r0 = blk * kRows + warp * kRowsPerWarp;
+  const int r0 = blk * kRows, n_rows = min(kRows, N - r0);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (!stage_rows(src + (head + r0) * kD, smem_u32(stage), n_rows, smem_u32(&bar), &abort_flag,
+                  dev_status))
+    return;
+  const bool rot = ROT && which < 2;
   float4 sg = make_float4(1.f, 1.f, 1.f, 1.f);
-  if (ROT && which < 2) sg = *reinterpret_cast<const float4 *>(signs + 4 * lane);
-  float4 x[kRowsPerWarp];
+  if (rot) sg = *reinterpret_cast<const float4 *>(signs + 4 * lane);
+  auto row_values = [&](int r) {
+    float4 x = staged4(stage, r, n_rows, lane);
+    if (rot) {
+      x = make_float4(x.x * sg.x, x.y * sg.y, x.z * sg.z, x.w * sg.w);
+      hadamard_row(x, lane);
+    }
+    return x;
+  };
+  // With the transform the rotated rows are kept in registers between the
+  // two passes (the butterfly is the costly part); without it they are
+  // re-read from shared memory, which keeps the kernel at 32 registers.
+  float4 xr[ROT ? kRowsPerWarp : 1];
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < kRowsPerWarp; ++i) {
-    const int r = r0 + i;
-    x[i] = r < N ? load_bf16x4(src + (head + r) * kD + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-    if (ROT && which < 2) {
-      x[i] = make_float4(x[i].x * sg.x, x[i].y * sg.y, x[i].z * sg.z, x[i].w * sg.w);
-      hadamard_row(x[i], lane);
-    }
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x[i].x), fabsf(x[i].y)),
-                             fmaxf(fabsf(x[i].z), fabsf(x[i].w))));
+    const float4 x = row_values(warp * kRowsPerWarp + i);
+    if (ROT) xr[ROT ? i : 0] = x;
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
   }
   amax = block_max(amax, red);
   if (which == 2) {
@@ -123,8 +168,10 @@ __global__ void __launch_bounds__(kThreads)
   uint8_t *dst = which == 0 ? q8 : k8;
 #pragma unroll
   for (int i = 0; i < kRowsPerWarp; ++i) {
-    const int r = r0 + i;
-    if (r < N) *reinterpret_cast<uint32_t *>(dst + (head + r) * kD + 4 * lane) = code4(x[i], inv);
+    const int r = warp * kRowsPerWarp + i;
+    const float4 x = ROT ? xr[ROT ? i : 0] : row_values(r);
+    if (r < n_rows)
+      *reinterpret_cast<uint32_t *>(dst + (head + r0 + r) * kD + 4 * lane) = code4(x, inv);
   }
   if (threadIdx.x == 0)
     (which == 0 ? q_scale : k_scale)[static_cast<int64_t>(bh) * n_blk + blk] =
@@ -132,30 +179,47 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // grid (n_blk, BH): codes one 128-row block of V with its head's scale and
-// writes it transposed into V^T [BH][128][Npad].
+// writes it transposed into V^T [BH][128][Npad].  The block's bulk copy is
+// issued first, so it lands while the head's block maxima are reduced.
 __global__ void __launch_bounds__(kThreads)
     fp8_quant_v_kernel(const uint16_t *__restrict__ v, const float *__restrict__ v_amax,
                        uint8_t *__restrict__ vt8, float *__restrict__ v_scale, int N, int n_blk,
-                       int n_pad) {
+                       int n_pad, int *__restrict__ dev_status) {
   constexpr int kPitch = kRows + 1;   // bytes per transposed row in shared memory
+  extern __shared__ __align__(128) uint8_t stage[];   // 128 rows x 256 bytes
   __shared__ uint8_t tile[kD * kPitch];
   __shared__ float red[kThreads / 32];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
   const int blk = blockIdx.x, bh = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t head = static_cast<int64_t>(bh) * N;
+  const int r0 = blk * kRows, n_rows = min(kRows, N - r0);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(smem_u32(&bar), static_cast<uint32_t>(n_rows) * kD * 2);
+    bulk_load(smem_u32(stage), v + (head + r0) * kD, static_cast<uint32_t>(n_rows) * kD * 2,
+              smem_u32(&bar));
+  }
   float amax = 0.f;
   for (int i = threadIdx.x; i < n_blk; i += kThreads)
     amax = fmaxf(amax, v_amax[static_cast<int64_t>(bh) * n_blk + i]);
   amax = block_max(amax, red);
   const float s = scale_of(amax);
   const float inv = __fdiv_rn(1.f, s);
-  const int64_t head = static_cast<int64_t>(bh) * N;
+  if (!mbar_wait(smem_u32(&bar), 0, &abort_flag)) {
+    if (threadIdx.x == 0) atomicExch(dev_status, kDevTimeout);
+    return;
+  }
 #pragma unroll 4
   for (int i = 0; i < kRowsPerWarp; ++i) {
     const int rl = warp * kRowsPerWarp + i;        // key within the block
-    const int r = blk * kRows + rl;
-    const float4 x =
-        r < N ? load_bf16x4(v + (head + r) * kD + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const uint32_t c = code4(x, inv);
+    const uint32_t c = code4(staged4(stage, rl, n_rows, lane), inv);
 #pragma unroll
     for (int e = 0; e < 4; ++e) tile[(4 * lane + e) * kPitch + rl] = (c >> (8 * e)) & 0xffu;
   }
@@ -176,6 +240,8 @@ __global__ void __launch_bounds__(kThreads)
   if (blk == 0 && threadIdx.x == 0) v_scale[bh] = s;
 }
 
+constexpr int kStageBytes = kRows * kD * 2;   // 32 KB of staged bf16 rows
+
 }  // namespace
 
 size_t fp8_quant_workspace_bytes(int BH, int N) {
@@ -185,24 +251,35 @@ size_t fp8_quant_workspace_bytes(int BH, int N) {
 cudaError_t launch_fp8_quantize(const void *q, const void *k, const void *v, const float *signs,
                                 void *q8, void *k8, void *vt8, float *q_scale, float *k_scale,
                                 float *v_scale, float *v_amax, int BH, int N, int n_pad,
-                                float rot_factor, cudaStream_t stream) {
+                                float rot_factor, int *dev_status, cudaStream_t stream) {
   const int n_blk = (N + kRows - 1) / kRows;
   const dim3 g1(n_blk, BH, 3);
   const auto *qq = static_cast<const uint16_t *>(q);
   const auto *kk = static_cast<const uint16_t *>(k);
   const auto *vv = static_cast<const uint16_t *>(v);
-  if (signs != nullptr)
-    fp8_quant_rows_kernel<true><<<g1, kThreads, 0, stream>>>(
+  cudaError_t e;
+  if (signs != nullptr) {
+    e = cudaFuncSetAttribute(fp8_quant_rows_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
+    if (e != cudaSuccess) return e;
+    fp8_quant_rows_kernel<true><<<g1, kThreads, kStageBytes, stream>>>(
         qq, kk, vv, signs, static_cast<uint8_t *>(q8), static_cast<uint8_t *>(k8), q_scale,
-        k_scale, v_amax, N, n_blk, rot_factor);
-  else
-    fp8_quant_rows_kernel<false><<<g1, kThreads, 0, stream>>>(
+        k_scale, v_amax, N, n_blk, rot_factor, dev_status);
+  } else {
+    e = cudaFuncSetAttribute(fp8_quant_rows_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
+    if (e != cudaSuccess) return e;
+    fp8_quant_rows_kernel<false><<<g1, kThreads, kStageBytes, stream>>>(
         qq, kk, vv, nullptr, static_cast<uint8_t *>(q8), static_cast<uint8_t *>(k8), q_scale,
-        k_scale, v_amax, N, n_blk, rot_factor);
-  cudaError_t e = cudaGetLastError();
+        k_scale, v_amax, N, n_blk, rot_factor, dev_status);
+  }
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  fp8_quant_v_kernel<<<dim3(n_blk, BH), kThreads, 0, stream>>>(
-      vv, v_amax, static_cast<uint8_t *>(vt8), v_scale, N, n_blk, n_pad);
+  e = cudaFuncSetAttribute(fp8_quant_v_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kStageBytes);
+  if (e != cudaSuccess) return e;
+  fp8_quant_v_kernel<<<dim3(n_blk, BH), kThreads, kStageBytes, stream>>>(
+      vv, v_amax, static_cast<uint8_t *>(vt8), v_scale, N, n_blk, n_pad, dev_status);
   return cudaGetLastError();
 }
 

@@ -66,7 +66,7 @@ size_t fp8_quant_workspace_bytes(int BH, int N);
 cudaError_t launch_fp8_quantize(const void *q, const void *k, const void *v, const float *signs,
                                 void *q8, void *k8, void *vt8, float *q_scale, float *k_scale,
                                 float *v_scale, float *v_amax, int BH, int N, int n_pad,
-                                float rot_factor, cudaStream_t stream);
+                                float rot_factor, int *dev_status, cudaStream_t stream);
 
 // Backward: workspace = fp32 dQ accumulator (row-major [BH][N][d] inside
 // B*H*Npad*d floats, Npad = N rounded up to 128), then [-LSE2 | -D] (2 x 128
