@@ -18,6 +18,7 @@ import threading
 
 __all__ = ["fa_forward", "fa_forward_f16", "fa_forward_masked", "forward_masked", "fa_forward_fp32", "fa_paged_decode", "fa_paged_decode_noalloc",
            "fa_backward", "fa_backward_workspace_bytes", "backward", "fa_paged_decode_gqa",
+           "fa_decode_gqa_select",
            "fa_status_string", "fa_quantize_fp8", "fa_quantize_fp8_workspace_bytes",
            "fa_fp8_vt_stride", "fa_forward_fp8", "quantize_fp8", "forward_fp8", "Fp8Inputs",
            "fa_device_status", "fa_release", "forward", "paged_decode", "FattnError",
@@ -66,6 +67,7 @@ EXPORTS = {
     "fa_device_status": ([], _i),
     "fa_release": ([], None),
     "fa_debug_inject_fault": ([_i], _i),
+    "fa_decode_gqa_select": ([_i], _i),
     "fa_version": ([], _i),
 }
 
@@ -197,6 +199,12 @@ def fa_debug_inject_fault(mode: int) -> int:
     """Test hook: arm (1) or disarm (0) a lost-copy fault in the next forward
     launch on the current device (see fattn.h)."""
     return _check("fa_debug_inject_fault", load().fa_debug_inject_fault(mode))
+
+
+def fa_decode_gqa_select(impl: int) -> int:
+    """Kernel for fa_paged_decode_gqa: 0 = automatic (default), 1 = the
+    CUDA-core kernel only, 2 = the tensor-core kernel only (see fattn.h)."""
+    return _check("fa_decode_gqa_select", load().fa_decode_gqa_select(impl))
 
 
 # ---------------------------------------------------------------- torch helpers

@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfattn.so")
 SOURCES = ["api.cu", "fwd_f32.cu", "fwd_bf16.cu", "decode.cu", "decode_noalloc.cu",
            "bwd_bf16.cu", "bwd_bf16_d128.cu", "decode_gqa.cu", "fp8_quant.cu",
-           "fwd_d256.cu", "mask_tiles.cu"]
+           "fwd_d256.cu", "mask_tiles.cu", "decode_gqa_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
          "--expt-relaxed-constexpr"]

@@ -7,6 +7,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -35,6 +36,7 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+std::atomic<int> g_decode_gqa_impl{0};   // fa_decode_gqa_select: 0 auto, 1 CUDA cores, 2 tensor cores
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -112,6 +114,37 @@ int encode_e4m3_map(CUtensorMap *m, const void *base, int BH, int rows, int inne
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// TMA views of the paged caches for the tensor-core grouped decode.  K cache
+// [blocks][Hk][16 d-groups][16 tokens][8]: 5-D dims (8 tokens x 8 values,
+// token half, d-group, head, block), boxes of 64 x 1 x 16 (one token half's
+// 16 d-groups: 2 KB of no-swizzle core matrices, in 128-byte rows).  V cache
+// [blocks][Hk][128 d][16 tokens]: 4-D dims (token, d, head, block), boxes of
+// 16 x 128 (a block's V^T, 4 KB) written with the 32-byte swizzle.  The block
+// extent is the largest int block id: which blocks are read comes from the
+// block tables, as in the plain decode.
+int encode_paged_kv_maps(CUtensorMap *tk, CUtensorMap *tv, const void *k_cache,
+                         const void *v_cache, int num_kv_heads) {
+  const cuuint64_t nb = 0x7fffffffull, hk = (cuuint64_t)num_kv_heads;
+  const cuuint64_t kd[5] = {64, 2, 16, hk, nb};
+  const cuuint64_t ks[4] = {128, 256, 4096, 4096 * hk};
+  const cuuint32_t kb[5] = {64, 1, 16, 1, 1};
+  const cuuint64_t vd[4] = {16, 128, hk, nb};
+  const cuuint64_t vs[3] = {32, 4096, 4096 * hk};
+  const cuuint32_t vb[4] = {16, 128, 1, 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  if (g_encode(tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(k_cache), kd, ks, kb,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return FA_ERR_CUDA;
+  if (g_encode(tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(v_cache), vd, vs, vb,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 // Keys per row of the transposed FP8 V: N rounded up to 16.
@@ -445,7 +478,11 @@ int fa_paged_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
   if (num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads != 0)
     return FA_ERR_INVALID_ARG;
   const int group = num_heads / num_kv_heads;
-  if (group > 1 && !fattn::decode_gqa_group_supported(group)) return FA_ERR_UNSUPPORTED;
+  const int impl = g_decode_gqa_impl.load();
+  const bool cc_ok = fattn::decode_gqa_group_supported(group);
+  const bool tc_ok = fattn::decode_gqa_tc_supported(group);
+  const bool tc = group > 1 && (impl == 2 ? tc_ok : impl == 0 ? (tc_ok && !cc_ok) : false);
+  if (group > 1 && !tc && (impl == 2 || !cc_ok)) return FA_ERR_UNSUPPORTED;
   float *ws = nullptr;
   int *counters = nullptr, *status = nullptr;
   const int rc = decode_prepare(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs,
@@ -457,6 +494,23 @@ int fa_paged_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
     return cuda_status(fattn::launch_paged_decode(q, k_cache, v_cache, block_tables,
                                                   context_lens, out, num_seqs, num_heads,
                                                   max_num_blocks_per_seq, scale, ws, counters, s));
+  if (tc) {
+    CUtensorMap tk, tv;
+    int *sched = nullptr;
+    {
+      std::lock_guard<std::mutex> lock(g_mu);
+      int dev = 0, rc2;
+      if ((rc2 = current_device(&dev)) != FA_OK) return rc2;
+      if ((rc2 = get_encoder()) != FA_OK) return rc2;
+      DeviceState &st = g_dev[dev];
+      sched = st.fwd_sched + 2 * (st.fwd_sched_next++ % fattn::kFwdSchedSlots);
+    }
+    int rc2;
+    if ((rc2 = encode_paged_kv_maps(&tk, &tv, k_cache, v_cache, num_kv_heads)) != FA_OK) return rc2;
+    return cuda_status(fattn::launch_paged_decode_gqa_tc(
+        tk, tv, q, block_tables, context_lens, out, num_seqs, num_heads, num_kv_heads,
+        max_num_blocks_per_seq, scale, ws, counters, sched, status, s));
+  }
   return cuda_status(fattn::launch_paged_decode_gqa(q, k_cache, v_cache, block_tables,
                                                     context_lens, out, num_seqs, num_heads,
                                                     num_kv_heads, max_num_blocks_per_seq, scale,
@@ -473,6 +527,12 @@ int fa_device_status(void) {
     return FA_ERR_CUDA;
   if (h != 0 && cudaMemset(g_dev[dev].status, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
   return h;
+}
+
+int fa_decode_gqa_select(int impl) {
+  if (impl < 0 || impl > 2) return FA_ERR_INVALID_ARG;
+  g_decode_gqa_impl.store(impl);
+  return FA_OK;
 }
 
 int fa_debug_inject_fault(int mode) {

@@ -133,6 +133,11 @@ __global__ void __launch_bounds__(kWarps * 32)
     for (int i = 0; i < 8; ++i) kv[i] = ld_stream(kb + ((2 * i + kpar) * kBlk + ktok) * kX);
 #pragma unroll
     for (int j = 0; j < 8; ++j) vv[j] = ld_stream(vb + (vrow + 16 * j) * kBlk + 8 * vhalf);
+    const int nv = ctx - b * kBlk - 8 * vhalf;   // this lane's value tokens inside the context
+    if (nv < 8) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) vv[j] = keep_first_16b(vv[j], nv);
+    }
 
     float t = 0.f;
 #pragma unroll

@@ -202,9 +202,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc2[g][j] = fmul2(acc2[g][j], a2);
     }
+    const int nv = ctx - b * kBlk - 8 * vhalf;   // this lane's value tokens inside the context
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const uint4 vv = *reinterpret_cast<const uint4 *>(vb + ((vrow + 16 * j) * kBlk + 8 * vhalf) * 2);
+      uint4 vv = *reinterpret_cast<const uint4 *>(vb + ((vrow + 16 * j) * kBlk + 8 * vhalf) * 2);
+      if (nv < 8) vv = keep_first_16b(vv, nv);
       const uint64_t v01 = f2(bf_lo(vv.x), bf_hi(vv.x)), v23 = f2(bf_lo(vv.y), bf_hi(vv.y));
       const uint64_t v45 = f2(bf_lo(vv.z), bf_hi(vv.z)), v67 = f2(bf_lo(vv.w), bf_hi(vv.w));
 #pragma unroll

@@ -100,6 +100,17 @@ cudaError_t launch_paged_decode_gqa(const void *q, const void *k_cache, const vo
                                     int num_seqs, int num_heads, int num_kv_heads, int max_blocks,
                                     float scale, float *workspace, int *counters,
                                     int *dev_status, cudaStream_t stream);
+// Grouped key/value heads on the tensor cores (decode_gqa_tc.cu): group =
+// num_heads / num_kv_heads from 2 to 16, or a multiple of 16.  tm_k / tm_v are
+// the 5-D views of the caches (encode_paged_kv_maps in api.cu); sched is a
+// pair of work counters kept at zero; same workspace and counters as above.
+bool decode_gqa_tc_supported(int group);
+cudaError_t launch_paged_decode_gqa_tc(const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                       const void *q, const int *block_tables,
+                                       const int *context_lens, void *out, int num_seqs,
+                                       int num_heads, int num_kv_heads, int max_blocks,
+                                       float scale, float *workspace, int *counters, int *sched,
+                                       int *dev_status, cudaStream_t stream);
 // Split-K workspace: per (sequence, head, partition) an unnormalised output
 // row and its (max, sum) pair, in fp32.  `counters` holds one int per
 // (sequence, head); it must be all zero before the first launch and every

@@ -263,11 +263,16 @@ int fa_paged_decode(const void *q, const void *k_cache, const void *v_cache,
  * head h attends with key/value head h / (num_heads / num_kv_heads), i.e.
  * consecutive query heads share one cached head (num_kv_heads = 1 is
  * multi-query attention).  q and out are [num_seqs, num_heads, head_size].
- * Each cached block is read once for up to four query heads of its group.
+ * Each cached block is read once for up to 16 query heads of its group
+ * (tensor-core kernel) or four (CUDA-core kernel).  Cache slots past a
+ * sequence's context may hold any bits, NaN included: they never reach the
+ * output.
  *
  * Arguments and errors as for fa_paged_decode, plus: FA_ERR_INVALID_ARG when
  * num_kv_heads <= 0 or does not divide num_heads; FA_ERR_UNSUPPORTED when the
- * group size num_heads / num_kv_heads is not 1, 2 or a multiple of 4.
+ * selected kernel does not take the group size num_heads / num_kv_heads.  By
+ * default sizes 1 to 16 and every multiple of 4 are taken; see
+ * fa_decode_gqa_select.
  * Group size 1 is exactly fa_paged_decode.  Shares fa_paged_decode's
  * library-owned workspace.
  */
@@ -276,6 +281,25 @@ int fa_paged_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
                         int num_seqs, int num_heads, int num_kv_heads, int head_size,
                         int block_size, int max_num_blocks_per_seq, float scale,
                         fa_stream_t stream);
+
+/*
+ * fa_decode_gqa_select -- chooses which kernel fa_paged_decode_gqa runs for
+ * group sizes 2 and up (process-wide, every device; takes effect at the next
+ * call).
+ *
+ *  impl 0 (the default): automatic -- the CUDA-core kernel for group sizes 2
+ *         and multiples of 4, the tensor-core kernel for the other sizes it
+ *         takes (3, 5, 6, 7, 9 ... 15).
+ *  impl 1: the CUDA-core kernel only (group 2 or a multiple of 4): up to four
+ *         query heads per pass over a cached block, fp32 FMAs.
+ *  impl 2: the tensor-core kernel only (group 2 to 16, or a multiple of 16):
+ *         128 context tokens are the M rows and up to 16 query heads the N
+ *         columns of tcgen05 MMAs; P is rounded to bf16 for the P V product.
+ *
+ * Both compute the same attention; results differ in rounding only.  Returns
+ * FA_OK, or FA_ERR_INVALID_ARG for another impl.
+ */
+int fa_decode_gqa_select(int impl);
 
 /*
  * fa_paged_decode_noalloc -- fa_paged_decode for callers that cannot allocate

@@ -82,17 +82,37 @@ def test_decode_argument_checks(lib, args, expect):
     assert lib.fa_paged_decode_gqa(*gargs, None) == expect
 
 
-@pytest.mark.parametrize("H,Hk,expect", [
-    (8, 0, -1),     # no key/value heads
-    (8, 3, -1),     # does not divide
-    (12, 4, -2),    # group of 3: not built
-    (24, 4, -2),    # group of 6: not built
-    (8, 4, 0),      # group of 2: valid (no sequences: no-op)
-    (32, 4, 0),     # group of 8
-    (64, 1, 0),     # multi-query
+@pytest.mark.parametrize("impl,H,Hk,expect", [
+    (0, 8, 0, -1),     # no key/value heads
+    (0, 8, 3, -1),     # does not divide
+    (0, 12, 4, 0),     # group of 3: tensor-core kernel
+    (0, 24, 4, 0),     # group of 6
+    (0, 36, 2, -2),    # group of 18: neither kernel
+    (0, 17, 1, -2),    # group of 17
+    (0, 40, 2, 0),     # group of 20: CUDA-core kernel (multiple of 4)
+    (0, 8, 4, 0),      # group of 2: valid (no sequences: no-op)
+    (0, 32, 4, 0),     # group of 8
+    (0, 64, 1, 0),     # multi-query
+    (1, 12, 4, -2),    # CUDA-core only: group of 3 is not built
+    (1, 24, 4, -2),    # group of 6
+    (1, 32, 4, 0),     # group of 8
+    (1, 64, 1, 0),     # multi-query
+    (2, 12, 4, 0),     # tensor-core only: group of 3
+    (2, 40, 2, -2),    # group of 20 is not a multiple of 16
+    (2, 64, 2, 0),     # group of 32: two slices of 16
+    (2, 8, 8, 0),      # group 1 is the one-head decode whatever the choice
 ])
-def test_gqa_decode_group_checks(lib, H, Hk, expect):
-    assert lib.fa_paged_decode_gqa(P, P, P, P, P, P, 0, H, Hk, 128, 16, 4, 0.1, None) == expect
+def test_gqa_decode_group_checks(lib, impl, H, Hk, expect):
+    assert lib.fa_decode_gqa_select(impl) == 0
+    try:
+        assert lib.fa_paged_decode_gqa(P, P, P, P, P, P, 0, H, Hk, 128, 16, 4, 0.1, None) == expect
+    finally:
+        lib.fa_decode_gqa_select(0)
+
+
+def test_gqa_select_rejects_unknown(lib):
+    assert lib.fa_decode_gqa_select(3) == -1
+    assert lib.fa_decode_gqa_select(-1) == -1
 
 
 W = 1 << 20  # a workspace size larger than any case below needs

@@ -99,3 +99,43 @@ def test_decode_repeat_is_deterministic_and_counters_reset():
     b = run_and_check(di)
     assert torch.equal(a, b)
     assert fa.fa_device_status() == 0
+
+
+def poisoned_caches(di):
+    """Copies of the caches with NaN in every slot past each sequence's
+    context: the tail of its last block and the blocks it does not use."""
+    kc, vc = di.k_cache.clone(), di.v_cache.clone()
+    bs = di.block_size
+    ctx = di.context_lens.cpu().tolist()
+    bt = di.block_tables.cpu()
+    for s, c in enumerate(ctx):
+        for j in range(bt.shape[1]):
+            first = c - bs * j                   # first unused slot of this block
+            if first >= bs:
+                continue
+            blk = int(bt[s, j])
+            kc[blk, :, :, max(first, 0):, :] = float("nan")
+            vc[blk, :, :, max(first, 0):] = float("nan")
+    return kc, vc
+
+
+def test_decode_ignores_cache_slots_past_the_context():
+    """Slots past a sequence's context may hold anything: with NaN there the
+    output is bit-equal to the clean run, for the allocating and the
+    fixed-scratch decode."""
+    di = inputs.decode_inputs(6, 4, 128, 16, 1000, seed=16, device=DEV)
+    di.context_lens.copy_(torch.tensor([1000, 3, 130, 515, 17, 999], dtype=torch.int32,
+                                       device=DEV))
+    clean = run_and_check(di).clone()
+    kc, vc = poisoned_caches(di)
+    out = fa.paged_decode(di.q, kc, vc, di.block_tables, di.context_lens, di.scale)
+    out2 = torch.empty_like(out)
+    S, H, D = di.q.shape
+    fa.fa_paged_decode_noalloc(di.q.data_ptr(), kc.data_ptr(), vc.data_ptr(),
+                               di.block_tables.data_ptr(), di.context_lens.data_ptr(),
+                               out2.data_ptr(), S, H, D, di.block_size, di.block_tables.shape[1],
+                               di.scale, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    assert torch.equal(out, clean)
+    assert torch.equal(out2, clean)
