@@ -30,6 +30,10 @@ struct DeviceState {
   unsigned fwd_sched_next = 0;    // slot for the next forward launch
   void *mask_ws = nullptr;        // tile summary of the last mask (fa_forward_masked)
   size_t mask_ws_bytes = 0;
+  CUtensorMap kv_map_k, kv_map_v; // last TMA views of paged caches (grouped decode)
+  const void *kv_maps_k = nullptr, *kv_maps_v = nullptr;
+  int kv_maps_hk = 0;
+  bool kv_maps_valid = false;
   int inject_fault = 0;           // fa_debug_inject_fault: armed for the next forward
   int checked = 0;                // 1: sm_103 verified, -1: unsupported
 };
@@ -481,7 +485,13 @@ int fa_paged_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
   const int impl = g_decode_gqa_impl.load();
   const bool cc_ok = fattn::decode_gqa_group_supported(group);
   const bool tc_ok = fattn::decode_gqa_tc_supported(group);
-  const bool tc = group > 1 && (impl == 2 ? tc_ok : impl == 0 ? (tc_ok && !cc_ok) : false);
+  // Automatic: the tensor-core kernel from group 3 up once there is at least
+  // a unit (sequence, partition, cached head) per SM; measured faster there,
+  // and slower for group 2 and for a handful of units.
+  const long long units_bound = (long long)num_seqs * num_kv_heads *
+                                fattn::decode_max_parts(max_num_blocks_per_seq);
+  const bool tc_auto = tc_ok && (!cc_ok || (group >= 3 && units_bound >= fattn::kDecodeTcMinUnits));
+  const bool tc = group > 1 && (impl == 2 ? tc_ok : impl == 0 ? tc_auto : false);
   if (group > 1 && !tc && (impl == 2 || !cc_ok)) return FA_ERR_UNSUPPORTED;
   float *ws = nullptr;
   int *counters = nullptr, *status = nullptr;
@@ -498,18 +508,31 @@ int fa_paged_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
     CUtensorMap tk, tv;
     int *sched = nullptr;
     {
+      // The views depend only on the caches' addresses and head count: the
+      // last pair encoded on the device is reused while those stay the same.
       std::lock_guard<std::mutex> lock(g_mu);
       int dev = 0, rc2;
       if ((rc2 = current_device(&dev)) != FA_OK) return rc2;
       if ((rc2 = get_encoder()) != FA_OK) return rc2;
       DeviceState &st = g_dev[dev];
       sched = st.fwd_sched + 2 * (st.fwd_sched_next++ % fattn::kFwdSchedSlots);
+      if (!(st.kv_maps_valid && st.kv_maps_k == k_cache && st.kv_maps_v == v_cache &&
+            st.kv_maps_hk == num_kv_heads)) {
+        st.kv_maps_valid = false;
+        if ((rc2 = encode_paged_kv_maps(&st.kv_map_k, &st.kv_map_v, k_cache, v_cache,
+                                        num_kv_heads)) != FA_OK)
+          return rc2;
+        st.kv_maps_k = k_cache;
+        st.kv_maps_v = v_cache;
+        st.kv_maps_hk = num_kv_heads;
+        st.kv_maps_valid = true;
+      }
+      tk = st.kv_map_k;
+      tv = st.kv_map_v;
     }
-    int rc2;
-    if ((rc2 = encode_paged_kv_maps(&tk, &tv, k_cache, v_cache, num_kv_heads)) != FA_OK) return rc2;
     return cuda_status(fattn::launch_paged_decode_gqa_tc(
         tk, tv, q, block_tables, context_lens, out, num_seqs, num_heads, num_kv_heads,
-        max_num_blocks_per_seq, scale, ws, counters, sched, status, s));
+        max_num_blocks_per_seq, scale, ws, sched, status, s));
   }
   return cuda_status(fattn::launch_paged_decode_gqa(q, k_cache, v_cache, block_tables,
                                                     context_lens, out, num_seqs, num_heads,

@@ -29,6 +29,7 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "decode_util.cuh"
 #include "ptx.cuh"
 
 namespace fattn {

@@ -43,7 +43,11 @@ namespace {
 
 constexpr int kHead = kDecodeHeadSize;                       // 128
 constexpr int kBlk = kDecodeBlockSize;                       // 16 tokens per cache block
-constexpr int kPartBlocks = kDecodePartitionTokens / kBlk;   // 32
+// Blocks per partition (a work unit's context span; partitions are merged by
+// a second kernel).  Up to 64: the producer warp holds two block ids a lane.
+constexpr int kPartBlocks = 64;
+static_assert(kPartBlocks % 8 == 0 && kPartBlocks <= 64, "partition size");
+constexpr int kPartTokens = kPartBlocks * kBlk;
 constexpr int kStepBlocks = 8;                               // 128 tokens per step
 constexpr int kNCols = 16;                                   // query heads per MMA (N)
 constexpr int kThreads = 320;
@@ -64,7 +68,7 @@ constexpr int kOffRing = 0;
 constexpr int kOffQ = kOffRing + kSlots * kStepBytes;     // 2 buffers
 constexpr int kOffP = kOffQ + 2 * kQBytes;                // 2 buffers
 constexpr int kOffRed = kOffP + 2 * kPBytes;              // [2][4 warps][16] floats
-constexpr int kOffStats = kOffRed + 2 * 4 * kNCols * 4;   // UnitStats [2], then [2][4] ints
+constexpr int kOffStats = kOffRed + 2 * 4 * kNCols * 4;   // UnitStats [2]
 constexpr int kOffSeq = kOffStats + 1024;                 // int2 [kDenseSeqs + 1]
 constexpr int kOffBar = kOffSeq + (kDenseSeqs + 32) * 8;
 constexpr int kSmemBytes = kOffBar + 512;
@@ -87,8 +91,7 @@ enum : int {
   kBarOFull = 27,      // + O buffer (2): the unit's last P V is done
   kBarOFree = 29,      // + O buffer (2): the epilogue has read O and the stats (count 4)
   kBarStats = 31,      // + O buffer (2): the softmax has written the stats (count 4)
-  kBarERed = 33,       // + 0/1: the 4 epilogue warps' exchange (count 4)
-  kNumBars = 35
+  kNumBars = 33
 };
 // Arrivals that free an item slot: the MMA thread and the 4 softmax warps.
 constexpr int kItemConsumers = 1 + 4;
@@ -101,7 +104,7 @@ struct UnitStats {
   float m[kNCols];
   float l[4][kNCols];
 };
-static_assert(2 * sizeof(UnitStats) + 2 * 4 * 4 <= 1024, "stats area");
+static_assert(2 * sizeof(UnitStats) <= 1024, "stats area");
 
 struct Misc {
   uint32_t tmem_base;
@@ -277,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                const int *__restrict__ block_tables,
                                const int *__restrict__ context_lens, uint16_t *__restrict__ out,
                                float *__restrict__ ws_o, float *__restrict__ ws_ml,
-                               int *__restrict__ counters, int *__restrict__ sched, int num_seqs,
+                               int *__restrict__ sched, int num_seqs,
                                int num_heads, int num_kv_heads, int group, int gs, int max_blocks,
                                int max_parts, float qscale, int *__restrict__ dev_status) {
   extern __shared__ uint8_t smem_raw[];
@@ -349,7 +352,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarOFull + i), 1);
       mbar_init(bar(kBarOFree + i), 4);
       mbar_init(bar(kBarStats + i), 4);
-      mbar_init(bar(kBarERed + i), 4);
     }
     mbar_init(bar(kBarDrain), 1);
     for (int i = 0; i < kItemSlots; ++i) {
@@ -392,6 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     Unit nxt;
     int lane_pb = 0;      // block id of the unit's block `lane` (the last one past the context)
+    int lane_pb2 = 0;     // and of its block 32 + lane
     uint4 qv[8];          // 16-byte chunk lane + 32 i of the unit's [16 heads][128] queries
     int w_pending = 0;    // lane 0: the claim in flight
     bool pending = false;
@@ -419,8 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto prefetch = [&]() {
       if (nxt.s < 0) return;
       const int n_blocks = (nxt.ctx + kBlk - 1) / kBlk;
-      lane_pb = block_tables[static_cast<int64_t>(nxt.s) * max_blocks +
-                             min(nxt.part * kPartBlocks + lane, n_blocks - 1)];
+      const int *bt = block_tables + static_cast<int64_t>(nxt.s) * max_blocks;
+      lane_pb = bt[min(nxt.part * kPartBlocks + lane, n_blocks - 1)];
+      if (kPartBlocks > 32) lane_pb2 = bt[min(nxt.part * kPartBlocks + 32 + lane, n_blocks - 1)];
       const uint4 *qr = reinterpret_cast<const uint4 *>(
           q + (static_cast<int64_t>(nxt.s) * num_heads + nxt.hb) * kHead);
 #pragma unroll
@@ -435,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (nxt.s >= 0) request();
     for (int k = 0; ok; ++k) {
       const Unit cur = nxt;
+      const int cur_pb = lane_pb, cur_pb2 = lane_pb2;
       if (lane == 0) {
         const int slot = k % kItemSlots;
         ok = mbar_wait(bar(kBarItemEmpty + slot), ((k / kItemSlots) & 1) ^ 1, abort_flag);
@@ -445,26 +450,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __shfl_sync(~0u, ok, 0);
       if (!ok || cur.s < 0) break;
-      // Q into buffer n_active & 1 once the MMA thread's last Q K^T of the
-      // unit two before has read it: [d-group][head][8], heads past the slice 0.
-      const int qb = n_active & 1;
-      if (lane == 0)
-        ok = mbar_wait(bar(kBarQEmpty + qb), ((n_active >> 1) & 1) ^ 1, abort_flag);
-      if (!(ok = __shfl_sync(~0u, ok, 0))) break;
-      uint8_t *qs = smem + kOffQ + qb * kQBytes;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int c = lane + 32 * i;
-        *reinterpret_cast<uint4 *>(qs + ((c & 15) * kNCols + (c >> 4)) * 16) = qv[i];
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarQFull + qb));
-      ++n_active;
-      const int cur_pb = lane_pb;
-      finish();
-      prefetch();
-      if (nxt.s >= 0) request();
       const int n_steps = steps_of(cur.part, cur.ctx);
       for (int st = 0; st < n_steps; ++st) {
         const int slot = n_steps_loaded % kSlots;
@@ -473,19 +458,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = __shfl_sync(~0u, ok, 0))) break;
         const uint32_t full = bar(kBarKVFull + slot);
         if (lane == 0) mbar_arrive_expect_tx(full, kStepBytes);
-        const uint32_t base = s_base + kOffRing + slot * kStepBytes;
-#pragma unroll
-        for (int b = 0; b < kStepBlocks; ++b) {
-          // Blocks past the context repeat the last block: finite or not,
-          // their tokens get zero weight and zero values.
-          const int pb = __shfl_sync(~0u, cur_pb, st * kStepBlocks + b);
-          if (lane == 0) {
-            tma_load_5d(base + (2 * b) * kBox, &tm_k, 0, 0, 0, cur.kvh, pb, full);
-            tma_load_5d(base + (2 * b + 1) * kBox, &tm_k, 0, 1, 0, cur.kvh, pb, full);
-            tma_load_4d(base + kStepK + (2 * b) * kBox, &tm_v, 0, 0, cur.kvh, pb, full);
-          }
+        __syncwarp();
+        // Lane b < 8 copies block b of the step: its two K boxes and its V box.
+        // Blocks past the context repeat the last block: finite or not, their
+        // tokens get zero weight and zero values.
+        const uint32_t base = s_base + kOffRing + slot * kStepBytes + (2 * (lane & 7)) * kBox;
+        const int bi = st * kStepBlocks + (lane & 7);   // block of the partition
+        const int pb0 = __shfl_sync(~0u, cur_pb, bi & 31);
+        const int pb = (kPartBlocks > 32 && bi >= 32) ? __shfl_sync(~0u, cur_pb2, bi & 31) : pb0;
+        if (lane < kStepBlocks) {
+          tma_load_5d(base, &tm_k, 0, 0, 0, cur.kvh, pb, full);
+          tma_load_5d(base + kBox, &tm_k, 0, 1, 0, cur.kvh, pb, full);
+          tma_load_4d(base + kStepK, &tm_v, 0, 0, cur.kvh, pb, full);
         }
         ++n_steps_loaded;
+        if (st == 0) {
+          // With the first step's copies under way: Q into buffer n_active & 1
+          // once the MMA thread's last Q K^T of the unit two before has read
+          // it ([d-group][head][8], heads past the slice 0), then the next
+          // unit's claim and loads.
+          const int qb = n_active & 1;
+          if (lane == 0)
+            ok = mbar_wait(bar(kBarQEmpty + qb), ((n_active >> 1) & 1) ^ 1, abort_flag);
+          if (!(ok = __shfl_sync(~0u, ok, 0))) break;
+          uint8_t *qs = smem + kOffQ + qb * kQBytes;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int c = lane + 32 * i;
+            *reinterpret_cast<uint4 *>(qs + ((c & 15) * kNCols + (c >> 4)) * 16) = qv[i];
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarQFull + qb));
+          ++n_active;
+          finish();
+          prefetch();
+          if (nxt.s >= 0) request();
+        }
       }
     }
     // A claim still in flight (after an abort) completes before the CTA's exit
@@ -639,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint32_t sv[NC];
         tmem_ld_cols<NC>(tmem + lane_off + kColS + kNCols * b, sv);
-        const bool valid = part * kDecodePartitionTokens + j * 128 + r < ctx;
+        const bool valid = part * kPartTokens + j * 128 + r < ctx;
         if (j == n_steps - 1 && __any_sync(~0u, !valid)) {
           // Cache slots past the context hold whatever was there before; a
           // zero weight does not cancel a NaN or an infinity, so the value rows
@@ -736,23 +745,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // --------------------------------------------------------------- epilogue
     // Warps 6-9: thread r = dimension row r of O^T (TMEM lane quarter warp % 4).
-    // One-partition units are written out; the others go to the workspace,
-    // and the last partition of a (sequence, head slice) to finish merges
-    // them (eq. (4)).
+    // One-partition units are written out; the others leave their unscaled
+    // row, maximum and sum in the workspace for the merge kernel.
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    int *xch = reinterpret_cast<int *>(smem + kOffStats + 2 * sizeof(UnitStats));   // [2][4]
-    int n_x = 0;
     bool ok = true;
-    auto x_sync = [&]() -> int {
-      const int buf = n_x & 1;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarERed + buf));
-      if (!mbar_wait(bar(kBarERed + buf), (n_x >> 1) & 1, abort_flag)) return -1;
-      ++n_x;
-      return buf;
-    };
     for (int ui = 0; ok; ++ui) {
       const int ob = ui & 1;
       if (!(ok = mbar_wait(bar(kBarStats + ob), (ui >> 1) & 1, abort_flag))) break;
@@ -788,39 +786,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (hh < gs) {
           const int64_t slot = (h0 + hh) * max_parts + part;
           ws_o[slot * kHead + r] = __uint_as_float(ov[hh]);
-          if (r == 0) {
-            ws_ml[slot * 2 + 0] = mm[hh];
-            ws_ml[slot * 2 + 1] = L[hh];
-          }
+          if (r == 0) *reinterpret_cast<float2 *>(ws_ml + slot * 2) = make_float2(mm[hh], L[hh]);
         }
       }
-      // All 128 threads' partial rows are written before the count goes up;
-      // the count's last arrival merges, and resets it for the next call.
-      __threadfence();
-      ok = x_sync() >= 0;
-      if (!ok) break;
-      int *counter = counters + h0;
-      int last = 0;
-      if (r == 0) last = atomicAdd(counter, 1) == n_parts - 1;
-      if (lane == 0) xch[(n_x & 1) * 4 + quarter] = last;
-      const int xb = x_sync();
-      ok = xb >= 0;
-      if (!ok) break;
-      if (!xch[xb * 4 + 0]) continue;
-      __threadfence();
-      for (int hh = 0; hh < gs; ++hh) {
-        const int64_t base = (h0 + hh) * max_parts;
-        float Mp = -INFINITY;
-        for (int p2 = 0; p2 < n_parts; ++p2) Mp = fmaxf(Mp, __ldcg(&ws_ml[(base + p2) * 2]));
-        float Lt = 0.f, Ot = 0.f;
-        for (int p2 = 0; p2 < n_parts; ++p2) {
-          const float f = ex2_approx(__ldcg(&ws_ml[(base + p2) * 2]) - Mp);
-          Lt += __ldcg(&ws_ml[(base + p2) * 2 + 1]) * f;
-          Ot += __ldcg(&ws_o[(base + p2) * kHead + r]) * f;
-        }
-        out[(h0 + hh) * kHead + r] = static_cast<uint16_t>(pack_bf16x2(Ot / Lt, 0.f) & 0xffffu);
-      }
-      if (r == 0) *counter = 0;
     }
   }
 
@@ -841,21 +809,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Merges the partitions of every (sequence, query head) with more than one
+// (eq. (4) of "Flash Attention", section "Online Softmax", across
+// partitions): one warp per row, lane l holding dimensions 4l .. 4l + 3.
+__global__ void __launch_bounds__(256)
+    paged_decode_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_ml,
+                              const int *__restrict__ context_lens, uint16_t *__restrict__ out,
+                              int num_seqs, int num_heads, int max_parts) {
+  const int lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= static_cast<long long>(num_seqs) * num_heads) return;
+  const int n_parts = partitions_of(context_lens[row / num_heads]);
+  if (n_parts <= 1) return;   // written by the decode kernel
+  const float *ml = ws_ml + row * max_parts * 2;
+  const float *o = ws_o + row * max_parts * kHead + 4 * lane;
+  float M = -INFINITY;
+  for (int p = lane; p < n_parts; p += 32) M = fmaxf(M, __ldcg(ml + 2 * p));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, off));
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int p0 = 0; p0 < n_parts; p0 += 32) {
+    float f = 0.f;
+    if (p0 + lane < n_parts) {
+      const float2 v = __ldcg(reinterpret_cast<const float2 *>(ml) + p0 + lane);
+      f = ex2_approx(v.x - M);
+      L += v.y * f;
+    }
+    const int cnt = min(32, n_parts - p0);
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const float fj = __shfl_sync(~0u, f, j);
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(o + static_cast<int64_t>(p0 + j) * kHead));
+      acc.x += fj * v.x;
+      acc.y += fj * v.y;
+      acc.z += fj * v.z;
+      acc.w += fj * v.w;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(~0u, L, off);
+  const float inv = 1.f / L;
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2 *>(out + row * kHead + 4 * lane) = packed;
+}
+
 int g_num_sms[64] = {};
 
 template <int NC>
 cudaError_t launch_nc(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const void *q,
                       const int *block_tables, const int *context_lens, void *out, int num_seqs,
                       int num_heads, int num_kv_heads, int group, int gs, int max_blocks,
-                      int max_parts, float qscale, float *ws_o, float *ws_ml, int *counters,
-                      int *sched, int *dev_status, int grid, cudaStream_t stream) {
+                      int max_parts, float qscale, float *ws_o, float *ws_ml, int *sched,
+                      int *dev_status, int grid, cudaStream_t stream) {
   const cudaError_t e = cudaFuncSetAttribute(paged_decode_gqa_tc_kernel<NC>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
   if (e != cudaSuccess) return e;
   paged_decode_gqa_tc_kernel<NC><<<grid, kThreads, kAlloc, stream>>>(
       tm_k, tm_v, static_cast<const uint16_t *>(q), block_tables, context_lens,
-      static_cast<uint16_t *>(out), ws_o, ws_ml, counters, sched, num_seqs, num_heads,
+      static_cast<uint16_t *>(out), ws_o, ws_ml, sched, num_seqs, num_heads,
       num_kv_heads, group, gs, max_blocks, max_parts, qscale, dev_status);
+  if (max_parts > 1) {
+    const long long rows = static_cast<long long>(num_seqs) * num_heads;
+    paged_decode_merge_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+        ws_o, ws_ml, context_lens, static_cast<uint16_t *>(out), num_seqs, num_heads, max_parts);
+  }
   return cudaGetLastError();
 }
 
@@ -867,7 +887,7 @@ cudaError_t launch_paged_decode_gqa_tc(const CUtensorMap &tm_k, const CUtensorMa
                                        const void *q, const int *block_tables,
                                        const int *context_lens, void *out, int num_seqs,
                                        int num_heads, int num_kv_heads, int max_blocks,
-                                       float scale, float *workspace, int *counters, int *sched,
+                                       float scale, float *workspace, int *sched,
                                        int *dev_status, cudaStream_t stream) {
   const int group = num_heads / num_kv_heads;
   if (!decode_gqa_tc_supported(group) || group * num_kv_heads != num_heads)
@@ -883,7 +903,8 @@ cudaError_t launch_paged_decode_gqa_tc(const CUtensorMap &tm_k, const CUtensorMa
     g_num_sms[dev] = n;
   }
   const int gs = group <= kNCols ? group : kNCols;
-  const int max_parts = decode_max_parts(max_blocks);
+  // Partitions of this kernel (no more than the split-K workspace holds).
+  const int max_parts = (max_blocks + kPartBlocks - 1) / kPartBlocks;
   // The most units there can be; the kernel counts the actual ones.
   const long long n_units =
       static_cast<long long>(max_parts) * num_seqs * num_kv_heads * (group / gs);
@@ -895,7 +916,7 @@ cudaError_t launch_paged_decode_gqa_tc(const CUtensorMap &tm_k, const CUtensorMa
   const int grid = static_cast<int>(n_units < g_num_sms[dev] ? n_units : g_num_sms[dev]);
 #define FATTN_GQA_TC_ARGS                                                                       \
   tm_k, tm_v, q, block_tables, context_lens, out, num_seqs, num_heads, num_kv_heads, group, gs, \
-      max_blocks, max_parts, qscale, ws_o, ws_ml, counters, sched, dev_status, grid, stream
+      max_blocks, max_parts, qscale, ws_o, ws_ml, sched, dev_status, grid, stream
   if (gs <= 4) return launch_nc<4>(FATTN_GQA_TC_ARGS);
   if (gs <= 8) return launch_nc<8>(FATTN_GQA_TC_ARGS);
   return launch_nc<16>(FATTN_GQA_TC_ARGS);

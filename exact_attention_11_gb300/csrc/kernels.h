@@ -102,14 +102,18 @@ cudaError_t launch_paged_decode_gqa(const void *q, const void *k_cache, const vo
                                     int *dev_status, cudaStream_t stream);
 // Grouped key/value heads on the tensor cores (decode_gqa_tc.cu): group =
 // num_heads / num_kv_heads from 2 to 16, or a multiple of 16.  tm_k / tm_v are
-// the 5-D views of the caches (encode_paged_kv_maps in api.cu); sched is a
-// pair of work counters kept at zero; same workspace and counters as above.
+// the TMA views of the caches (encode_paged_kv_maps in api.cu); sched is a
+// pair of work counters kept at zero; the workspace is the split-K one below
+// (a second kernel merges the partitions; no counters).
 bool decode_gqa_tc_supported(int group);
+// Below this many (sequence, partition, cached head) units the automatic
+// choice keeps the CUDA-core kernel (fewer launches, less set-up).
+constexpr long long kDecodeTcMinUnits = 152;
 cudaError_t launch_paged_decode_gqa_tc(const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                        const void *q, const int *block_tables,
                                        const int *context_lens, void *out, int num_seqs,
                                        int num_heads, int num_kv_heads, int max_blocks,
-                                       float scale, float *workspace, int *counters, int *sched,
+                                       float scale, float *workspace, int *sched,
                                        int *dev_status, cudaStream_t stream);
 // Split-K workspace: per (sequence, head, partition) an unnormalised output
 // row and its (max, sum) pair, in fp32.  `counters` holds one int per

@@ -363,16 +363,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// The first nv of the eight 16-bit values in v (memory order), the others
-// cleared to +0.  Used on cache slots past a sequence's context, whose bits are
-// arbitrary: a zero attention weight does not cancel a NaN or an infinity.
-__device__ __forceinline__ uint4 keep_first_16b(uint4 v, int nv) {
-  auto k2 = [nv](uint32_t w, int i) -> uint32_t {
-    return i + 1 < nv ? w : (i < nv ? (w & 0xffffu) : 0u);
-  };
-  return make_uint4(k2(v.x, 0), k2(v.y, 2), k2(v.z, 4), k2(v.w, 6));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

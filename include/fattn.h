@@ -287,9 +287,11 @@ int fa_paged_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
  * group sizes 2 and up (process-wide, every device; takes effect at the next
  * call).
  *
- *  impl 0 (the default): automatic -- the CUDA-core kernel for group sizes 2
- *         and multiples of 4, the tensor-core kernel for the other sizes it
- *         takes (3, 5, 6, 7, 9 ... 15).
+ *  impl 0 (the default): automatic -- the tensor-core kernel for group sizes
+ *         3 and up when num_seqs x num_kv_heads x ceil(max_num_blocks_per_seq
+ *         / 32) is at least 152, and for the sizes only it takes; otherwise
+ *         the CUDA-core kernel (group 2, and small problems, where it is
+ *         faster).
  *  impl 1: the CUDA-core kernel only (group 2 or a multiple of 4): up to four
  *         query heads per pass over a cached block, fp32 FMAs.
  *  impl 2: the tensor-core kernel only (group 2 to 16, or a multiple of 16):
