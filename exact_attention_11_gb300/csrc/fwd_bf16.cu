@@ -93,8 +93,12 @@ struct Cfg {
   static constexpr int kK0 = kQ + 2 * kTileBytes;
   static constexpr int kV0 = kK0 + kStages * kTileBytes;
   static constexpr int kBar = kV0 + kStages * kTileBytes;
-  static constexpr int kBytes = kBar + 512;
+  // Epilogue staging: per softmax warp (2 tiles x 4) its 32 rows x 64 columns
+  // of bf16 output, 4 KB.
+  static constexpr int kStage = kBar + 512;
+  static constexpr int kBytes = kStage + 8 * 4096;
   static constexpr int kAlloc = kBytes + 1024;      // slack for 1 KB alignment
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
 };
@@ -677,28 +681,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float inv_l = (MASK && l == 0.f) ? 0.f : 1.f / l;
       if (FP8) inv_l *= v_scale[bh];
-      uint16_t *orow = o + (static_cast<int64_t>(bh) * N + row) * D;
+      // O rows leave through shared memory: each warp packs its 32 rows, 64
+      // columns at a time, into a 4 KB buffer (16-byte chunks swizzled by the
+      // row so that neither side has bank conflicts) and reads it back so that
+      // eight lanes store one row's 128 contiguous bytes: 4 lines per store
+      // instruction instead of 32.
+      uint8_t *stg = smem + C::kStage + (t * 4 + quarter) * 4096;
+      const int lane = threadIdx.x & 31;
+      const int row_w = row - lane;   // this warp's first row
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(o_tmem + c * 32, ov);
-        tmem_wait_ld(ov);
-        if (row < N) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+      for (int h = 0; h < D / 64; ++h) {
+        uint32_t ov[2][32];
+        tmem_ld32(o_tmem + 64 * h, ov[0]);
+        tmem_ld32(o_tmem + 64 * h + 32, ov[1]);
+        tmem_wait_ld(ov[0]);
+        tmem_wait_ld(ov[1]);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 v;
-            v.x = pack2<F16>(__uint_as_float(ov[8 * e + 0]) * inv_l,
-                              __uint_as_float(ov[8 * e + 1]) * inv_l);
-            v.y = pack2<F16>(__uint_as_float(ov[8 * e + 2]) * inv_l,
-                              __uint_as_float(ov[8 * e + 3]) * inv_l);
-            v.z = pack2<F16>(__uint_as_float(ov[8 * e + 4]) * inv_l,
-                              __uint_as_float(ov[8 * e + 5]) * inv_l);
-            v.w = pack2<F16>(__uint_as_float(ov[8 * e + 6]) * inv_l,
-                              __uint_as_float(ov[8 * e + 7]) * inv_l);
-            dst[e] = v;
-          }
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t *c8 = &ov[k >> 2][(k & 3) * 8];
+          uint4 v;
+          v.x = pack2<F16>(__uint_as_float(c8[0]) * inv_l, __uint_as_float(c8[1]) * inv_l);
+          v.y = pack2<F16>(__uint_as_float(c8[2]) * inv_l, __uint_as_float(c8[3]) * inv_l);
+          v.z = pack2<F16>(__uint_as_float(c8[4]) * inv_l, __uint_as_float(c8[5]) * inv_l);
+          v.w = pack2<F16>(__uint_as_float(c8[6]) * inv_l, __uint_as_float(c8[7]) * inv_l);
+          *reinterpret_cast<uint4 *>(stg + lane * 128 + ((k ^ (lane & 7)) * 16)) = v;
         }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int rr = (lane >> 3) + 4 * k, ch = lane & 7;
+          const uint4 v = *reinterpret_cast<const uint4 *>(stg + rr * 128 + ((ch ^ (rr & 7)) * 16));
+          if (row_w + rr < N)
+            *reinterpret_cast<uint4 *>(o + (static_cast<int64_t>(bh) * N + row_w + rr) * D +
+                                       64 * h + ch * 8) = v;
+        }
+        __syncwarp();
       }
       if (lse != nullptr && row < N)
         lse[static_cast<int64_t>(bh) * N + row] =
