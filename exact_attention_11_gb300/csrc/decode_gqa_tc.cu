@@ -371,6 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
   const int n_units = nb.n_units();
+  // The merge kernel may be scheduled now: its threads wait (griddepcontrol)
+  // until this grid has finished and its writes are visible.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   auto read_item = [&](int k, int4 &it) -> bool {
     if (!mbar_wait(bar(kBarItemFull + k % kItemSlots), (k / kItemSlots) & 1, abort_flag))
@@ -816,6 +819,9 @@ __global__ void __launch_bounds__(256)
     paged_decode_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_ml,
                               const int *__restrict__ context_lens, uint16_t *__restrict__ out,
                               int num_seqs, int num_heads, int max_parts) {
+  // Launched as a programmatic dependent of the decode kernel: wait for it to
+  // finish (its workspace writes are then visible).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (row >= static_cast<long long>(num_seqs) * num_heads) return;
@@ -872,9 +878,26 @@ cudaError_t launch_nc(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const vo
       static_cast<uint16_t *>(out), ws_o, ws_ml, sched, num_seqs, num_heads,
       num_kv_heads, group, gs, max_blocks, max_parts, qscale, dev_status);
   if (max_parts > 1) {
+    // Programmatic dependent launch: the merge grid is scheduled while the
+    // decode grid runs and starts its work when that grid completes, which
+    // hides its launch latency.
     const long long rows = static_cast<long long>(num_seqs) * num_heads;
-    paged_decode_merge_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-        ws_o, ws_ml, context_lens, static_cast<uint16_t *>(out), num_seqs, num_heads, max_parts);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_merge_kernel,
+                                             static_cast<const float *>(ws_o),
+                                             static_cast<const float *>(ws_ml), context_lens,
+                                             static_cast<uint16_t *>(out), num_seqs, num_heads,
+                                             max_parts);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
