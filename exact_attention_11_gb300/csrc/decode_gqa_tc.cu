@@ -6,8 +6,8 @@
 // q[s,h,:] over the context_lens[s] cached tokens of key/value head
 // h / G ("PagedAttention", data-sketchers.com, sections "Inputs", "Key",
 // "Value"), with the online softmax of eqs. (2)-(4) of "Flash Attention"
-// (suniverse77.github.io, section "Online Softmax") and 512-token partitions
-// merged with eq. (4).
+// (suniverse77.github.io, section "Online Softmax") and 1024-token partitions
+// merged with eq. (4) by a second kernel.
 //
 // Per 128-token step (8 cache blocks), for a slice of gs <= 16 query heads:
 //   S^T [128 tokens][16 heads] = K [128 tokens][128 d] . Q^T     (8 MMAs, K = 16 each)
@@ -18,17 +18,17 @@
 // values, 2 KB), exactly the no-swizzle K-major core matrices (8 rows x 16
 // bytes) of A = K, and 16 boxes 2 KB apart make one 128-row operand; a V box
 // is a block's V^T (128 dimensions x 16 tokens, 4 KB) in the 32-byte-swizzle
-// K-major layout of A = V^T, one MMA (K = 16 tokens) per block.  The softmax is cheap:
-// each thread holds one token's scores, and a step needs one cross-warp
-// maximum per head; row sums stay per thread until the end.
+// K-major layout of A = V^T, one MMA (K = 16 tokens) per block.  The softmax
+// is cheap: each thread holds one token's scores, and a step needs one
+// cross-warp maximum per head; row sums stay per thread until the end.
 //
 // Persistent CTAs (one per SM) take work units (sequence, partition, cached
 // head, head slice) from a device-wide counter.  Warp roles:
-//   warps 0-3   softmax (thread = token row of S^T) and epilogue (thread =
-//               dimension row of O^T)
+//   warps 0-3   softmax (thread = token row of S^T)
 //   warp 4      producer: claims units (prefetching the next unit's block ids
 //               and queries), writes Q, issues the TMA copies
 //   warp 5      MMA issuer (one lane), polling for whichever MMA group is ready
+//   warps 6-9   epilogue (thread = dimension row of O^T, double-buffered)
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -54,7 +54,7 @@ constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 64;     // S^T 2 x 16 | O^T 2 x 16
 constexpr uint32_t kColS = 0, kColO = 32;
 
-constexpr int kBox = 2048;                          // one 5-D TMA box
+constexpr int kBox = 2048;                          // one K box (a V box is two)
 constexpr int kStepK = 2 * kStepBlocks * kBox;      // 32 KB of K boxes
 constexpr int kStepBytes = 2 * kStepK;              // K and V of a step
 constexpr int kSlots = 3;                           // steps in flight
