@@ -20,8 +20,8 @@
  *  - NaN or Inf inputs are not checked for; they propagate per IEEE rules.
  *
  * The library owns only small per-device state (the split-K workspace of the
- * paged decode, its counters, and cached launch attributes); fa_release()
- * frees it.  Calls on one device from several host threads are safe; calls
+ * paged decode, its counters, cached launch attributes and the last TMA views
+ * of a paged cache); fa_release() frees it.  Calls on one device from several host threads are safe; calls
  * whose work overlaps on the GPU may share that workspace only if they are
  * ordered on one stream.
  */
@@ -245,7 +245,8 @@ int fa_backward(const void *q, const void *k, const void *v, const void *o,
  * of 512 tokens whose partial (max, sum, output) triples are merged with the
  * output update of eq. (4) of the "Flash Attention" page; the partials live
  * in a workspace the library owns and grows on first use for a given size
- * (cudaMallocAsync on `stream`).  num_seqs == 0 is a no-op.
+ * (cudaMalloc; growing it first frees the smaller one, which synchronises
+ * the device).  num_seqs == 0 is a no-op.
  */
 int fa_paged_decode(const void *q, const void *k_cache, const void *v_cache,
                     const int *block_tables, const int *context_lens, void *out,
