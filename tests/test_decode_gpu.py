@@ -139,3 +139,14 @@ def test_decode_ignores_cache_slots_past_the_context():
     assert fa.fa_device_status() == 0
     assert torch.equal(out, clean)
     assert torch.equal(out2, clean)
+
+
+def test_decode_shared_prefix_blocks():
+    """Sequences sharing physical cache blocks (a common prefix) read them
+    independently."""
+    di = inputs.decode_inputs(4, 4, 128, 16, 900, seed=17, device=DEV)
+    bt = di.block_tables.clone()
+    bt[1:, :5] = bt[0, :5]
+    di.block_tables.copy_(bt)
+    di.context_lens.copy_(torch.tensor([900, 700, 333, 81], dtype=torch.int32, device=DEV))
+    run_and_check(di)

@@ -55,6 +55,7 @@ def _check(di, ctx=None):
     (3, 7, 1, 700),      # group 7
     (2, 32, 2, 1500),    # group 16: every MMA column
     (2, 64, 2, 800),     # group 32: two slices of 16
+    (2, 96, 2, 700),     # group 48: three slices of 16 / twelve sub-groups of 4
 ])
 def test_gqa_decode_matches_oracle(impl, S, H, Hk, max_ctx):
     if impl == 1 and H // Hk in TC_ONLY:
@@ -114,6 +115,16 @@ def test_gqa_decode_many_sequences(impl):
     fa.fa_decode_gqa_select(impl)
     torch.cuda.synchronize()
     assert (out.float() - other.float()).abs().max().item() <= TOL
+
+
+def test_gqa_decode_shared_prefix_blocks(impl):
+    """Sequences whose block tables share physical blocks (a cached common
+    prefix) each read them as their own."""
+    di = inputs.decode_inputs(4, 16, 128, 16, 900, seed=51, device=DEV, num_kv_heads=4)
+    bt = di.block_tables.clone()
+    bt[1:, :5] = bt[0, :5]
+    di.block_tables.copy_(bt)
+    _check(di, ctx=[900, 700, 333, 81])
 
 
 def test_gqa_decode_repeat_calls_are_identical(impl):
