@@ -77,7 +77,7 @@ static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 
 constexpr int kItemSlots = 4;
 enum : int {
-  kBarKVFull = 0,      // + slot (3)
+  kBarKFull = 0,       // + slot (3): the step's K boxes have landed
   kBarSlotFree = 3,    // + slot (3)
   kBarQFull = 6,       // + buffer (2)
   kBarQEmpty = 8,      // + buffer (2)
@@ -91,7 +91,8 @@ enum : int {
   kBarOFull = 27,      // + O buffer (2): the unit's last P V is done
   kBarOFree = 29,      // + O buffer (2): the epilogue has read O and the stats (count 4)
   kBarStats = 31,      // + O buffer (2): the softmax has written the stats (count 4)
-  kNumBars = 33
+  kBarVFull = 33,      // + slot (3): the step's V boxes have landed
+  kNumBars = 36
 };
 // Arrivals that free an item slot: the MMA thread and the 4 softmax warps.
 constexpr int kItemConsumers = 1 + 4;
@@ -339,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSlots; ++i) {
-      mbar_init(bar(kBarKVFull + i), 1);
+      mbar_init(bar(kBarKFull + i), 1);
+      mbar_init(bar(kBarVFull + i), 1);
       mbar_init(bar(kBarSlotFree + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -459,21 +461,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0)
           ok = mbar_wait(bar(kBarSlotFree + slot), ((n_steps_loaded / kSlots) & 1) ^ 1, abort_flag);
         if (!(ok = __shfl_sync(~0u, ok, 0))) break;
-        const uint32_t full = bar(kBarKVFull + slot);
-        if (lane == 0) mbar_arrive_expect_tx(full, kStepBytes);
+        const uint32_t kfull = bar(kBarKFull + slot), vfull = bar(kBarVFull + slot);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(kfull, kStepK);
+          mbar_arrive_expect_tx(vfull, kStepBytes - kStepK);
+        }
         __syncwarp();
-        // Lane b < 8 copies block b of the step: its two K boxes and its V box.
-        // Blocks past the context repeat the last block: finite or not, their
-        // tokens get zero weight and zero values.
+        // Lane b < 8 copies block b of the step: its two K boxes, then (after
+        // every lane's K) its V box, on separate barriers so that Q K^T can
+        // start while V is still arriving.  Blocks past the context repeat the
+        // last block: finite or not, their tokens get zero weight and zero
+        // values.
         const uint32_t base = s_base + kOffRing + slot * kStepBytes + (2 * (lane & 7)) * kBox;
         const int bi = st * kStepBlocks + (lane & 7);   // block of the partition
         const int pb0 = __shfl_sync(~0u, cur_pb, bi & 31);
         const int pb = (kPartBlocks > 32 && bi >= 32) ? __shfl_sync(~0u, cur_pb2, bi & 31) : pb0;
         if (lane < kStepBlocks) {
-          tma_load_5d(base, &tm_k, 0, 0, 0, cur.kvh, pb, full);
-          tma_load_5d(base + kBox, &tm_k, 0, 1, 0, cur.kvh, pb, full);
-          tma_load_4d(base + kStepK, &tm_v, 0, 0, cur.kvh, pb, full);
+          tma_load_5d(base, &tm_k, 0, 0, 0, cur.kvh, pb, kfull);
+          tma_load_5d(base + kBox, &tm_k, 0, 1, 0, cur.kvh, pb, kfull);
         }
+        __syncwarp();
+        if (lane < kStepBlocks) tma_load_4d(base + kStepK, &tm_v, 0, 0, cur.kvh, pb, vfull);
         ++n_steps_loaded;
         if (st == 0) {
           // With the first step's copies under way: Q into buffer n_active & 1
@@ -504,8 +512,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // is counted, so that the counter reset cannot be overtaken.
     if (pending && __shfl_sync(~0u, w_pending, 0) == -1) misc->abort = 1;
     if (!ok && lane == 0)
-      for (int i = (n_steps_loaded > kSlots ? n_steps_loaded - kSlots : 0); i < n_steps_loaded; ++i)
-        drain_wait(bar(kBarKVFull + i % kSlots), (i / kSlots) & 1);
+      for (int i = (n_steps_loaded > kSlots ? n_steps_loaded - kSlots : 0); i < n_steps_loaded;
+           ++i) {
+        drain_wait(bar(kBarKFull + i % kSlots), (i / kSlots) & 1);
+        drain_wait(bar(kBarVFull + i % kSlots), (i / kSlots) & 1);
+      }
   } else if (warp == 5) {
     if (elect_one()) {
       // ------------------------------------------------------------ MMA issuer
@@ -526,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool progress = false;
         const int ob = u_head & 1;
         if (gp < gq && mbar_try_wait(bar(kBarPReady + (gp & 1)), (gp >> 1) & 1) &&
+            mbar_try_wait(bar(kBarVFull + gp % kSlots), (gp / kSlots) & 1) &&
             (jp > 0 || mbar_try_wait(bar(kBarOFree + ob), ((u_head >> 1) & 1) ^ 1))) {
           tc_fence_after();
           const uint32_t vbase = s_base + kOffRing + (gp % kSlots) * kStepBytes + kStepK;
@@ -566,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             if (!q_ready)
               q_ready = mbar_try_wait(bar(kBarQFull + (n_qunits & 1)), (n_qunits >> 1) & 1);
-            if (q_ready && mbar_try_wait(bar(kBarKVFull + gq % kSlots), (gq / kSlots) & 1)) {
+            if (q_ready && mbar_try_wait(bar(kBarKFull + gq % kSlots), (gq / kSlots) & 1)) {
               tc_fence_after();
               const uint32_t kbase = s_base + kOffRing + (gq % kSlots) * kStepBytes;
               const uint32_t qbase = s_base + kOffQ + (n_qunits & 1) * kQBytes;
@@ -655,9 +667,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j == n_steps - 1 && __any_sync(~0u, !valid)) {
           // Cache slots past the context hold whatever was there before; a
           // zero weight does not cancel a NaN or an infinity, so the value rows
-          // of those tokens are cleared (the step's copies have landed: the
-          // same transaction completed before S was computed).
-          if (!(ok = mbar_wait(bar(kBarKVFull + g % kSlots), (g / kSlots) & 1, abort_flag))) break;
+          // of those tokens are cleared once the step's V boxes have landed.
+          if (!(ok = mbar_wait(bar(kBarVFull + g % kSlots), (g / kSlots) & 1, abort_flag))) break;
           if (!valid) {
             // Token r's value of dimension d: block r / 16's box, row d, 16-byte
             // chunk (token half) swizzled by bit 2 of d.
