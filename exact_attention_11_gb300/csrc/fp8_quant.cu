@@ -127,6 +127,8 @@ __global__ void __launch_bounds__(kThreads)
   const uint16_t *src = which == 0 ? q : which == 1 ? k : v;
   const int64_t head = static_cast<int64_t>(bh) * N;
   const int r0 = blk * kRows, n_rows = min(kRows, N - r0);
+  // The V kernel may be scheduled once every block of this one has begun.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bar), 1);
     abort_flag = 0;
@@ -206,6 +208,9 @@ __global__ void __launch_bounds__(kThreads)
     bulk_load(smem_u32(stage), v + (head + r0) * kD, static_cast<uint32_t>(n_rows) * kD * 2,
               smem_u32(&bar));
   }
+  // A programmatic dependent of the rows kernel: its V block is already on
+  // the way; the per-block maxima it reads next come from that kernel.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   float amax = 0.f;
   for (int i = threadIdx.x; i < n_blk; i += kThreads)
     amax = fmaxf(amax, v_amax[static_cast<int64_t>(bh) * n_blk + i]);
@@ -278,9 +283,18 @@ cudaError_t launch_fp8_quantize(const void *q, const void *k, const void *v, con
   e = cudaFuncSetAttribute(fp8_quant_v_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kStageBytes);
   if (e != cudaSuccess) return e;
-  fp8_quant_v_kernel<<<dim3(n_blk, BH), kThreads, kStageBytes, stream>>>(
-      vv, v_amax, static_cast<uint8_t *>(vt8), v_scale, N, n_blk, n_pad, dev_status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_blk, BH);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kStageBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fp8_quant_v_kernel, vv, static_cast<const float *>(v_amax),
+                            static_cast<uint8_t *>(vt8), v_scale, N, n_blk, n_pad, dev_status);
 }
 
 }  // namespace fattn

@@ -271,6 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
+  // The masked forward is launched as a programmatic dependent of the mask
+  // summary kernels: its set-up above overlaps their tail, and nothing it
+  // reads from global memory is touched before they have finished.
+  if (MASK) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
@@ -773,6 +777,24 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
   const int grid = static_cast<int>(n_items < g_num_sms[dev] ? n_items : g_num_sms[dev]);
   const float scale_log2 = scale * 1.4426950408889634f;
   const int n_sblk = (N + BM - 1) / BM;
+  if (MASK) {
+    // After the mask summary kernels: a programmatic dependent launch (the
+    // kernel waits for them with griddepcontrol.wait after its set-up).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fwd_bf16_tc_kernel<D, F16, MASK, FP8>, tq, tk, tv,
+                              reinterpret_cast<uint16_t *>(o), lse, N, BH, n_qblocks, scale_log2,
+                              causal, sched, dev_status, fault_cta, mask, mask_bh_stride, q_scale,
+                              k_scale, v_scale, n_sblk, mask_ranges, mask_flags);
+  }
   fwd_bf16_tc_kernel<D, F16, MASK, FP8><<<grid, kThreads, C::kAlloc, stream>>>(
       tq, tk, tv, reinterpret_cast<uint16_t *>(o), lse, N, BH, n_qblocks, scale_log2, causal,
       sched, dev_status, fault_cta, mask, mask_bh_stride, q_scale, k_scale, v_scale, n_sblk,

@@ -32,6 +32,8 @@ __device__ __forceinline__ bool all_bytes_nonzero(uint32_t x) {
 __global__ void __launch_bounds__(256)
     mask_tile_flags_kernel(const uint8_t *__restrict__ mask, int64_t bh_stride, int N, int n_t,
                            uint8_t *__restrict__ flags) {
+  // The ranges kernel may be scheduled once every block of this one has begun.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int kt = blockIdx.x, qt = blockIdx.y, mh = blockIdx.z;
   const uint8_t *base = mask + static_cast<int64_t>(mh) * bh_stride;
   int any = 0, all = 1;
@@ -57,6 +59,10 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(32)
     mask_item_ranges_kernel(const uint8_t *__restrict__ flags, int n_t, int n_pairs,
                             int2 *__restrict__ ranges) {
+  // A programmatic dependent of the flags kernel: wait for its flags; the
+  // forward that follows may be scheduled meanwhile.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int qp = blockIdx.x, mh = blockIdx.y, lane = threadIdx.x;
   const uint8_t *fa = flags + (static_cast<int64_t>(mh) * n_t + 2 * qp) * n_t;
   const bool has_b = 2 * qp + 1 < n_t;
@@ -103,7 +109,19 @@ cudaError_t launch_mask_summary(const uint8_t *mask, int64_t bh_stride, int N, i
                                                                           f);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mask_item_ranges_kernel<<<dim3(n_pairs, mask_heads), 32, 0, stream>>>(f, n_t, n_pairs, r);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_pairs, mask_heads);
+  cfg.blockDim = dim3(32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mask_item_ranges_kernel, static_cast<const uint8_t *>(f), n_t,
+                         n_pairs, r);
+  if (e != cudaSuccess) return e;
   *flags = f;
   *ranges = r;
   return cudaGetLastError();
