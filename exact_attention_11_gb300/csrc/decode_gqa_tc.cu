@@ -309,35 +309,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // P columns past NC are never written: zero both P buffers once.
   for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += kThreads)
     reinterpret_cast<uint4 *>(smem + kOffP)[i] = make_uint4(0u, 0u, 0u, 0u);
-  if (nb.dense) {
-    // Partition counts per sequence, then their exclusive prefix sum (warp 0).
-    // Sequences with no context get zero outputs here, from CTA 0.
-    for (int i = threadIdx.x; i < num_seqs; i += kThreads) {
-      const int c = context_lens[i];
-      seq[i] = make_int2(partitions_of(c), c);
-      if (c <= 0 && blockIdx.x == 0) {
-        uint4 *o = reinterpret_cast<uint4 *>(out + static_cast<int64_t>(i) * num_heads * kHead);
-        for (int j = 0; j < num_heads * kHead / 8; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      int carry = 0;
-      for (int base = 0; base < num_seqs; base += 32) {
-        const int i = base + lane;
-        const int v = i < num_seqs ? seq[i].x : 0;
-        int incl = v;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int t = __shfl_up_sync(~0u, incl, off);
-          if (lane >= off) incl += t;
-        }
-        if (i < num_seqs) seq[i].x = carry + incl - v;
-        carry += __shfl_sync(~0u, incl, 31);
-      }
-      if (lane == 0) seq[num_seqs] = make_int2(carry, 0);
-    }
-  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(bar(kBarKFull + i), 1);
@@ -372,6 +343,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
+  // Launched as a programmatic dependent of the kernel before it on the
+  // stream (the previous call's merge kernel, say): the set-up above overlaps
+  // that kernel's tail; no global memory is read or written before this wait.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (nb.dense) {
+    // Partition counts per sequence, then their exclusive prefix sum (warp 0).
+    // Sequences with no context get zero outputs here, from CTA 0.
+    for (int i = threadIdx.x; i < num_seqs; i += kThreads) {
+      const int c = context_lens[i];
+      seq[i] = make_int2(partitions_of(c), c);
+      if (c <= 0 && blockIdx.x == 0) {
+        uint4 *o = reinterpret_cast<uint4 *>(out + static_cast<int64_t>(i) * num_heads * kHead);
+        for (int j = 0; j < num_heads * kHead / 8; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int carry = 0;
+      for (int base = 0; base < num_seqs; base += 32) {
+        const int i = base + lane;
+        const int v = i < num_seqs ? seq[i].x : 0;
+        int incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int t = __shfl_up_sync(~0u, incl, off);
+          if (lane >= off) incl += t;
+        }
+        if (i < num_seqs) seq[i].x = carry + incl - v;
+        carry += __shfl_sync(~0u, incl, 31);
+      }
+      if (lane == 0) seq[num_seqs] = make_int2(carry, 0);
+    }
+  }
+  __syncthreads();
   const int n_units = nb.n_units();
   // The merge kernel may be scheduled now: its threads wait (griddepcontrol)
   // until this grid has finished and its writes are visible.
@@ -831,7 +836,9 @@ __global__ void __launch_bounds__(256)
                               const int *__restrict__ context_lens, uint16_t *__restrict__ out,
                               int num_seqs, int num_heads, int max_parts) {
   // Launched as a programmatic dependent of the decode kernel: wait for it to
-  // finish (its workspace writes are then visible).
+  // finish (its workspace writes are then visible).  The next decode call may
+  // be scheduled once every block of this kernel has begun.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -884,10 +891,23 @@ cudaError_t launch_nc(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const vo
   const cudaError_t e = cudaFuncSetAttribute(paged_decode_gqa_tc_kernel<NC>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
   if (e != cudaSuccess) return e;
-  paged_decode_gqa_tc_kernel<NC><<<grid, kThreads, kAlloc, stream>>>(
-      tm_k, tm_v, static_cast<const uint16_t *>(q), block_tables, context_lens,
-      static_cast<uint16_t *>(out), ws_o, ws_ml, sched, num_seqs, num_heads,
-      num_kv_heads, group, gs, max_blocks, max_parts, qscale, dev_status);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(
+        &cfg, paged_decode_gqa_tc_kernel<NC>, tm_k, tm_v, static_cast<const uint16_t *>(q),
+        block_tables, context_lens, static_cast<uint16_t *>(out), ws_o, ws_ml, sched, num_seqs,
+        num_heads, num_kv_heads, group, gs, max_blocks, max_parts, qscale, dev_status);
+    if (e != cudaSuccess) return e;
+  }
   if (max_parts > 1) {
     // Programmatic dependent launch: the merge grid is scheduled while the
     // decode grid runs and starts its work when that grid completes, which
