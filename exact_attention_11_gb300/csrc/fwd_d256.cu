@@ -62,7 +62,9 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + 4 * kBox;
 constexpr int kOffV = kOffK + kKChunks * kBox;
 constexpr int kOffBar = kOffV + kVHalves * kVHalfBytes;
-constexpr int kSmemBytes = kOffBar + 512;
+// Epilogue staging: per softmax warp its 32 rows x 64 columns of output, 4 KB.
+constexpr int kOffStage = kOffBar + 512;
+constexpr int kSmemBytes = kOffStage + 4 * 4096;
 constexpr int kAlloc = kSmemBytes + 1024;     // slack for 1 KB alignment
 static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 
@@ -456,28 +458,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait(bar(kBarPVDone + bl), ((g - 1) >> 1) & 1, abort_flag))) break;
       tc_fence_after();
       const float inv_l = 1.f / l;
-      uint16_t *orow = o + (static_cast<int64_t>(bh) * N + row) * D;
+      // O rows leave through shared memory, 64 columns at a time: each warp
+      // packs its 32 rows into a 4 KB buffer (16-byte chunks swizzled by the
+      // row) and reads it back so that eight lanes store one row's 128
+      // contiguous bytes, four whole lines per store instruction.
+      const int lane = threadIdx.x & 31;
+      uint8_t *stg = smem + kOffStage + quarter * 4096;
+      const int row_w = row - lane;   // this warp's first row
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(o_tmem + c * 32, ov);
-        tmem_wait_ld(ov);
-        if (row < N) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+      for (int h = 0; h < D / 64; ++h) {
+        uint32_t ov[2][32];
+        tmem_ld32(o_tmem + 64 * h, ov[0]);
+        tmem_ld32(o_tmem + 64 * h + 32, ov[1]);
+        tmem_wait_ld(ov[0]);
+        tmem_wait_ld(ov[1]);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 v;
-            v.x = pack2<F16>(__uint_as_float(ov[8 * e + 0]) * inv_l,
-                             __uint_as_float(ov[8 * e + 1]) * inv_l);
-            v.y = pack2<F16>(__uint_as_float(ov[8 * e + 2]) * inv_l,
-                             __uint_as_float(ov[8 * e + 3]) * inv_l);
-            v.z = pack2<F16>(__uint_as_float(ov[8 * e + 4]) * inv_l,
-                             __uint_as_float(ov[8 * e + 5]) * inv_l);
-            v.w = pack2<F16>(__uint_as_float(ov[8 * e + 6]) * inv_l,
-                             __uint_as_float(ov[8 * e + 7]) * inv_l);
-            dst[e] = v;
-          }
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t *c8 = &ov[k >> 2][(k & 3) * 8];
+          uint4 v;
+          v.x = pack2<F16>(__uint_as_float(c8[0]) * inv_l, __uint_as_float(c8[1]) * inv_l);
+          v.y = pack2<F16>(__uint_as_float(c8[2]) * inv_l, __uint_as_float(c8[3]) * inv_l);
+          v.z = pack2<F16>(__uint_as_float(c8[4]) * inv_l, __uint_as_float(c8[5]) * inv_l);
+          v.w = pack2<F16>(__uint_as_float(c8[6]) * inv_l, __uint_as_float(c8[7]) * inv_l);
+          *reinterpret_cast<uint4 *>(stg + lane * 128 + ((k ^ (lane & 7)) * 16)) = v;
         }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int rr = (lane >> 3) + 4 * k, ch = lane & 7;
+          const uint4 v = *reinterpret_cast<const uint4 *>(stg + rr * 128 + ((ch ^ (rr & 7)) * 16));
+          if (row_w + rr < N)
+            *reinterpret_cast<uint4 *>(o + (static_cast<int64_t>(bh) * N + row_w + rr) * D +
+                                       64 * h + ch * 8) = v;
+        }
+        __syncwarp();
       }
       // O has been read: the next item's first P V may overwrite it (it
       // waits for this warpgroup's first P of that item).
