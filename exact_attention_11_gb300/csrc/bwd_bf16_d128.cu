@@ -404,27 +404,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = wait_warp(bar(kBarKVDone), 0, abort_flag);
     if (ok) {
       tc_fence_after();
-      const int64_t off = (static_cast<int64_t>(bh) * N + key) * D;
-      __nv_bfloat16 *dst = (t ? dk : dv) + off;
+      __nv_bfloat16 *base = (t ? dk : dv) + static_cast<int64_t>(bh) * N * D;
       const float mul = t ? scale : 1.f;
       const uint32_t col = t ? 256u + D : 256u;
+      // The rows leave through shared memory (the Q ring is idle now: every
+      // MMA that read it has completed), 64 columns at a time: each warp packs
+      // its 32 rows into 4 KB (16-byte chunks swizzled by the row) and reads
+      // them back so that eight lanes store one row's 128 contiguous bytes.
+      uint8_t *stg = smem + kOffQ + (t * 4 + quarter) * 4096;
+      const int key_w = key - lane;   // this warp's first key row
+#pragma unroll 1
+      for (int h = 0; h < D / 64; ++h) {
+        uint32_t v[2][32];
+        tmem_ld32(tmem + lane_off + col + 64 * h, v[0]);
+        tmem_ld32(tmem + lane_off + col + 64 * h + 32, v[1]);
+        tmem_wait_ld(v[0]);
+        tmem_wait_ld(v[1]);
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + col + ch * 32, v);
-        tmem_wait_ld(v);
-        if (key < N) {
-          uint4 *w = reinterpret_cast<uint4 *>(dst + ch * 32);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 x;
-            x.x = pack_bf16x2(__uint_as_float(v[8 * e + 0]) * mul, __uint_as_float(v[8 * e + 1]) * mul);
-            x.y = pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul);
-            x.z = pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul);
-            x.w = pack_bf16x2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul);
-            w[e] = x;
-          }
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t *c8 = &v[k >> 2][(k & 3) * 8];
+          uint4 x;
+          x.x = pack_bf16x2(__uint_as_float(c8[0]) * mul, __uint_as_float(c8[1]) * mul);
+          x.y = pack_bf16x2(__uint_as_float(c8[2]) * mul, __uint_as_float(c8[3]) * mul);
+          x.z = pack_bf16x2(__uint_as_float(c8[4]) * mul, __uint_as_float(c8[5]) * mul);
+          x.w = pack_bf16x2(__uint_as_float(c8[6]) * mul, __uint_as_float(c8[7]) * mul);
+          *reinterpret_cast<uint4 *>(stg + lane * 128 + ((k ^ (lane & 7)) * 16)) = x;
         }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int rr = (lane >> 3) + 4 * k, ch = lane & 7;
+          const uint4 x = *reinterpret_cast<const uint4 *>(stg + rr * 128 + ((ch ^ (rr & 7)) * 16));
+          if (key_w + rr < N)
+            *reinterpret_cast<uint4 *>(base + static_cast<int64_t>(key_w + rr) * D + 64 * h +
+                                       ch * 8) = x;
+        }
+        __syncwarp();
       }
     }
   }
