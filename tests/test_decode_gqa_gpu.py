@@ -171,3 +171,32 @@ def test_gqa_decode_equals_replicated_one_head_decode():
     gf, mf = g.float(), m.float()
     assert ((gf - mf).abs() <= mf.abs() * 2.0 ** -7 + 1e-6).all()
     assert (gf == mf).float().mean().item() > 0.8
+
+
+def test_gqa_decode_in_cuda_graph():
+    """The tensor-core decode (its dependent launches included) captured in a
+    CUDA graph replays to the eager result, bit for bit."""
+    di = inputs.decode_inputs(8, 32, 128, 16, 2000, seed=61, device=DEV, num_kv_heads=8)
+    fa.fa_decode_gqa_select(2)
+    try:
+        out = torch.empty_like(di.q)
+        fa.paged_decode(di.q, di.k_cache, di.v_cache, di.block_tables, di.context_lens,
+                        di.scale, out=out)          # workspace and cache views set up
+        torch.cuda.synchronize()
+        eager = out.clone()
+        graph = torch.cuda.CUDAGraph()
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                fa.paged_decode(di.q, di.k_cache, di.v_cache, di.block_tables,
+                                di.context_lens, di.scale, out=out)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            out.zero_()
+            graph.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out, eager)
+        assert fa.fa_device_status() == 0
+    finally:
+        fa.fa_decode_gqa_select(0)
