@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(256)
     bwd_prep_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
                     const float *__restrict__ lse, float *__restrict__ vec,
                     float *__restrict__ dq_acc, int N, int n_qb, int64_t padded_rows) {
+  // The main kernel may be scheduled once every block of this one has begun.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t prow = static_cast<int64_t>(blockIdx.x) * 16 + (threadIdx.x >> 4);
   const int part = threadIdx.x & 15;
   const bool live = prow < padded_rows;
@@ -502,6 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256)
     bwd_dq_kernel(const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, int64_t n8,
                   float scale) {
+  // A programmatic dependent of the main kernel: wait for its last additions.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
   if (i >= n8) return;
   const float4 a = reinterpret_cast<const float4 *>(acc)[2 * i];
@@ -550,9 +554,18 @@ cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   }
   if (e != cudaSuccess) return e;
   const int64_t n8 = rows * D / 8;
-  bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
-      dq_acc, reinterpret_cast<__nv_bfloat16 *>(dq), n8, scale);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((n8 + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bwd_dq_kernel, static_cast<const float *>(dq_acc),
+                            reinterpret_cast<__nv_bfloat16 *>(dq), n8, scale);
 }
 
 }  // namespace

@@ -222,6 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
+  // A programmatic dependent of the preparation kernel: its set-up above
+  // overlaps that kernel's tail; no global memory is touched before this wait.
+  // The dQ kernel may be scheduled once every block of this one is past it.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLoad));
@@ -464,10 +469,20 @@ cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_qb = (N + BQ - 1) / BQ;
-  bwd_pipe_kernel<<<n_qb * BH, kThreads, kSmemBytes, stream>>>(
-      tq64, tk, tv, tdo64, vecs, dq_acc, reinterpret_cast<__nv_bfloat16 *>(dk),
-      reinterpret_cast<__nv_bfloat16 *>(dv), N, BH, scale, causal, dev_status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_qb * BH);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bwd_pipe_kernel, tq64, tk, tv, tdo64, vecs, dq_acc,
+                            reinterpret_cast<__nv_bfloat16 *>(dk),
+                            reinterpret_cast<__nv_bfloat16 *>(dv), N, BH, scale, causal,
+                            dev_status);
 }
 
 }  // namespace fattn
