@@ -271,10 +271,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
-  // The masked forward is launched as a programmatic dependent of the mask
-  // summary kernels: its set-up above overlaps their tail, and nothing it
-  // reads from global memory is touched before they have finished.
-  if (MASK) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The bf16 / fp16 forwards are launched as programmatic dependents of the
+  // kernel before them on the stream (the mask summary kernels, or whatever
+  // wrote Q, K and V): their set-up above overlaps that kernel's tail, and
+  // nothing they read or write in global memory is touched before it has
+  // finished.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
@@ -777,29 +779,24 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
   const int grid = static_cast<int>(n_items < g_num_sms[dev] ? n_items : g_num_sms[dev]);
   const float scale_log2 = scale * 1.4426950408889634f;
   const int n_sblk = (N + BM - 1) / BM;
-  if (MASK) {
-    // After the mask summary kernels: a programmatic dependent launch (the
-    // kernel waits for them with griddepcontrol.wait after its set-up).
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::kAlloc;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fwd_bf16_tc_kernel<D, F16, MASK, FP8>, tq, tk, tv,
-                              reinterpret_cast<uint16_t *>(o), lse, N, BH, n_qblocks, scale_log2,
-                              causal, sched, dev_status, fault_cta, mask, mask_bh_stride, q_scale,
-                              k_scale, v_scale, n_sblk, mask_ranges, mask_flags);
-  }
-  fwd_bf16_tc_kernel<D, F16, MASK, FP8><<<grid, kThreads, C::kAlloc, stream>>>(
-      tq, tk, tv, reinterpret_cast<uint16_t *>(o), lse, N, BH, n_qblocks, scale_log2, causal,
-      sched, dev_status, fault_cta, mask, mask_bh_stride, q_scale, k_scale, v_scale, n_sblk,
-      mask_ranges, mask_flags);
-  return cudaGetLastError();
+  // A programmatic dependent launch: the kernel waits with
+  // griddepcontrol.wait after its set-up for the work before it (the wait is
+  // a no-op in an ordinary launch).  The FP8 forward is launched the ordinary
+  // way: after the quantization kernels the dependent launch measured slower.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = FP8 ? 0 : 1;
+  return cudaLaunchKernelEx(&cfg, fwd_bf16_tc_kernel<D, F16, MASK, FP8>, tq, tk, tv,
+                            reinterpret_cast<uint16_t *>(o), lse, N, BH, n_qblocks, scale_log2,
+                            causal, sched, dev_status, fault_cta, mask, mask_bh_stride, q_scale,
+                            k_scale, v_scale, n_sblk, mask_ranges, mask_flags);
 }
 
 }  // namespace

@@ -181,6 +181,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
+  // Launched as a programmatic dependent of the kernel before it: the set-up
+  // above overlaps that kernel's tail; global memory is touched only after it.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // Reads item slot k once it is published (every consumer but the MMA
   // thread frees its share right away; the MMA thread frees it after the
@@ -539,10 +542,20 @@ cudaError_t launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorM
   if (e != cudaSuccess) return e;
   const long long n_items = static_cast<long long>((N + BM - 1) / BM) * BH;
   const int grid = static_cast<int>(n_items < g_num_sms[dev] ? n_items : g_num_sms[dev]);
-  fwd_d256_kernel<F16><<<grid, kThreads, kAlloc, stream>>>(
-      tq, tk, tv, static_cast<uint16_t *>(o), lse, N, BH, scale * 1.4426950408889634f, causal,
-      sched, dev_status);
-  return cudaGetLastError();
+  // A programmatic dependent launch: the kernel waits with
+  // griddepcontrol.wait after its set-up for the work before it.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fwd_d256_kernel<F16>, tq, tk, tv, static_cast<uint16_t *>(o),
+                            lse, N, BH, scale * 1.4426950408889634f, causal, sched, dev_status);
 }
 
 }  // namespace
