@@ -28,8 +28,10 @@ __device__ __forceinline__ bool all_bytes_nonzero(uint32_t x) {
   return ((x - 0x01010101u) & ~x & 0x80808080u) == 0u;
 }
 
-// grid (n_t, n_t, mask heads), 256 threads: one 128 x 128 block each.
-__global__ void __launch_bounds__(256)
+constexpr int kFlagThreads = 256;
+
+// grid (n_t, n_t, mask heads), kFlagThreads threads: one 128 x 128 block each.
+__global__ void __launch_bounds__(kFlagThreads)
     mask_tile_flags_kernel(const uint8_t *__restrict__ mask, int64_t bh_stride, int N, int n_t,
                            uint8_t *__restrict__ flags) {
   // The ranges kernel may be scheduled once every block of this one has begun.
@@ -37,15 +39,27 @@ __global__ void __launch_bounds__(256)
   const int kt = blockIdx.x, qt = blockIdx.y, mh = blockIdx.z;
   const uint8_t *base = mask + static_cast<int64_t>(mh) * bh_stride;
   int any = 0, all = 1;
-  // 128 rows x 8 chunks of 16 bytes; N is a multiple of 16, so a chunk lies
+  // 128 rows x 8 chunks of 16 bytes, four chunks a thread, all four loads
+  // issued before the first is used; N is a multiple of 16, so a chunk lies
   // wholly inside or wholly outside the sequence.
-  for (int i = threadIdx.x; i < kT * 8; i += blockDim.x) {
+  constexpr int kPer = kT * 8 / kFlagThreads;
+  uint4 v[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = threadIdx.x + u * kFlagThreads;
+    const int r = qt * kT + (i >> 3), c0 = kt * kT + (i & 7) * 16;
+    v[u] = (r < N && c0 < N)
+               ? __ldg(reinterpret_cast<const uint4 *>(base + static_cast<int64_t>(r) * N + c0))
+               : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = threadIdx.x + u * kFlagThreads;
     const int r = qt * kT + (i >> 3), c0 = kt * kT + (i & 7) * 16;
     if (r < N && c0 < N) {
-      const uint4 v = *reinterpret_cast<const uint4 *>(base + static_cast<int64_t>(r) * N + c0);
-      any |= (v.x | v.y | v.z | v.w) != 0u;
-      all &= all_bytes_nonzero(v.x) && all_bytes_nonzero(v.y) && all_bytes_nonzero(v.z) &&
-             all_bytes_nonzero(v.w);
+      any |= (v[u].x | v[u].y | v[u].z | v[u].w) != 0u;
+      all &= all_bytes_nonzero(v[u].x) && all_bytes_nonzero(v[u].y) &&
+             all_bytes_nonzero(v[u].z) && all_bytes_nonzero(v[u].w);
     }
   }
   any = __syncthreads_or(any);
@@ -105,8 +119,8 @@ cudaError_t launch_mask_summary(const uint8_t *mask, int64_t bh_stride, int N, i
   const size_t flag_bytes = (static_cast<size_t>(mask_heads) * n_t * n_t + 15) / 16 * 16;
   uint8_t *f = static_cast<uint8_t *>(ws);
   int2 *r = reinterpret_cast<int2 *>(f + flag_bytes);
-  mask_tile_flags_kernel<<<dim3(n_t, n_t, mask_heads), 256, 0, stream>>>(mask, bh_stride, N, n_t,
-                                                                          f);
+  mask_tile_flags_kernel<<<dim3(n_t, n_t, mask_heads), kFlagThreads, 0, stream>>>(
+      mask, bh_stride, N, n_t, f);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
