@@ -35,6 +35,8 @@ constexpr int kD = 128;
 constexpr int kRows = 128;          // rows per quantization block
 constexpr int kThreads = 256;       // 8 warps x 16 rows
 constexpr int kRowsPerWarp = kRows / (kThreads / 32);
+static_assert(kThreads == 256 && kD == 128 && kRows == 128,
+              "the V^T store pattern covers 128 rows with 8 warps x 4 passes");
 
 // One butterfly stage across lanes: the lane whose `mask` bit is clear keeps
 // a + b, its partner a - b (a the lower-index value, b the higher).
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(kThreads)
                        int n_pad, int *__restrict__ dev_status) {
   constexpr int kPitch = kRows + 1;   // bytes per transposed row in shared memory
   extern __shared__ __align__(128) uint8_t stage[];   // 128 rows x 256 bytes
-  __shared__ uint8_t tile[kD * kPitch];
+  __shared__ __align__(16) uint8_t tile[kD * kPitch];
   __shared__ float red[kThreads / 32];
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -229,18 +231,30 @@ __global__ void __launch_bounds__(kThreads)
     for (int e = 0; e < 4; ++e) tile[(4 * lane + e) * kPitch + rl] = (c >> (8 * e)) & 0xffu;
   }
   __syncthreads();
-  // Row c of V^T: keys blk*128 .. +127, as 32 words; words past Npad are
-  // not written (Npad is a multiple of 16, so a word never straddles it).
+  // Row c of V^T, keys blk*128 .. +127: lane l of warp w stores the 16 keys
+  // of chunk l & 7 of row c = 16 w + i + 4 (l >> 3) in pass i, gathered from
+  // the byte tile by five aligned word loads and funnel shifts.  Byte 129 c +
+  // 16 k lies in word 32 c + 4 k + c / 4 at byte c & 3 = i, so the warp's 32
+  // loads of a pass fall in 32 different banks and its stores fill four whole
+  // 128-byte rows.  Chunks at or past Npad are not written (Npad is a
+  // multiple of 16, so a chunk never straddles it).
   uint8_t *out = vt8 + static_cast<int64_t>(bh) * kD * n_pad;
-  for (int w = threadIdx.x; w < kD * 32; w += kThreads) {
-    const int c = w >> 5, kw = w & 31;
-    const int key = blk * kRows + 4 * kw;
-    if (key >= n_pad) continue;
-    const uint8_t *t = tile + c * kPitch + 4 * kw;
-    const uint32_t word = static_cast<uint32_t>(t[0]) | (static_cast<uint32_t>(t[1]) << 8) |
-                          (static_cast<uint32_t>(t[2]) << 16) |
-                          (static_cast<uint32_t>(t[3]) << 24);
-    *reinterpret_cast<uint32_t *>(out + static_cast<int64_t>(c) * n_pad + key) = word;
+  const int chunk = lane & 7;
+  const int key = blk * kRows + 16 * chunk;
+  if (key < n_pad) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = 16 * warp + i + 4 * (lane >> 3);
+      const uint32_t *wp =
+          reinterpret_cast<const uint32_t *>(tile + ((c * kPitch + 16 * chunk) & ~3));
+      uint32_t w[5];
+#pragma unroll
+      for (int j = 0; j < 5; ++j) w[j] = wp[j];
+      const uint32_t sh = 8u * static_cast<uint32_t>(i);
+      const uint4 o = make_uint4(__funnelshift_r(w[0], w[1], sh), __funnelshift_r(w[1], w[2], sh),
+                                 __funnelshift_r(w[2], w[3], sh), __funnelshift_r(w[3], w[4], sh));
+      *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(c) * n_pad + key) = o;
+    }
   }
   if (blk == 0 && threadIdx.x == 0) v_scale[bh] = s;
 }
