@@ -843,10 +843,49 @@ __global__ void __launch_bounds__(256)
   const int lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (row >= static_cast<long long>(num_seqs) * num_heads) return;
-  const int n_parts = partitions_of(context_lens[row / num_heads]);
-  if (n_parts <= 1) return;   // written by the decode kernel
   const float *ml = ws_ml + row * max_parts * 2;
   const float *o = ws_o + row * max_parts * kHead + 4 * lane;
+  // The first kSpec partitions' (max, sum) pairs and output slices are loaded
+  // together with the context length (one round trip to memory instead of
+  // three); those past the row's partition count are loaded but not used.
+  constexpr int kSpec = 4;
+  float2 ml_s[kSpec];
+  float4 o_s[kSpec];
+  const int ctx = context_lens[row / num_heads];
+#pragma unroll
+  for (int p = 0; p < kSpec; ++p) {
+    if (p < max_parts) {
+      ml_s[p] = __ldcg(reinterpret_cast<const float2 *>(ml) + p);
+      o_s[p] = __ldcg(reinterpret_cast<const float4 *>(o + static_cast<int64_t>(p) * kHead));
+    }
+  }
+  const int n_parts = partitions_of(ctx);
+  if (n_parts <= 1) return;   // written by the decode kernel
+  if (n_parts <= kSpec) {
+    float M = ml_s[0].x;
+#pragma unroll
+    for (int p = 1; p < kSpec; ++p)
+      if (p < n_parts) M = fmaxf(M, ml_s[p].x);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int p = 0; p < kSpec; ++p) {
+      if (p < n_parts) {
+        const float f = ex2_approx(ml_s[p].x - M);
+        L += ml_s[p].y * f;
+        acc.x += f * o_s[p].x;
+        acc.y += f * o_s[p].y;
+        acc.z += f * o_s[p].z;
+        acc.w += f * o_s[p].w;
+      }
+    }
+    const float inv = 1.f / L;
+    uint2 packed;
+    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2 *>(out + row * kHead + 4 * lane) = packed;
+    return;
+  }
   float M = -INFINITY;
   for (int p = lane; p < n_parts; p += 32) M = fmaxf(M, __ldcg(ml + 2 * p));
 #pragma unroll
