@@ -79,6 +79,15 @@ def test_gqa_decode_tile_boundaries(impl):
     _check(di, ctx=ctx)
 
 
+def test_gqa_decode_many_partitions(impl):
+    """Contexts of up to four 1024-token partitions of the tensor-core kernel
+    (merged from registers loaded in one round trip) and of five to nine
+    (merged by the general loop), at and next to the four-partition edge."""
+    ctx = [3072, 4095, 4096, 4097, 5121, 9000]
+    di = inputs.decode_inputs(len(ctx), 8, 128, 16, 9000, seed=31, device=DEV, num_kv_heads=2)
+    _check(di, ctx=ctx)
+
+
 def test_gqa_decode_ignores_cache_slots_past_the_context(impl):
     """Slots past a sequence's context (the tail of its last block, and blocks
     it does not use) may hold anything: NaN there changes no output bit."""
