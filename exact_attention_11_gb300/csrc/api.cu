@@ -25,9 +25,10 @@ struct DeviceState {
   float *decode_ws = nullptr;     // split-K partials
   size_t decode_ws_bytes = 0;
   int *decode_counters = nullptr; // one int per (sequence, head), kept at zero
-  size_t decode_counter_count = 0;
-  int *fwd_sched = nullptr;       // kFwdSchedSlots pairs of forward work counters, kept at zero
-  unsigned fwd_sched_next = 0;    // slot for the next forward launch
+  size_t decode_counter_bytes = 0;
+  int *fwd_sched = nullptr;       // 2 * kFwdSchedSlots pairs of work counters, kept at zero
+  unsigned fwd_sched_next = 0;    // slot for the next eager launch
+  unsigned fwd_sched_next_captured = 0;  // slot for the next launch captured into a graph
   void *mask_ws = nullptr;        // tile summary of the last mask (fa_forward_masked)
   size_t mask_ws_bytes = 0;
   CUtensorMap kv_map_k, kv_map_v; // last TMA views of paged caches (grouped decode)
@@ -69,7 +70,7 @@ int current_device(int *dev_out) {
     if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
   }
   if (st.fwd_sched == nullptr) {
-    const size_t bytes = sizeof(int) * 2 * fattn::kFwdSchedSlots;
+    const size_t bytes = sizeof(int) * 2 * 2 * fattn::kFwdSchedSlots;
     if (cudaMalloc(&st.fwd_sched, bytes) != cudaSuccess) return FA_ERR_NO_MEMORY;
     if (cudaMemset(st.fwd_sched, 0, bytes) != cudaSuccess) return FA_ERR_CUDA;
   }
@@ -184,13 +185,44 @@ int check_forward_args(const void *q, const void *k, const void *v, const void *
   return FA_OK;
 }
 
+// Grows a library-owned buffer to at least `bytes`, in stream order on `s`:
+// the old buffer is released with cudaFreeAsync and the new one taken with
+// cudaMallocAsync, so growing never synchronises the device.  Earlier calls
+// that used the old buffer are ordered before this one (the header's rule for
+// calls that share library state), so the release cannot overtake them.
+// During stream capture nothing may be allocated: a buffer that is too small
+// then gives FA_ERR_UNSUPPORTED.  With `zero`, the new buffer is cleared on
+// `s`.
+int grow_on_stream(void **buf, size_t *have, size_t bytes, cudaStream_t s, bool zero) {
+  if (*have >= bytes) return FA_OK;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    cudaGetLastError();  // the legacy stream while another stream captures: consume the error
+    return FA_ERR_UNSUPPORTED;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return FA_ERR_UNSUPPORTED;
+  if (*buf != nullptr && cudaFreeAsync(*buf, s) != cudaSuccess) return FA_ERR_CUDA;
+  *buf = nullptr;
+  *have = 0;
+  void *p = nullptr;
+  if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) return FA_ERR_NO_MEMORY;
+  if (zero && cudaMemsetAsync(p, 0, bytes, s) != cudaSuccess) {
+    cudaFreeAsync(p, s);
+    return FA_ERR_CUDA;
+  }
+  *buf = p;
+  *have = bytes;
+  return FA_OK;
+}
+
 // Checks shared by the decode entry points; grows the library-owned split-K
-// workspace and counters for (num_seqs, num_heads, max_num_blocks_per_seq).
+// workspace and counters for (num_seqs, num_heads, max_num_blocks_per_seq)
+// on the call's stream.
 int decode_prepare(const void *q, const void *k_cache, const void *v_cache,
                    const int *block_tables, const int *context_lens, const void *out,
                    int num_seqs, int num_heads, int head_size, int block_size,
-                   int max_num_blocks_per_seq, float scale, float **ws, int **counters,
-                   int **status) {
+                   int max_num_blocks_per_seq, float scale, cudaStream_t stream, float **ws,
+                   int **counters, int **status) {
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
     return FA_ERR_INVALID_ARG;
   if (num_seqs < 0 || num_heads <= 0 || max_num_blocks_per_seq <= 0) return FA_ERR_INVALID_ARG;
@@ -208,23 +240,13 @@ int decode_prepare(const void *q, const void *k_cache, const void *v_cache,
   int dev = 0, rc;
   if ((rc = current_device(&dev)) != FA_OK) return rc;
   DeviceState &st = g_dev[dev];
-  if (st.decode_ws_bytes < ws_bytes) {
-    if (st.decode_ws) cudaFree(st.decode_ws);  // synchronises: no launch still uses it
-    st.decode_ws = nullptr;
-    st.decode_ws_bytes = 0;
-    if (cudaMalloc(&st.decode_ws, ws_bytes) != cudaSuccess) return FA_ERR_NO_MEMORY;
-    st.decode_ws_bytes = ws_bytes;
-  }
-  if (st.decode_counter_count < n_counters) {
-    if (st.decode_counters) cudaFree(st.decode_counters);
-    st.decode_counters = nullptr;
-    st.decode_counter_count = 0;
-    if (cudaMalloc(&st.decode_counters, n_counters * sizeof(int)) != cudaSuccess)
-      return FA_ERR_NO_MEMORY;
-    if (cudaMemset(st.decode_counters, 0, n_counters * sizeof(int)) != cudaSuccess)
-      return FA_ERR_CUDA;
-    st.decode_counter_count = n_counters;
-  }
+  if ((rc = grow_on_stream(reinterpret_cast<void **>(&st.decode_ws), &st.decode_ws_bytes,
+                           ws_bytes, stream, false)) != FA_OK)
+    return rc;
+  if ((rc = grow_on_stream(reinterpret_cast<void **>(&st.decode_counters),
+                           &st.decode_counter_bytes, n_counters * sizeof(int), stream, true)) !=
+      FA_OK)
+    return rc;
   *ws = st.decode_ws;
   *counters = st.decode_counters;
   *status = st.status;
@@ -232,6 +254,25 @@ int decode_prepare(const void *q, const void *k_cache, const void *v_cache,
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+// The work-counter pair of a persistent-kernel launch.  Eager launches take
+// the first kFwdSchedSlots pairs round robin, so concurrent calls share one
+// only with the 64th call after them.  A launch captured into a CUDA graph
+// keeps its pair for every replay: it takes one of the other kFwdSchedSlots
+// pairs, never handed to an eager launch, shared only with the 64th captured
+// launch after it.  (A graph must not run concurrently with itself.)
+int *sched_slot(DeviceState &st, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  bool captured = false;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess)
+    cudaGetLastError();  // the legacy stream while another stream captures: not captured
+  else
+    captured = cs != cudaStreamCaptureStatusNone;
+  const unsigned slot = captured
+                            ? fattn::kFwdSchedSlots + st.fwd_sched_next_captured++ % fattn::kFwdSchedSlots
+                            : st.fwd_sched_next++ % fattn::kFwdSchedSlots;
+  return st.fwd_sched + 2 * slot;
+}
 
 }  // namespace
 
@@ -274,18 +315,14 @@ int forward16(const void *q, const void *k, const void *v, void *o, float *lse, 
     if ((rc = current_device(&dev)) != FA_OK) return rc;
     if ((rc = get_encoder()) != FA_OK) return rc;
     DeviceState &st = g_dev[dev];
-    sched = st.fwd_sched + 2 * (st.fwd_sched_next++ % fattn::kFwdSchedSlots);
+    sched = sched_slot(st, reinterpret_cast<cudaStream_t>(stream));
     fault_cta = st.inject_fault ? 0 : -1;
     st.inject_fault = 0;
     if (mask != nullptr) {
       const size_t need = fattn::mask_summary_bytes(mask_heads, N);
-      if (st.mask_ws_bytes < need) {
-        if (st.mask_ws) cudaFree(st.mask_ws);  // synchronises: no launch still uses it
-        st.mask_ws = nullptr;
-        st.mask_ws_bytes = 0;
-        if (cudaMalloc(&st.mask_ws, need) != cudaSuccess) return FA_ERR_NO_MEMORY;
-        st.mask_ws_bytes = need;
-      }
+      if ((rc = grow_on_stream(&st.mask_ws, &st.mask_ws_bytes, need,
+                               reinterpret_cast<cudaStream_t>(stream), false)) != FA_OK)
+        return rc;
       mask_ws = st.mask_ws;
     }
   }
@@ -405,7 +442,7 @@ int fa_forward_fp8(const void *q8, const void *k8, const void *vt8, const float 
     if ((rc = current_device(&dev)) != FA_OK) return rc;
     if ((rc = get_encoder()) != FA_OK) return rc;
     DeviceState &st = g_dev[dev];
-    sched = st.fwd_sched + 2 * (st.fwd_sched_next++ % fattn::kFwdSchedSlots);
+    sched = sched_slot(st, reinterpret_cast<cudaStream_t>(stream));
   }
   if ((rc = encode_e4m3_map(&tq, q8, BH, N, d)) != FA_OK) return rc;
   if ((rc = encode_e4m3_map(&tk, k8, BH, N, d)) != FA_OK) return rc;
@@ -466,7 +503,7 @@ int fa_paged_decode(const void *q, const void *k_cache, const void *v_cache,
   int *counters = nullptr, *status = nullptr;
   const int rc = decode_prepare(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs,
                                 num_heads, head_size, block_size, max_num_blocks_per_seq, scale,
-                                &ws, &counters, &status);
+                                reinterpret_cast<cudaStream_t>(stream), &ws, &counters, &status);
   if (rc != FA_OK || num_seqs == 0) return rc;
   return cuda_status(fattn::launch_paged_decode(q, k_cache, v_cache, block_tables, context_lens,
                                                 out, num_seqs, num_heads, max_num_blocks_per_seq,
@@ -497,7 +534,7 @@ int fa_paged_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
   int *counters = nullptr, *status = nullptr;
   const int rc = decode_prepare(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs,
                                 num_heads, head_size, block_size, max_num_blocks_per_seq, scale,
-                                &ws, &counters, &status);
+                                reinterpret_cast<cudaStream_t>(stream), &ws, &counters, &status);
   if (rc != FA_OK || num_seqs == 0) return rc;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (group == 1)
@@ -515,7 +552,7 @@ int fa_paged_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
       if ((rc2 = current_device(&dev)) != FA_OK) return rc2;
       if ((rc2 = get_encoder()) != FA_OK) return rc2;
       DeviceState &st = g_dev[dev];
-      sched = st.fwd_sched + 2 * (st.fwd_sched_next++ % fattn::kFwdSchedSlots);
+      sched = sched_slot(st, reinterpret_cast<cudaStream_t>(stream));
       if (!(st.kv_maps_valid && st.kv_maps_k == k_cache && st.kv_maps_v == v_cache &&
             st.kv_maps_hk == num_kv_heads)) {
         st.kv_maps_valid = false;
@@ -572,6 +609,9 @@ void fa_release(void) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
   DeviceState &st = g_dev[dev];
+  // The buffers grown in stream order may still be in use by work the caller
+  // has not waited for; cudaFree does not order itself after it.
+  cudaDeviceSynchronize();
   if (st.decode_ws) cudaFree(st.decode_ws);
   if (st.decode_counters) cudaFree(st.decode_counters);
   if (st.status) cudaFree(st.status);

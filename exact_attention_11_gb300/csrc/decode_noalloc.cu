@@ -25,14 +25,17 @@
 //    calls whose work overlaps on the GPU (different streams, no ordering
 //    between them) race on the array and may return wrong results; order
 //    them on one stream or with events.
-//  * The first call on a device looks up the array's device address with
-//    cudaGetSymbolAddress (this may load the library's module on that
-//    device).  Make that first call before any stream capture begins.
+//  * Every call looks up the array's device address on the current device
+//    with cudaGetSymbolAddress.  The first lookup on a device may load the
+//    library's module there, so make the first call on each device before
+//    any stream capture begins.  Looking the address up on every call (it is
+//    cheap once the module is loaded) keeps it right after a context
+//    teardown such as cudaDeviceReset, which may reload the module at
+//    another address.
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "fattn.h"
 #include "kernels.h"
@@ -46,22 +49,16 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 namespace {
 
-std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-
 size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 
-// Device address of g_decode_scratch on device `dev` (which must be current),
-// looked up once per device.
-int scratch_address(int dev, void **out) {
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
-      return FA_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+// Device address of g_decode_scratch on the current device.  Host code only
+// holds a host-side stand-in under the array's name; the device address
+// must come from the runtime.
+int scratch_address(void **out) {
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
+    return FA_ERR_CUDA;
+  *out = p;
   return FA_OK;
 }
 
@@ -97,7 +94,7 @@ extern "C" int fa_paged_decode_noalloc(const void *q, const void *k_cache, const
       major != 10 || minor != 3)
     return FA_ERR_NO_DEVICE;
   void *base = nullptr;
-  const int rc = scratch_address(dev, &base);
+  const int rc = scratch_address(&base);
   if (rc != FA_OK) return rc;
 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -19,11 +19,24 @@
  *    fa_device_status() reads.
  *  - NaN or Inf inputs are not checked for; they propagate per IEEE rules.
  *
- * The library owns only small per-device state (the split-K workspace of the
- * paged decode, its counters, cached launch attributes and the last TMA views
- * of a paged cache); fa_release() frees it.  Calls on one device from several host threads are safe; calls
- * whose work overlaps on the GPU may share that workspace only if they are
- * ordered on one stream.
+ * The library owns only small per-device state: the split-K workspace of the
+ * paged decodes and its counters, the block summary of the last boolean mask,
+ * the work counters of the persistent kernels and the last TMA views of a
+ * paged cache; fa_release() frees it.  Calls on one device from several host
+ * threads are safe.  The decode workspace and the mask summary are one
+ * buffer per device: calls that use the same one (fa_paged_decode and
+ * fa_paged_decode_gqa with each other; fa_forward_masked with itself) must
+ * not overlap on the GPU -- issue them on one stream, or make the later
+ * call's stream wait for an event recorded after the earlier call.  These
+ * buffers grow in stream order on the calling stream (cudaMallocAsync and
+ * cudaFreeAsync), so a larger problem never synchronises the device; a call
+ * being captured into a CUDA graph cannot grow them and returns
+ * FA_ERR_UNSUPPORTED instead, so run one call of the largest size before
+ * capturing.  The forward kernels and the tensor-core grouped decode take a
+ * pair of work counters per launch: eager launches rotate through 64 pairs,
+ * launches captured into a graph through 64 others that a graph keeps for
+ * every replay; so at most 64 eager calls may be in flight on a device at
+ * once, and a graph must not run concurrently with itself.
  */
 #ifndef FATTN_H_
 #define FATTN_H_
@@ -99,8 +112,9 @@ int fa_forward_f16(const void *q, const void *k, const void *v, void *o, float *
  * lse = -inf.  Each call first summarises the mask per 128 x 128 block (one
  * read of the mask): key tiles that none of a query block's rows can see are
  * skipped, and fully visible blocks are not read again.  The summary lives
- * in a library-owned buffer grown on demand (calls that overlap on the GPU
- * must not share a device).  d is 64 or 128.  Other arguments, layouts and errors as for
+ * in a library-owned buffer grown on demand in stream order; two masked
+ * calls must not overlap on the GPU (order them on one stream or with an
+ * event).  d is 64 or 128.  Other arguments, layouts and errors as for
  * fa_forward (bf16).
  */
 int fa_forward_masked(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -244,9 +258,13 @@ int fa_backward(const void *q, const void *k, const void *v, const void *o,
  * num_kv_heads equals num_heads.  Long contexts are split into partitions
  * of 512 tokens whose partial (max, sum, output) triples are merged with the
  * output update of eq. (4) of the "Flash Attention" page; the partials live
- * in a workspace the library owns and grows on first use for a given size
- * (cudaMalloc; growing it first frees the smaller one, which synchronises
- * the device).  num_seqs == 0 is a no-op.
+ * in a workspace the library owns and grows, in stream order on `stream`,
+ * the first time a problem needs more (cudaFreeAsync of the smaller buffer,
+ * then cudaMallocAsync; the device is not synchronised).  That workspace is
+ * one per device and is shared with fa_paged_decode_gqa: two decode calls
+ * whose work could overlap on the GPU return wrong results; order them on
+ * one stream, or make the second call's stream wait on an event recorded
+ * after the first.  num_seqs == 0 is a no-op.
  */
 int fa_paged_decode(const void *q, const void *k_cache, const void *v_cache,
                     const int *block_tables, const int *context_lens, void *out,
@@ -275,7 +293,8 @@ int fa_paged_decode(const void *q, const void *k_cache, const void *v_cache,
  * default sizes 1 to 16 and every multiple of 4 are taken; see
  * fa_decode_gqa_select.
  * Group size 1 is exactly fa_paged_decode.  Shares fa_paged_decode's
- * library-owned workspace.
+ * library-owned workspace, with the same ordering rule: decode calls must
+ * not overlap on the GPU.
  */
 int fa_paged_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
                         const int *block_tables, const int *context_lens, void *out,
@@ -327,9 +346,10 @@ int fa_decode_gqa_select(int impl);
  *    place; the counters that must start at zero are cleared on `stream` at
  *    the start of each call.  Calls whose work overlaps on the GPU race on
  *    the array: order them on one stream or with events.
- *  - The first call on a device looks up the array's address
- *    (cudaGetSymbolAddress) and may load the library's module there; make
- *    that first call before any stream capture begins.
+ *  - Each call looks up the array's device address with
+ *    cudaGetSymbolAddress on the current device.  The first lookup on a
+ *    device may load the library's module there, so make the first call on
+ *    each device before any stream capture begins.
  */
 int fa_paged_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
                             const int *block_tables, const int *context_lens, void *out,
@@ -359,8 +379,9 @@ const char *fa_status_string(int status);
  */
 int fa_device_status(void);
 
-/* Frees the library-owned per-device state on the current device.  The
- * caller must ensure no enqueued libfattn work is still running. */
+/* Frees the library-owned per-device state on the current device, after
+ * synchronising the device.  No libfattn call may be enqueued or captured
+ * concurrently with it. */
 void fa_release(void);
 
 /* Library version as major*10000 + minor*100 + patch. */

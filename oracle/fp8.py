@@ -14,8 +14,9 @@ youngju.dev, section 9.2, item 3, FP8 low-precision support) names two steps:
   matrix before quantization, which spreads outlier values over all
   coordinates.
 
-Readings taken where the page is silent (each one is how the CUDA path works
-too, so that the quantized codes can be compared bit for bit):
+Readings taken where the page is silent.  The quantization readings fix the
+codes and scales, which are compared bit for bit; the bound on the forward's
+result follows from the E4M3 format alone:
 
 * the format is E4M3 (sign, 4 exponent bits with bias 7, 3 mantissa bits, no
   infinities; normal values 2^-6 .. 448, subnormals k * 2^-9);
@@ -33,8 +34,16 @@ too, so that the quantized codes can be compared bit for bit):
   factor, fp32(1/sqrt(d)), multiplies the block's scale instead (an fp32
   product), so that codes times scales stand for the rows of Q M and K M;
 * the FP8 path aims at exact attention on the dequantized inputs (codes times
-  scales).  Its kernel also rounds the softmax weights to E4M3 before P V;
-  `forward_fp8_reference` turns that into an error bound per output element.
+  scales), with the softmax weights P V multiplies also held in FP8.  The
+  plainest reading is that each weight p in [0, 1] (relative to its row's
+  maximum) is replaced by an E4M3 value.  The format alone then bounds the
+  change of a weight: at or above the smallest normal 2^-6 the three mantissa
+  bits give a relative error <= 2^-4; below it the subnormal step 2^-9 gives
+  an absolute error <= 2^-10.  An implementation that rounds p * 2^e for some
+  0 <= e <= 8 (any such scaling keeps the largest weight below 448) and
+  divides by 2^e again only shrinks the absolute part, so the bound holds for
+  every such choice.  `forward_fp8_reference` turns it into a bound per output
+  element.
 """
 from __future__ import annotations
 
@@ -139,29 +148,28 @@ def dequantized(q, k, v, signs=None):
     return dequantize_rows(qc, qs), dequantize_rows(kc, ks), vc * vs[:, :, None, None].astype(np.float64)
 
 
-# Rounding of the softmax weights in the kernel: each weight p <= 1 (relative
-# to the row max) is carried as E4M3 of p * 2^e with 0 <= e <= 8 chosen so
-# that the largest possible value stays below 448; a weight at or above
-# 2^-6 / 2^e keeps 3 mantissa bits (relative error <= 2^-4), smaller ones an
-# absolute error <= 2^-10 / 2^e <= 2^-10, which in units of the row max is at
-# most 2^-14 once e >= 4.
+# Change of one softmax weight p in [0, 1] when it is held as an E4M3 value,
+# from the format alone: relative 2^-4 (half the step of 3 mantissa bits) for
+# normal values, absolute 2^-10 (half the subnormal step 2^-9) below 2^-6.
 P_REL = 2.0 ** -4
-P_ABS = 2.0 ** -14
+P_ABS = 2.0 ** -10
 OUT_REL = 2.0 ** -8      # bf16 output: half an ulp is 2^-9 relative; doubled
 
 
-def forward_fp8_reference(q, k, v, scale: float, causal: bool, signs=None, rows=None):
+def forward_fp8_reference(q, k, v, scale: float, causal: bool, signs=None, rows=None,
+                          p_rel: float = P_REL, p_abs: float = P_ABS):
     """(O, LSE, bound, sigma) for the FP8 forward.
 
     O and LSE are exact attention (float64) on the dequantized inputs.  For each
     output element, ``bound`` is
-        sum_j max(P_REL p_j, P_ABS) |v_j| / l + OUT_REL |O|  (+ 1e-5),
+        sum_j max(p_rel p_j, p_abs) |v_j| / l + OUT_REL |O|  (+ 1e-5),
     with p_j = exp(s_j - max_j s_j) and l = sum_j p_j: what E4M3 weights and a
-    bf16 output can move the result at most.  ``sigma`` is the standard
-    deviation of that error if each weight's rounding error is an independent,
-    zero-mean value no larger than the bound allows (uniform: bound / sqrt 3),
-    for a statistical check of the typical error.  ``rows`` restricts all four
-    to the given query rows."""
+    bf16 output can move the result at most (by default the format's own
+    limits, P_REL and P_ABS).  ``sigma`` is the standard deviation of that
+    error if each weight's rounding error is an independent, zero-mean value
+    no larger than the bound allows (uniform: bound / sqrt 3), for a
+    statistical check of the typical error.  ``rows`` restricts all four to
+    the given query rows."""
     qd, kd, vd = dequantized(q, k, v, signs)
     B, H, N, d = qd.shape
     rows = np.arange(N) if rows is None else np.asarray(rows)
@@ -176,7 +184,7 @@ def forward_fp8_reference(q, k, v, scale: float, causal: bool, signs=None, rows=
                 s = np.where(key[None, :] <= rows[:, None], s, -np.inf)
             p = np.exp(s - s.max(axis=1, keepdims=True))
             l = p.sum(axis=1, keepdims=True)
-            w = np.where(np.isfinite(s), np.maximum(P_REL * p, P_ABS), 0.0)
+            w = np.where(np.isfinite(s), np.maximum(p_rel * p, p_abs), 0.0)
             bound[b, h] = (w @ np.abs(vd[b, h])) / l
             var[b, h] = ((w * w / 3.0) @ (vd[b, h] ** 2)) / (l * l)
     bound += OUT_REL * np.abs(o) + 1e-5

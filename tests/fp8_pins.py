@@ -12,8 +12,9 @@ it with a plausible mistake planted in them.  The facts used:
   diag(sigma) H / sqrt(d);
 * closed-form properties of per-block scaling (the largest value of a block
   maps to +-448, every value is reproduced within half an E4M3 step);
-* the error of E4M3 softmax weights, simulated directly, against the bound the
-  oracle reports;
+* the error of E4M3 softmax weights, simulated directly (with and without a
+  power-of-two scaling of the weights), against the bound the oracle reports,
+  whose constants are the E4M3 format's own rounding limits;
 * the claim of "FlashAttention: GPU 메모리 계층을 활용한 어텐션 최적화 분석"
   (youngju.dev, section 9.2, item 3) that the random orthogonal transform
   lowers the FP8 error when the inputs have outliers.
@@ -143,28 +144,59 @@ def check_rotation_is_orthogonal_transform(f):
     assert np.all(np.abs(vc).reshape(B, H, -1).max(axis=2) == 448.0)
 
 
+def _simulated_fp8_output(f, qd, kd, vd, scale, e):
+    """Exact attention on dequantized inputs with every softmax weight p
+    replaced by E4M3(p * 2^e) / 2^e, in float64 (causal)."""
+    B, H, N, d = qd.shape
+    sim = np.zeros((B, H, N, d))
+    for h in range(H):
+        s = scale * (qd[0, h] @ kd[0, h].T)
+        s = np.where(np.tril(np.ones((N, N), dtype=bool)), s, -np.inf)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        pr = f.e4m3_round(p * 2.0 ** e) / 2.0 ** e
+        sim[0, h] = (pr @ vd[0, h]) / p.sum(axis=1, keepdims=True)
+    return sim
+
+
 def check_weight_rounding_within_bound(f):
-    """Simulate the kernel's E4M3 softmax weights (p * 2^4, rounded) on the
-    dequantized inputs: the error against exact attention stays inside the
-    reported bound everywhere, and its typical size matches ``sigma``."""
+    """Simulate E4M3 softmax weights on the dequantized inputs: rounding each
+    weight p itself (the plain reading), or p * 2^e for e = 2, 4, 8 (a scaling
+    an implementation may pick to use more of the format's range), keeps the
+    error against exact attention inside the bound the oracle reports, which
+    depends on the format only; its typical size matches ``sigma``.  A scaling
+    the other way (e = -4, pushing weights into the subnormal range) leaves
+    the bound: a kernel that did so would be caught, whatever it claimed."""
     B, H, N, d = 1, 2, 384, 64
     q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=14)
     scale = d ** -0.5
     o, lse, bound, sigma = f.forward_fp8_reference(q, k, v, scale, True)
     qd, kd, vd = f.dequantized(q, k, v)
-    sim = np.zeros_like(o)
-    for h in range(H):
-        s = scale * (qd[0, h] @ kd[0, h].T)
-        s = np.where(np.tril(np.ones((N, N), dtype=bool)), s, -np.inf)
-        p = np.exp(s - s.max(axis=1, keepdims=True))
-        pr = f.e4m3_round(p * 16.0) / 16.0
-        sim[0, h] = (pr @ vd[0, h]) / p.sum(axis=1, keepdims=True)
-    err = np.abs(sim - o)
-    assert np.all(err <= bound)
-    ratio = np.sqrt(np.mean((err / sigma) ** 2))
-    assert 0.2 < ratio < 1.0, ratio
+    for e in (0, 2, 4, 8):
+        err = np.abs(_simulated_fp8_output(f, qd, kd, vd, scale, e) - o)
+        assert np.all(err <= bound), e
+        ratio = np.sqrt(np.mean((err / sigma) ** 2))
+        assert 0.2 < ratio < 1.0, (e, ratio)
+    err = np.abs(_simulated_fp8_output(f, qd, kd, vd, scale, -4) - o)
+    assert np.any(err > bound)
     ro, rl = oracle.attention_forward(qd, kd, vd, scale, True)
     assert np.array_equal(o, ro) and np.array_equal(lse, rl)
+
+
+def check_format_bound_constants(f):
+    """The weight bound is the E4M3 format's own: half the step of three
+    mantissa bits relative to a normal value, half the subnormal step 2^-9
+    absolute.  Checked on every value of the codebook in [0, 1] and at the
+    midpoints between them, where rounding errs most."""
+    c = _codebook()
+    c = np.unique(c[np.isfinite(c) & (c >= 0) & (c <= 1)])
+    mids = (c[:-1] + c[1:]) / 2.0
+    x = np.concatenate([c, mids, np.nextafter(mids, 0), np.nextafter(mids, 1)])
+    err = np.abs(f.e4m3_round(x) - x)
+    assert np.all(err <= np.maximum(f.P_REL * x, f.P_ABS))
+    # neither constant is looser than the format needs: the absolute limit is
+    # reached, the relative one approached (1/17 just above a power of two)
+    assert np.any(err == f.P_ABS)
+    assert np.any((err > 0.9 * f.P_REL * x) & (x >= 2.0 ** -6))
 
 
 def check_incoherent_processing_helps_with_outliers(f):
@@ -194,5 +226,6 @@ ALL_CHECKS = [
     check_block_scales_closed_form,
     check_rotation_is_orthogonal_transform,
     check_weight_rounding_within_bound,
+    check_format_bound_constants,
     check_incoherent_processing_helps_with_outliers,
 ]

@@ -101,3 +101,66 @@ def test_decode_shapes(S, H, max_ctx, ctx):
     ro, _ = oracle.paged_decode(di.q, di.k_cache, di.v_cache, di.block_tables, di.context_lens,
                                 di.scale)
     assert np.abs(out.float().cpu().numpy() - ro).max() <= TOL_O
+
+
+def test_decode_workspace_grows_on_a_second_stream_while_a_forward_runs():
+    """A small decode on one stream, then (ordered after it by an event) a
+    larger decode on a second stream whose split-K workspace must grow, in
+    stream order, while a forward runs on a third stream.  Nothing waits for
+    the device in between; all three results match the oracle."""
+    fa.fa_release()   # start from an empty workspace, so the second decode grows it
+    small = inputs.decode_inputs(2, 2, 128, 16, 600, seed=51, device=DEV)
+    large = inputs.decode_inputs(24, 8, 128, 16, 3000, seed=52, device=DEV)
+    q, k, v = (t.to(DEV) for t in inputs.forward_inputs(2, 8, 2048, 128, torch.bfloat16, seed=53))
+    s1, s2, s3 = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s3):
+        o, lse = fa.forward(q, k, v, causal=True)
+    with torch.cuda.stream(s1):
+        out_small = fa.paged_decode(small.q, small.k_cache, small.v_cache, small.block_tables,
+                                    small.context_lens, small.scale)
+        done = torch.cuda.Event()
+        done.record(s1)
+    s2.wait_event(done)
+    with torch.cuda.stream(s2):
+        out_large = fa.paged_decode(large.q, large.k_cache, large.v_cache, large.block_tables,
+                                    large.context_lens, large.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    for di, out in ((small, out_small), (large, out_large)):
+        ro, _ = oracle.paged_decode(di.q, di.k_cache, di.v_cache, di.block_tables,
+                                    di.context_lens, di.scale)
+        assert np.abs(out.float().cpu().numpy() - ro).max() <= TOL_O
+    rows = [0, 1000, 2047]
+    ro, rl = _ref(q.cpu(), k.cpu(), v.cpu(), True, rows)
+    assert np.abs(o[:, :, rows].float().cpu().numpy() - ro).max() <= TOL_O
+    assert np.abs(lse[:, :, rows].cpu().numpy() - rl).max() <= TOL_L
+
+
+def test_decode_workspace_cannot_grow_during_capture():
+    """A call being captured into a graph may not allocate: with a workspace
+    too small for it, the decode returns FA_ERR_UNSUPPORTED and the capture
+    can still be ended."""
+    fa.fa_release()
+    small = inputs.decode_inputs(1, 1, 128, 16, 100, seed=54, device=DEV)
+    large = inputs.decode_inputs(8, 8, 128, 16, 2000, seed=55, device=DEV)
+    fa.paged_decode(small.q, small.k_cache, small.v_cache, small.block_tables,
+                    small.context_lens, small.scale)
+    torch.cuda.synchronize()
+    out = torch.empty_like(large.q)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    err = None
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        try:
+            fa.fa_paged_decode(large.q.data_ptr(), large.k_cache.data_ptr(),
+                               large.v_cache.data_ptr(), large.block_tables.data_ptr(),
+                               large.context_lens.data_ptr(), out.data_ptr(), 8, 8, 128, 16,
+                               large.max_blocks, large.scale, s.cuda_stream)
+        except fa.FattnError as e:
+            err = e
+        finally:
+            g.capture_end()
+    assert err is not None and err.status == -2   # FA_ERR_UNSUPPORTED
+    torch.cuda.synchronize()

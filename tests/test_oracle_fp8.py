@@ -39,6 +39,8 @@ MUTANTS = [
     ("v_per_block", "vc, vs = quantize_heads(v)\n    return dequantize_rows(qc, qs), dequantize_rows(kc, ks), vc * vs[:, :, None, None].astype(np.float64)",
      "vc, vs = quantize_rows(v)\n    return dequantize_rows(qc, qs), dequantize_rows(kc, ks), dequantize_rows(vc, vs)"),
     ("bound_without_v", "bound[b, h] = (w @ np.abs(vd[b, h])) / l", "bound[b, h] = w.sum(axis=1, keepdims=True) / l * 0.25"),
+    ("weight_bound_kernel_specific", "P_ABS = 2.0 ** -10", "P_ABS = 2.0 ** -14"),
+    ("weight_bound_relative_too_tight", "P_REL = 2.0 ** -4", "P_REL = 2.0 ** -5"),
     ("sigma_without_third", "var[b, h] = ((w * w / 3.0) @ (vd[b, h] ** 2)) / (l * l)",
      "var[b, h] = ((w * w) @ (vd[b, h] ** 2)) / (l * l) * 9.0"),
 ]
