@@ -619,6 +619,7 @@ def gpu_arm(args):
 
     # ---- grouped-head decode (4 query heads per cached head) ---------------
     if want("decode_gqa"):
+        fa.fa_decode_gqa_select(args.gqa_impl)
         dg = decode_workload(DEC_GQA, args.decode_seqs)
         Sg, Hg, Dg = dg.q.shape
         gqs = [dg.q] + [dg.q.clone() for _ in range(3)]
@@ -631,7 +632,8 @@ def gpu_arm(args):
                                    dg.context_lens.data_ptr(), gouts[i % 4].data_ptr(), Sg, Hg,
                                    dg.num_kv_heads, Dg, dg.block_size, dg.max_blocks, dg.scale,
                                    sptr)
-        rec = timer.run(run_gqa, False, launches_per_call=2)
+        rec = timer.run(run_gqa, False, launches_per_call=1 if args.gqa_impl == 1 else 2)
+        fa.fa_decode_gqa_select(0)
         launches += rec["launches"]
         times["decode_gqa"] = rec["ms"]
         legs["decode_gqa"] = rec
@@ -765,13 +767,13 @@ def gpu_arm(args):
                                  "(fa_quantize_fp8: 128-row blocks for Q and K, per-head V; no "
                                  "transform), bf16 output",
                                  recorded_traffic("fwd_bf16_tc_kernel<128,0,0,1>"))
-        n_el = B * H * N * d
-        quant_bytes = 2 * n_el * 2 + 2 * n_el + (2 * n_el + 2 * n_el + n_el)
+        # algorithmic: each bf16 input read once, each E4M3 code written once
+        quant_bytes = 3 * B * H * N * d * 3
         res["fwd_fp8"]["quantize"] = leg_out(
             "fp8_quant", quant_bytes, 1e9, "GB/s", peak_h, hbm_kind, "hbm",
             "fp8_quant_rows_kernel + fp8_quant_v_kernel",
-            "fa_quantize_fp8 of the forward workload (Q, K: 2 B read + 1 B written per "
-            "element; V: 2 + 2 B read + 1 B written)")
+            "fa_quantize_fp8 of the forward workload (algorithmic bytes: 2 B read + 1 B "
+            "written per element of Q, K and V; the kernels read V twice)")
         res["fwd_fp8"]["value_with_quantize"] = round(
             weak_scaling_rate(flops, ws, times["fwd_fp8"] + times["fp8_quant"], 1e12), 2)
     if "backward" in legs:
@@ -791,13 +793,14 @@ def gpu_arm(args):
                                       recorded_traffic("bwd_main_kernel<64>"),
                                       {"flops_per_launch": bf})
     if "decode_gqa" in legs:
+        gk = ("paged_decode_gqa_kernel<4>" if args.gqa_impl == 1 else
+              "paged_decode_gqa_tc_kernel<4> + paged_decode_merge_kernel")
         res["decode_gqa"] = leg_out("decode_gqa", gqa_bytes, 1e9, "GB/s", peak_h, hbm_kind,
-                                    "hbm", "paged_decode_gqa_tc_kernel<4> + "
-                                    "paged_decode_merge_kernel",
+                                    "hbm", gk,
                                     f"fa_paged_decode_gqa bf16 {args.decode_seqs} seqs x 32 query "
                                     "heads x 8 key/value heads x head 128, block 16, ctx "
                                     "U[1,4096]; q and out rotated over 4 buffers",
-                                    recorded_traffic("paged_decode_gqa_tc_kernel<4>"),
+                                    recorded_traffic(gk.split(" ")[0]),
                                     {"bytes_per_launch": gqa_bytes})
 
     if only is not None:
@@ -1084,6 +1087,9 @@ def main():
                     help=f"comma-separated legs to run alone ({', '.join(LEGS)})")
     ap.add_argument("--decode-seqs", type=int, default=DEC["num_seqs"],
                     help="sequences of the decode workloads (smaller for profiling)")
+    ap.add_argument("--gqa-impl", type=int, default=0, choices=[0, 1, 2],
+                    help="grouped-decode kernel (fa_decode_gqa_select): 0 automatic, 1 CUDA "
+                         "cores, 2 tensor cores")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
         ap.error("--warmup must be >= 3")

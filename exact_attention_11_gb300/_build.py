@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfattn.so")
 SOURCES = ["api.cu", "fwd_f32.cu", "fwd_bf16.cu", "decode.cu", "decode_noalloc.cu",
-           "bwd_bf16.cu", "bwd_bf16_d128.cu", "decode_gqa.cu", "fp8_quant.cu",
+           "bwd_bf16.cu", "bwd_bf16_d128.cu", "bwd_bf16_d64.cu", "decode_gqa.cu", "fp8_quant.cu",
            "fwd_d256.cu", "mask_tiles.cu", "decode_gqa_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
@@ -51,7 +51,7 @@ def up_to_date() -> bool:
 # exactly this many registers per thread at launch, or the warpgroups that
 # raise their count could wait forever for registers that do not exist.
 SETMAXNREG_KERNELS = {"fwd_bf16.cu": ("fwd_bf16_tc_kernel", 168),
-                      "bwd_bf16.cu": ("bwd_main_kernel", 168),
+                      "bwd_bf16_d64.cu": ("bwd_pipe64_kernel", 168),
                       "bwd_bf16_d128.cu": ("bwd_pipe_kernel", 168)}
 
 

@@ -185,13 +185,25 @@ __global__ void __launch_bounds__(kThreads)
 // grid (n_blk, BH): codes one 128-row block of V with its head's scale and
 // writes it transposed into V^T [BH][128][Npad].  The block's bulk copy is
 // issued first, so it lands while the head's block maxima are reduced.
+//
+// Transposition: warp w codes keys 16 w .. 16 w + 15 of the block and lane l
+// the four dimensions 4 l .. 4 l + 3, four keys at a time.  The four code
+// words of four keys (one byte per dimension) are transposed in registers
+// with byte permutes into four words of one dimension (one byte per key), so
+// after four rounds the lane holds, for each of its dimensions, the 16 keys
+// of the warp as one 16-byte chunk.  The chunks pass through shared memory
+// (a 16 KB tile in the staging buffer, chunk index XOR-swizzled by the
+// dimension, so that neither the writes nor the reads have bank conflicts)
+// and leave as whole 128-byte rows of V^T: eight lanes per row, four rows per
+// store instruction.
 __global__ void __launch_bounds__(kThreads)
     fp8_quant_v_kernel(const uint16_t *__restrict__ v, const float *__restrict__ v_amax,
                        uint8_t *__restrict__ vt8, float *__restrict__ v_scale, int N, int n_blk,
                        int n_pad, int *__restrict__ dev_status) {
-  constexpr int kPitch = kRows + 1;   // bytes per transposed row in shared memory
   extern __shared__ __align__(128) uint8_t stage[];   // 128 rows x 256 bytes
-  __shared__ __align__(16) uint8_t tile[kD * kPitch];
+  // The V^T block (128 dims x 128 keys, 16 KB) reuses the staging buffer once
+  // every row has been read, so a CTA needs 32 KB and seven fit per SM.
+  uint8_t *tile = stage;
   __shared__ float red[kThreads / 32];
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -223,37 +235,44 @@ __global__ void __launch_bounds__(kThreads)
     if (threadIdx.x == 0) atomicExch(dev_status, kDevTimeout);
     return;
   }
-#pragma unroll 4
-  for (int i = 0; i < kRowsPerWarp; ++i) {
-    const int rl = warp * kRowsPerWarp + i;        // key within the block
-    const uint32_t c = code4(staged4(stage, rl, n_rows, lane), inv);
+  uint32_t t4[4][4];   // [dimension 4 lane + e][round]: keys 4 round .. +3 of the warp
 #pragma unroll
-    for (int e = 0; e < 4; ++e) tile[(4 * lane + e) * kPitch + rl] = (c >> (8 * e)) & 0xffu;
+  for (int r = 0; r < 4; ++r) {
+    uint32_t cw[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      cw[kk] = code4(staged4(stage, 16 * warp + 4 * r + kk, n_rows, lane), inv);
+    const uint32_t lo01 = __byte_perm(cw[0], cw[1], 0x5140);   // [a0 b0 a1 b1]
+    const uint32_t lo23 = __byte_perm(cw[2], cw[3], 0x5140);   // [c0 d0 c1 d1]
+    const uint32_t hi01 = __byte_perm(cw[0], cw[1], 0x7362);   // [a2 b2 a3 b3]
+    const uint32_t hi23 = __byte_perm(cw[2], cw[3], 0x7362);   // [c2 d2 c3 d3]
+    t4[0][r] = __byte_perm(lo01, lo23, 0x5410);
+    t4[1][r] = __byte_perm(lo01, lo23, 0x7632);
+    t4[2][r] = __byte_perm(hi01, hi23, 0x5410);
+    t4[3][r] = __byte_perm(hi01, hi23, 0x7632);
+  }
+  __syncthreads();   // every staged row has been read: the tile may overwrite it
+  // Chunk w of dimension row dd sits at 16-byte slot w ^ ((dd >> 2) & 7).
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int dd = 4 * lane + e;
+    *reinterpret_cast<uint4 *>(tile + dd * kRows + ((warp ^ ((dd >> 2) & 7)) << 4)) =
+        make_uint4(t4[e][0], t4[e][1], t4[e][2], t4[e][3]);
   }
   __syncthreads();
-  // Row c of V^T, keys blk*128 .. +127: lane l of warp w stores the 16 keys
-  // of chunk l & 7 of row c = 16 w + i + 4 (l >> 3) in pass i, gathered from
-  // the byte tile by five aligned word loads and funnel shifts.  Byte 129 c +
-  // 16 k lies in word 32 c + 4 k + c / 4 at byte c & 3 = i, so the warp's 32
-  // loads of a pass fall in 32 different banks and its stores fill four whole
-  // 128-byte rows.  Chunks at or past Npad are not written (Npad is a
-  // multiple of 16, so a chunk never straddles it).
+  // Row dd of V^T, keys blk*128 .. +127: lane l of warp w stores chunk l & 7
+  // of row 16 w + 4 i + (l >> 3) in pass i.  Chunks at or past Npad are not
+  // written (Npad is a multiple of 16, so a chunk never straddles it).
   uint8_t *out = vt8 + static_cast<int64_t>(bh) * kD * n_pad;
   const int chunk = lane & 7;
   const int key = blk * kRows + 16 * chunk;
   if (key < n_pad) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int c = 16 * warp + i + 4 * (lane >> 3);
-      const uint32_t *wp =
-          reinterpret_cast<const uint32_t *>(tile + ((c * kPitch + 16 * chunk) & ~3));
-      uint32_t w[5];
-#pragma unroll
-      for (int j = 0; j < 5; ++j) w[j] = wp[j];
-      const uint32_t sh = 8u * static_cast<uint32_t>(i);
-      const uint4 o = make_uint4(__funnelshift_r(w[0], w[1], sh), __funnelshift_r(w[1], w[2], sh),
-                                 __funnelshift_r(w[2], w[3], sh), __funnelshift_r(w[3], w[4], sh));
-      *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(c) * n_pad + key) = o;
+      const int dd = 16 * warp + 4 * i + (lane >> 3);
+      const uint4 o = *reinterpret_cast<const uint4 *>(
+          tile + dd * kRows + ((chunk ^ ((dd >> 2) & 7)) << 4));
+      *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(dd) * n_pad + key) = o;
     }
   }
   if (blk == 0 && threadIdx.x == 0) v_scale[bh] = s;

@@ -74,7 +74,7 @@ cudaError_t launch_fp8_quantize(const void *q, const void *k, const void *v, con
 // of dO) are bf16 maps like the forward's but with boxes of
 // bwd_qdo_box_rows(d) rows; tk, tv as in the forward; tdq is the fp32 map of
 // the accumulator (boxes of 32 x 32 x 1, 128-byte swizzle; used for d = 64).
-inline int bwd_qdo_box_rows(int d) { return d == 128 ? 64 : 128; }
+inline int bwd_qdo_box_rows(int) { return 64; }
 size_t bwd_workspace_bytes(int BH, int N, int d);
 cudaError_t launch_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const CUtensorMap &tdo, const CUtensorMap &tdq, const void *o,
@@ -89,6 +89,14 @@ cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
                                  const float *vecs, float *dq_acc, void *dk, void *dv, int BH,
                                  int N, float scale, int causal, int *dev_status,
                                  cudaStream_t stream);
+
+// The d = 64 main kernel (bwd_bf16_d64.cu); tdq = the accumulator's fp32 map
+// (its dQ' tiles are added with TMA reduces).
+cudaError_t launch_bwd_main_d64(const CUtensorMap &tq64, const CUtensorMap &tk,
+                                const CUtensorMap &tv, const CUtensorMap &tdo64,
+                                const CUtensorMap &tdq, const float *vecs, void *dk, void *dv,
+                                int BH, int N, float scale, int causal, int *dev_status,
+                                cudaStream_t stream);
 
 int decode_max_parts(int max_num_blocks_per_seq);
 // Grouped key/value heads (decode_gqa.cu): group = num_heads / num_kv_heads
