@@ -121,7 +121,7 @@ cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   if (e != cudaSuccess) return e;
   // Q and dO maps have 64-row boxes (the main kernels' 64-query sub-tiles).
   if constexpr (D == 128)
-    e = launch_bwd_main_d128(tq, tk, tv, tdo, vecs, dq_acc, dk, dv, BH, N, scale, causal,
+    e = launch_bwd_main_d128(tq, tk, tv, tdo, tdq, vecs, dk, dv, BH, N, scale, causal,
                              dev_status, stream);
   else
     e = launch_bwd_main_d64(tq, tk, tv, tdo, tdq, vecs, dk, dv, BH, N, scale, causal,

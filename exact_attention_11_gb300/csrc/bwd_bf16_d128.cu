@@ -18,11 +18,12 @@
 //   dQ_t'^T = K_j^T dS_t^T -> R_t[64,128) (lanes = d, columns = queries)
 //   dV_j += P_t^T dO_t,  dK_j += dS_t^T Q_t            (A operands from TMEM)
 //   group t reads dQ_t'^T out of TMEM and adds it to the fp32 dQ accumulator
-//   from registers: for each query the warp's 32 lanes (32 consecutive d)
-//   add one contiguous 128-byte run of its row.
+//   with TMA reduces: each warp stages its 32 d x 64 queries as two
+//   [query][d] boxes in its own quarter of the dS^T buffer, which dQ_t'^T has
+//   finished reading and the group only writes again in its next element
+//   step.
 // The kernel is bound by shared-memory bandwidth (MMA operands, TMA writes,
-// dS stores), so operands come from TMEM wherever the TMEM budget allows and
-// dQ' never passes through shared memory.
+// dS stores), so operands come from TMEM wherever the TMEM budget allows.
 // MMA order per sub-tile: dQ'_t, dV_t, dK_t, then S_t, dP_t of the next step
 // (after group t has released R_t), then the other sub-tile.  Q and dO
 // arrive as 64-row halves through 4-slot rings, two steps ahead.
@@ -106,7 +107,8 @@ constexpr int kDevBadSmemBase = -2;
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_pipe_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const float *__restrict__ vecs, float *__restrict__ dq_acc,
+                    const __grid_constant__ CUtensorMap tm_dq,
+                    const float *__restrict__ vecs,
                     __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int N, int BH,
                     float scale, int causal, int *__restrict__ dev_status) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -326,16 +328,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarTmemFree + t));
-      // Add into the row-major accumulator: for query q0 + qq the 32 lanes
-      // (d = 32*quarter + lane) cover one contiguous 128-byte run of its row.
-      float *dst = dq_acc + (static_cast<int64_t>(bh) * N + q0) * D + r;
+      // Add into the row-major accumulator with TMA reduces: this warp's
+      // quarter of the dS^T buffer (its own key rows, free now that dQ'^T,
+      // which read it, is complete) stages one 32-query x 32-d box at a time
+      // as [query][d] fp32 rows with the 128-byte swizzle.
+      {
+        uint8_t *stg = ds_buf + quarter * 4096;
+        const uint32_t stg_u32 = s_base + kOffDS + t * kDSBytes + quarter * 4096;
 #pragma unroll
-      for (int qq = 0; qq < 32; ++qq)
-        if (q0 + qq < N) red_add_f32(dst + static_cast<int64_t>(qq) * D, __uint_as_float(g0[qq]));
+        for (int bx = 0; bx < 2; ++bx) {
+          if (bx == 1) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
 #pragma unroll
-      for (int qq = 0; qq < 32; ++qq)
-        if (q0 + 32 + qq < N)
-          red_add_f32(dst + static_cast<int64_t>(32 + qq) * D, __uint_as_float(g1[qq]));
+          for (int qq = 0; qq < 32; ++qq)
+            *reinterpret_cast<uint32_t *>(stg + qq * 128 + ((((lane >> 2) ^ (qq & 7))) << 4) +
+                                          (lane & 3) * 4) = bx ? g1[qq] : g0[qq];
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d(&tm_dq, stg_u32, 32 * quarter, q0 + 32 * bx, bh);
+            bulk_commit();
+          }
+        }
+        // The next element phase writes dS^T rows over the staging area.
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+      }
     }
 
     // Epilogue: group 0 writes dV_j, group 1 dK_j = scale * (dS^T Q), as bf16
@@ -383,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (warp >= 4 && (threadIdx.x & 31) == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -396,7 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
                                  const CUtensorMap &tv, const CUtensorMap &tdo64,
-                                 const float *vecs, float *dq_acc, void *dk, void *dv, int BH,
+                                 const CUtensorMap &tdq,
+                                 const float *vecs, void *dk, void *dv, int BH,
                                  int N, float scale, int causal, int *dev_status,
                                  cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(bwd_pipe_kernel,
@@ -413,7 +435,7 @@ cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bwd_pipe_kernel, tq64, tk, tv, tdo64, vecs, dq_acc,
+  return cudaLaunchKernelEx(&cfg, bwd_pipe_kernel, tq64, tk, tv, tdo64, tdq, vecs,
                             reinterpret_cast<__nv_bfloat16 *>(dk),
                             reinterpret_cast<__nv_bfloat16 *>(dv), N, BH, scale, causal,
                             dev_status);

@@ -73,7 +73,7 @@ cudaError_t launch_fp8_quantize(const void *q, const void *k, const void *v, con
 // fp32) per 128-query block: 4 * B*H*Npad*(d + 2) bytes.  tq and tdo (the map
 // of dO) are bf16 maps like the forward's but with boxes of
 // bwd_qdo_box_rows(d) rows; tk, tv as in the forward; tdq is the fp32 map of
-// the accumulator (boxes of 32 x 32 x 1, 128-byte swizzle; used for d = 64).
+// the accumulator (boxes of 32 x 32 x 1, 128-byte swizzle).
 inline int bwd_qdo_box_rows(int) { return 64; }
 size_t bwd_workspace_bytes(int BH, int N, int d);
 cudaError_t launch_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
@@ -83,10 +83,11 @@ cudaError_t launch_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             int *dev_status, cudaStream_t stream);
 
 // The d = 128 main kernel (bwd_bf16_d128.cu); vecs = the [-LSE2 | -D]
-// blocks, dq_acc = the row-major fp32 accumulator.
+// blocks, tdq = the fp32 map of the row-major dQ accumulator (TMA reduces).
 cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
                                  const CUtensorMap &tv, const CUtensorMap &tdo64,
-                                 const float *vecs, float *dq_acc, void *dk, void *dv, int BH,
+                                 const CUtensorMap &tdq, const float *vecs, void *dk, void *dv,
+                                 int BH,
                                  int N, float scale, int causal, int *dev_status,
                                  cudaStream_t stream);
 
