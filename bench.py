@@ -787,10 +787,10 @@ def gpu_arm(args):
     if "backward_d64" in legs:
         bf = bwd_flops_of(**BWD_D64)
         res["backward_d64"] = leg_out("backward_d64", bf, 1e12, "TFLOP/s", peak_t, tensor_kind,
-                                      "tensor", "bwd_prep_kernel + bwd_main_kernel<64> + "
+                                      "tensor", "bwd_prep_kernel + bwd_pipe64_kernel + "
                                       "bwd_dq_kernel",
                                       "fa_backward bf16 B=2 H=16 N=4096 d=64 causal",
-                                      recorded_traffic("bwd_main_kernel<64>"),
+                                      recorded_traffic("bwd_pipe64_kernel"),
                                       {"flops_per_launch": bf})
     if "decode_gqa" in legs:
         gk = ("paged_decode_gqa_kernel<4>" if args.gqa_impl == 1 else
