@@ -93,12 +93,23 @@ def test_bf16_workload_b2_h16_n4096_d128_causal_full():
     check(o, lse, ro, rl, BF16_TOL_O, BF16_TOL_LSE, "2x16x4096x128 causal")
 
 
+def test_bf16_workload_b1_h8_n16384_d128_causal_full():
+    """Every output (all 16384 rows of all 8 heads, O and LSE) of the
+    1 x 8 x 16384 x 128 causal workload with inputs N(0,1) * 0.5 (the oracle
+    takes some seconds on the host cores)."""
+    q, k, v = inputs.forward_inputs(1, 8, 16384, 128, torch.bfloat16, seed=4, amp=0.5)
+    o, lse = gpu_forward(q, k, v, True)
+    ro, rl = oracle.attention_forward(q, k, v, 128 ** -0.5, True)
+    check(o, lse, ro, rl, BF16_TOL_O, BF16_TOL_LSE, "1x8x16384x128 causal")
+
+
 @pytest.mark.parametrize("B,H,N,d,amp,nrows,seed", [
     (1, 8, 16384, 128, 0.5, 256, 4),    # 1 x 8 x 16384 x 128 causal, inputs * 0.5
 ])
 def test_bf16_large_causal_sampled_rows(B, H, N, d, amp, nrows, seed):
-    """The 16K causal workload; the oracle checks a seeded sample of 256 query
-    rows of every head plus the first, second and last rows."""
+    """The 16K causal workload on the seeded sample of 256 query rows per head
+    (plus the first, second and last rows) that the workload's parity
+    statement names; the full comparison is the test above."""
     q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=seed, amp=amp)
     o, lse = gpu_forward(q, k, v, True)
     rows = sorted(set(inputs.sample_rows(N, nrows, seed=seed + 100).tolist()) | {0, 1, N - 1})
