@@ -58,6 +58,10 @@ def _compare(got, ref, name):
     (1, 1, 130, 64, False),     # two-row tail past one tile
     (1, 2, 1000, 128, False),   # eight key blocks, non-causal
     (1, 1, 1, 128, True),       # a single row
+    (2, 3, 333, 64, True),      # d = 64: ragged tail, several heads
+    (1, 2, 1000, 64, False),    # d = 64: eight key blocks, non-causal
+    (1, 1, 1, 64, True),        # d = 64: a single row
+    (1, 1, 65, 64, True),       # d = 64: one key block, second sub-tile empty
 ])
 def test_backward_matches_oracle(B, H, N, d, causal):
     (q, k, v, do), (dq, dk, dv) = _run(B, H, N, d, causal, seed=N + d)
