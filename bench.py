@@ -582,8 +582,16 @@ def gpu_arm(args):
                                sptr)
         rec = timer.run(run_fp8, True)
         recq = timer.run(run_quant, True, launches_per_call=2)
+        # context for the quantization's rate: a plain device copy moving the
+        # same number of bytes (half read, half written), timed the same way
+        # (L2 flushed before each call, so both pay for its dirty lines)
+        csrc = torch.empty((3 * B * H * N * d * 3) // 2, dtype=torch.uint8, device=dev)
+        cdst = torch.empty_like(csrc)
+        recc = timer.run(lambda _i=0: cdst.copy_(csrc), True, launches_per_call=0)
+        del csrc, cdst
         launches += rec["launches"] + recq["launches"]
         times["fwd_fp8"], times["fp8_quant"] = rec["ms"], recq["ms"]
+        times["copy_same_bytes"] = recc["ms"]
         legs["fwd_fp8"], legs["fp8_quant"] = rec, recq
         del x8, o8, l8, qws, qq, kk, vv
 
@@ -774,6 +782,12 @@ def gpu_arm(args):
             "fp8_quant_rows_kernel + fp8_quant_v_kernel",
             "fa_quantize_fp8 of the forward workload (algorithmic bytes: 2 B read + 1 B "
             "written per element of Q, K and V; the kernels read V twice)")
+        res["fwd_fp8"]["quantize"]["same_bytes_copy"] = {
+            "what": f"torch device copy of {quant_bytes / 2e6:.1f} MB ({quant_bytes / 1e6:.0f} MB "
+                    "moved), timed like the quantization",
+            "ms": times["copy_same_bytes"],
+            "GB/s": round(quant_bytes / (times["copy_same_bytes"] * 1e-3) / 1e9, 1),
+            "quantize_rate_over_copy_rate": round(times["copy_same_bytes"] / times["fp8_quant"], 3)}
         res["fwd_fp8"]["value_with_quantize"] = round(
             weak_scaling_rate(flops, ws, times["fwd_fp8"] + times["fp8_quant"], 1e12), 2)
     if "backward" in legs:

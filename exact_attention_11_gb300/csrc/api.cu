@@ -411,6 +411,7 @@ int fa_quantize_fp8(const void *q, const void *k, const void *v, const float *si
   if (BH > 65535 || N > (1 << 30)) return FA_ERR_UNSUPPORTED;
   if (BH == 0 || N == 0) return FA_OK;
   if (!workspace) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 4 != 0) return FA_ERR_ALIGNMENT;
   if (workspace_bytes < fattn::fp8_quant_workspace_bytes((int)BH, N)) return FA_ERR_INVALID_ARG;
   int dev = 0, rc;
   {

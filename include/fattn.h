@@ -153,7 +153,8 @@ int fa_forward_masked(const void *q, const void *k, const void *v, void *o, floa
  * rounded to nearest even and saturated to +-448; the stored scale is s, or
  * s * fp32(1/sqrt(128)) with signs, so that code * scale stands for the
  * value.  workspace: at least fa_quantize_fp8_workspace_bytes bytes of device
- * memory, used during the call only.  Errors: FA_ERR_INVALID_ARG (null
+ * memory (4-byte aligned), used during the call only; calls that may run at
+ * the same time need separate workspaces.  Errors: FA_ERR_INVALID_ARG (null
  * pointer, negative size, workspace too small), FA_ERR_ALIGNMENT,
  * FA_ERR_UNSUPPORTED (d != 128, B*H > 65535 or N > 2^30), FA_ERR_CUDA.
  * Asynchronous on `stream`; B*H = 0 or N = 0 does nothing.

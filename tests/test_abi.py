@@ -179,6 +179,7 @@ QW = 4 * 2 * 3          # workspace of fa_quantize_fp8 for B=2, H=3, N <= 128
     ((P, P, P, NULL, P + 8, P, P, P, P, P, 2, 3, 100, 128, P, QW), -3),   # misaligned q8
     ((P, P, P, NULL, P, P, P, P, P, P, 2, 3, 100, 128, NULL, QW), -1),    # no workspace
     ((P, P, P, NULL, P, P, P, P, P, P, 2, 3, 100, 128, P, QW - 1), -1),   # one byte short
+    ((P, P, P, NULL, P, P, P, P, P, P, 2, 3, 100, 128, P + 2, QW), -3),   # misaligned workspace
     ((P, P, P, NULL, P, P, P, P, P, P, 300, 300, 100, 128, P, 1 << 40), -2),  # B*H > 65535
     ((P, P, P, NULL, P, P, P, P, P, P, -1, 3, 100, 128, P, QW), -1),      # negative B
     ((P, P, P, NULL, P, P, P, P, P, P, 0, 3, 100, 128, NULL, 0), 0),      # empty: no-op
@@ -188,6 +189,7 @@ def test_quantize_fp8_argument_checks(lib, args, expect):
 
 
 def test_quantize_fp8_sizes(lib):
+    # one fp32 block maximum per 128 rows of V
     assert lib.fa_quantize_fp8_workspace_bytes(2, 3, 100, 128) == 4 * 2 * 3
     assert lib.fa_quantize_fp8_workspace_bytes(2, 3, 129, 128) == 4 * 2 * 3 * 2
     assert lib.fa_quantize_fp8_workspace_bytes(-1, 3, 100, 128) == 0

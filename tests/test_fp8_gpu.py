@@ -71,6 +71,39 @@ def test_quantize_codes_and_scales_bit_exact(B, H, N, rot):
     assert np.array_equal(x.v_scale.cpu().numpy(), vscales)
 
 
+@pytest.mark.parametrize("B,H,N,rot", [
+    (2, 16, 2050, False),    # more blocks than resident CTAs, ragged tail
+    (2, 16, 2050, True),
+    (2, 16, 4096, False),    # the benchmark's shape
+])
+def test_quantize_large_bit_exact_with_reused_workspace(B, H, N, rot):
+    """Thousands of blocks (several waves of CTAs); the workspace starts as
+    garbage and is reused for a second call, which must give the same bytes."""
+    d = 128
+    q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=N + B)
+    signs = inputs.rotation_signs(d, seed=5) if rot else None
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    sd = None if signs is None else signs.to(DEV)
+    ws = torch.full((fa.fa_quantize_fp8_workspace_bytes(B, H, N, d),), 0xAB, dtype=torch.uint8,
+                    device=DEV)
+    x1 = fa.quantize_fp8(qd, kd, vd, sd, workspace=ws)
+    x2 = fa.quantize_fp8(qd, kd, vd, sd, workspace=ws)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    sg = None if signs is None else signs.numpy()
+    for got, got_s, src in ((x1.q8, x1.q_scale, q), (x1.k8, x1.k_scale, k)):
+        codes, scales = ofp8.quantize_rows(src, sg)
+        assert np.array_equal(got.cpu().numpy(), _e4m3_bytes(codes))
+        assert np.array_equal(got_s.cpu().numpy(), scales)
+    vcodes, vscales = ofp8.quantize_heads(v)
+    vt = x1.vt8.cpu().numpy()
+    assert np.array_equal(vt[..., :N], _e4m3_bytes(vcodes).transpose(0, 1, 3, 2))
+    assert np.all(vt[..., N:] == 0)
+    assert np.array_equal(x1.v_scale.cpu().numpy(), vscales)
+    for name in ("q8", "k8", "vt8", "q_scale", "k_scale", "v_scale"):
+        assert torch.equal(getattr(x1, name), getattr(x2, name)), name
+
+
 def test_quantize_zero_block_and_outliers():
     """A block of zeros (scale 1, zero codes) and inputs with large entries."""
     B, H, N, d = 1, 2, 384, 128
