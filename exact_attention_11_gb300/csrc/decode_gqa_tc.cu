@@ -49,6 +49,7 @@ constexpr int kPartBlocks = 64;
 static_assert(kPartBlocks % 8 == 0 && kPartBlocks <= 64, "partition size");
 constexpr int kPartTokens = kPartBlocks * kBlk;
 constexpr int kStepBlocks = 8;                               // 128 tokens per step
+constexpr int kStepsPerPart = kPartBlocks / kStepBlocks;     // 8
 constexpr int kNCols = 16;                                   // query heads per MMA (N)
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 64;     // S^T 2 x 16 | O^T 2 x 16
@@ -70,7 +71,9 @@ constexpr int kOffP = kOffQ + 2 * kQBytes;                // 2 buffers
 constexpr int kOffRed = kOffP + 2 * kPBytes;              // [2][4 warps][16] floats
 constexpr int kOffStats = kOffRed + 2 * 4 * kNCols * 4;   // UnitStats [2]
 constexpr int kOffSeq = kOffStats + 1024;                 // int2 [kDenseSeqs + 1]
-constexpr int kOffBar = kOffSeq + (kDenseSeqs + 32) * 8;
+constexpr int kOffPart = kOffSeq + (kDenseSeqs + 32) * 8;  // int16 [kDenseSeqs]: ragged tails
+constexpr int kOffBins = kOffPart + kDenseSeqs * 2;       // int [16]: tails per step count
+constexpr int kOffBar = kOffBins + 64;
 constexpr int kSmemBytes = kOffBar + 512;
 constexpr int kAlloc = kSmemBytes + 1024;
 static_assert(kAlloc <= 227 * 1024, "shared memory budget");
@@ -235,18 +238,25 @@ struct Unit {
 
 // Unit numbering.  Units of one (sequence, partition) pair are its cached
 // heads' slices, next to each other so that a cached head's second slice is
-// read from L2.  Dense: pairs are numbered sequence-major from the prefix sum
-// seq[s].x (seq[s].y = context length; seq[num_seqs].x = number of pairs), so
-// no unit is empty.  Sparse: pairs are (partition, sequence) with partitions
-// outermost, and those past a sequence's context are empty.
+// read from L2.
+// Dense (longest first, so that the units claimed last are the shortest and
+// the CTAs run out of work together): first every full partition
+// (kPartTokens tokens), numbered sequence-major from the prefix sum seq[s].x
+// of the sequences' full-partition counts (seq[s].y = context length); then
+// each sequence's ragged last partition, if it has one, in the order of
+// tail[] -- by step count, longest first.  seq[num_seqs] = (number of full
+// partitions, number of ragged ones).  No unit is empty.
+// Sparse: pairs are (partition, sequence) with partitions outermost, and
+// those past a sequence's context are empty.
 struct Numbering {
   int num_seqs, num_kv_heads, n_sub, group, gs, max_parts;
   bool dense;
   const int2 *seq;
+  const int16_t *tail;
   const int *context_lens;
   __device__ int per_pair() const { return num_kv_heads * n_sub; }
   __device__ int n_units() const {
-    return (dense ? seq[num_seqs].x : max_parts * num_seqs) * per_pair();
+    return (dense ? seq[num_seqs].x + seq[num_seqs].y : max_parts * num_seqs) * per_pair();
   }
   // Unit w (< n_units) -> u; returns false if it is an empty unit.
   __device__ bool decode(int w, Unit &u) const {
@@ -254,14 +264,20 @@ struct Numbering {
     u.kvh = rem / n_sub;
     u.hb = u.kvh * group + (rem - u.kvh * n_sub) * gs;
     if (dense) {
-      int lo = 0, hi = num_seqs - 1;   // the last s with seq[s].x <= p
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (seq[mid].x <= p) lo = mid; else hi = mid - 1;
+      const int n_full = seq[num_seqs].x;
+      if (p < n_full) {
+        int lo = 0, hi = num_seqs - 1;   // the last s with seq[s].x <= p
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (seq[mid].x <= p) lo = mid; else hi = mid - 1;
+        }
+        u.s = lo;
+        u.part = p - seq[lo].x;
+      } else {
+        u.s = tail[p - n_full];
+        u.part = seq[u.s].y / kPartTokens;
       }
-      u.s = lo;
-      u.part = p - seq[lo].x;
-      u.ctx = seq[lo].y;
+      u.ctx = seq[u.s].y;
       return true;
     }
     u.part = p / num_seqs;
@@ -270,6 +286,14 @@ struct Numbering {
     return u.part < partitions_of(u.ctx);
   }
 };
+
+// Steps (128 tokens) in the ragged last partition of a context of c tokens;
+// 0 if it has none.
+__device__ __forceinline__ int tail_steps(int c) {
+  if (c <= 0) return 0;
+  const int r = c % kPartTokens;
+  return (r + kStepBlocks * kBlk - 1) / (kStepBlocks * kBlk);
+}
 
 // NC = the query heads of a slice the softmax and epilogue handle (4, 8 or
 // 16 >= gs); MMA columns past NC hold zero P and are never read back.
@@ -304,6 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   nb.max_parts = max_parts;
   nb.dense = num_seqs <= kDenseSeqs;
   nb.seq = seq;
+  int16_t *tail = reinterpret_cast<int16_t *>(smem + kOffPart);
+  int *bins = reinterpret_cast<int *>(smem + kOffBins);
+  nb.tail = tail;
   nb.context_lens = context_lens;
 
   // P columns past NC are never written: zero both P buffers once.
@@ -348,17 +375,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // that kernel's tail; no global memory is read or written before this wait.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (nb.dense) {
-    // Partition counts per sequence, then their exclusive prefix sum (warp 0).
-    // Sequences with no context get zero outputs here, from CTA 0.
+    // Full-partition counts per sequence, then their exclusive prefix sum
+    // (warp 0); warp 9 - t counts the ragged tails of t steps (t = 1 .. 8),
+    // then lists them after the longer ones, in sequence order.  Sequences
+    // with no context get zero outputs here, from CTA 0.
     for (int i = threadIdx.x; i < num_seqs; i += kThreads) {
       const int c = context_lens[i];
-      seq[i] = make_int2(partitions_of(c), c);
+      seq[i] = make_int2(c > 0 ? c / kPartTokens : 0, c);
       if (c <= 0 && blockIdx.x == 0) {
         uint4 *o = reinterpret_cast<uint4 *>(out + static_cast<int64_t>(i) * num_heads * kHead);
         for (int j = 0; j < num_heads * kHead / 8; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
     __syncthreads();
+    const int t_steps = 9 - warp;   // warps 1 .. 8: tails of 8 .. 1 steps
     if (warp == 0) {
       int carry = 0;
       for (int base = 0; base < num_seqs; base += 32) {
@@ -373,7 +403,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i < num_seqs) seq[i].x = carry + incl - v;
         carry += __shfl_sync(~0u, incl, 31);
       }
-      if (lane == 0) seq[num_seqs] = make_int2(carry, 0);
+      if (lane == 0) seq[num_seqs].x = carry;
+    } else if (warp <= 8) {
+      int n = 0;
+      for (int base = 0; base < num_seqs; base += 32) {
+        const int i = base + lane;
+        n += __popc(__ballot_sync(~0u, i < num_seqs && tail_steps(seq[i].y) == t_steps));
+      }
+      if (lane == 0) bins[t_steps] = n;
+    }
+    __syncthreads();
+    if (warp >= 1 && warp <= 8) {
+      int at = 0;   // tails with more steps come first
+      for (int t = t_steps + 1; t <= kStepsPerPart; ++t) at += bins[t];
+      for (int base = 0; base < num_seqs; base += 32) {
+        const int i = base + lane;
+        const bool mine = i < num_seqs && tail_steps(seq[i].y) == t_steps;
+        const uint32_t m = __ballot_sync(~0u, mine);
+        if (mine) tail[at + __popc(m & ((1u << lane) - 1u))] = static_cast<int16_t>(i);
+        at += __popc(m);
+      }
+      if (warp == 1 && lane == 0) {
+        int n_tails = 0;
+        for (int t = 1; t <= kStepsPerPart; ++t) n_tails += bins[t];
+        seq[num_seqs].y = n_tails;
+      }
     }
   }
   __syncthreads();
