@@ -88,6 +88,46 @@ def test_gqa_decode_many_partitions(impl):
     _check(di, ctx=ctx)
 
 
+def test_gqa_decode_tails_of_every_length(impl):
+    """Contexts whose last 1024-token partition holds each of 1 .. 8 steps of
+    128 tokens, or none (whole partitions only), and empty ones, in an order
+    not sorted by length: the tensor-core kernel hands out the whole
+    partitions first and then these ragged tails, longest first."""
+    ctx = []
+    for full in range(3):
+        for steps in (8, 1, 5, 3, 7, 2, 6, 4):
+            ctx.append(1024 * full + 128 * (steps - 1) + 1 + (37 * steps + 11 * full) % 127)
+    ctx += [1024, 0, 2048, 3072, 0]
+    di = inputs.decode_inputs(len(ctx), 32, 128, 16, 3100, seed=47, device=DEV, num_kv_heads=8)
+    got = _check(di, ctx=ctx)
+    assert (got[[25, 28]] == 0).all()
+
+
+def test_gqa_decode_dense_numbering_limit(impl):
+    """1024 sequences, the most the tensor-core kernel numbers from its
+    shared-memory prefix sums (one ragged tail each, of every length), some
+    empty: 16 sampled sequences against the oracle, all against the other
+    kernel."""
+    S = 1024
+    di = inputs.decode_inputs(S, 8, 128, 16, 1000, seed=53, device=DEV, num_kv_heads=2)
+    di.context_lens[::89] = 0
+    out = fa.paged_decode(di.q, di.k_cache, di.v_cache, di.block_tables, di.context_lens,
+                          di.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    assert (out[::89] == 0).all()
+    sel = torch.tensor(list(range(3, S, 67)), device=DEV)
+    ref, _ = oracle.paged_decode(di.q[sel], di.k_cache, di.v_cache, di.block_tables[sel],
+                                 di.context_lens[sel], di.scale)
+    assert np.abs(out[sel].float().cpu().numpy() - ref).max() <= TOL
+    fa.fa_decode_gqa_select(3 - impl)
+    other = fa.paged_decode(di.q, di.k_cache, di.v_cache, di.block_tables, di.context_lens,
+                            di.scale)
+    fa.fa_decode_gqa_select(impl)
+    torch.cuda.synchronize()
+    assert (out.float() - other.float()).abs().max().item() <= TOL
+
+
 def test_gqa_decode_ignores_cache_slots_past_the_context(impl):
     """Slots past a sequence's context (the tail of its last block, and blocks
     it does not use) may hold anything: NaN there changes no output bit."""
