@@ -169,13 +169,12 @@ def test_fp8_forward_with_transform_on_outliers():
     assert e_plain > 1.2 * e_rot, (e_plain, e_rot)
 
 
-def test_fp8_forward_benchmark_shape_sampled_rows():
-    """2 x 16 x 4096 x 128 causal, the benchmark's forward shape; 48 sampled
-    rows per head plus the first and last are checked."""
+def test_fp8_forward_benchmark_shape_full():
+    """2 x 16 x 4096 x 128 causal, the benchmark's forward shape: every row of
+    every head against the oracle's bounds."""
     B, H, N, d = 2, 16, 4096, 128
     q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=3)
-    rows = sorted(set(inputs.sample_rows(N, 48, seed=N).tolist()) | {0, N - 1})
-    _check_forward(q, k, v, True, rows=np.asarray(rows))
+    _check_forward(q, k, v, True)
 
 
 def test_fp8_distance_from_bf16_is_the_quantization_error():
