@@ -476,11 +476,13 @@ int fa_backward(const void *q, const void *k, const void *v, const void *o, cons
   // The preparation kernel runs 16 padded rows per block of its 1-D grid.
   if ((long long)BH * ((N + 127) / 128) * 8 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   int dev = 0;
+  int *sched = nullptr;
   CUtensorMap tq, tk, tv, tdo, tdq;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if ((rc = current_device(&dev)) != FA_OK) return rc;
     if ((rc = get_encoder()) != FA_OK) return rc;
+    sched = sched_slot(g_dev[dev], reinterpret_cast<cudaStream_t>(stream));
   }
   const int qdo_rows = fattn::bwd_qdo_box_rows(d);
   if ((rc = encode_qkv_map(&tq, q, BH, N, d, qdo_rows)) != FA_OK) return rc;
@@ -491,7 +493,7 @@ int fa_backward(const void *q, const void *k, const void *v, const void *o, cons
   return cuda_status(fattn::launch_bwd_bf16(tq, tk, tv, tdo, tdq, o, dout, lse, dq, dk, dv, BH,
                                             N, d,
                                             scale, causal ? 1 : 0,
-                                            reinterpret_cast<float *>(workspace),
+                                            reinterpret_cast<float *>(workspace), sched,
                                             g_dev[dev].status,
                                             reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -27,6 +27,16 @@
 // MMA order per sub-tile: dQ'_t, dV_t, dK_t, then S_t, dP_t of the next step
 // (after group t has released R_t), then the other sub-tile.  Q and dO
 // arrive as 64-row halves through 4-slot rings, two steps ahead.
+//
+// The CTAs are persistent (one per SM): the producer claims (key block,
+// head) items from a device-wide counter, heaviest first, and hands them to
+// the other roles through a two-entry ring in shared memory.  Every barrier
+// keeps counting across items.  At an item boundary the producer loads the
+// next item's first Q and dO halves as soon as ring slots free up and its K
+// and V once the last MMA of the current item has read theirs; the MMA warp
+// starts the next item's first S and dP while the groups write the current
+// item's dV and dK, and its first dV, dK products wait only for the groups
+// to have read those accumulators out of TMEM.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -66,7 +76,7 @@ constexpr int kDSBytes = BM * BH_ * 2;               // 16 KB
 constexpr int kOffVec = kOffDS + 2 * kDSBytes;       // kSlots x [LSE2 64 | D 64] f32
 constexpr int kVecBytes = 2 * BH_ * 4;               // 512 B
 constexpr int kOffBar = kOffVec + kSlots * kVecBytes;
-constexpr int kSmemBytes = kOffBar + 256;
+constexpr int kSmemBytes = kOffBar + 512;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 enum : int {
@@ -79,16 +89,22 @@ enum : int {
   kBarPReady = 19,      // + t, 4 warps
   kBarDQFull = 21,      // + t
   kBarTmemFree = 23,    // + t, 4 warps: dQ'_t read out of TMEM
-  kBarKVDone = 25,
+  kBarKVDone = 25,      // every MMA of the item is complete (K, V free; dV, dK final)
   kBarDrain = 26,
-  kNumBars = 27
+  kBarEpiDone = 27,     // 8 warps: the item's dV, dK have been read out of TMEM
+  kBarItemFull = 28,    // + ring slot (2)
+  kBarItemEmpty = 30,   // + ring slot (2)
+  kNumBars = 32
 };
-static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
+// Arrivals that free an item-ring slot: the MMA thread and the 8 group warps.
+constexpr int kItemConsumers = 1 + 8;
 
 struct Misc {
   uint32_t tmem_base;
   int abort;
+  int item[2];
 };
+static_assert(kNumBars * 8 + sizeof(Misc) <= 512, "barrier area");
 
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t ph, volatile int *abort_flag) {
   return __all_sync(~0u, mbar_wait(bar, ph, abort_flag));
@@ -104,13 +120,28 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t ph) {
 // boundary (the layout above assumes it; the kernel then does nothing).
 constexpr int kDevBadSmemBase = -2;
 
+// An item: key block jb of head bh (items heaviest first: under the causal
+// mask key block 0 is visited by every query block).
+struct BwdItem {
+  int jb, bh, k0, i_first, n_steps, n_halves;
+  __device__ void decode(int w, int BH, int n_qb, int causal) {
+    jb = w / BH;
+    bh = w - jb * BH;
+    k0 = jb * BM;
+    i_first = causal ? jb : 0;
+    n_steps = n_qb - i_first;
+    n_halves = 2 * n_steps;
+  }
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_pipe_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dq,
                     const float *__restrict__ vecs,
                     __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int N, int BH,
-                    float scale, int causal, int *__restrict__ dev_status) {
+                    float scale, int causal, int *__restrict__ sched,
+                    int *__restrict__ dev_status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t s_base = smem_u32(smem);
   if ((s_base & 1023u) != 0) {
@@ -121,14 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return bars + 8u * i; };
   Misc *misc = reinterpret_cast<Misc *>(smem + kOffBar + 8 * kNumBars);
   volatile int *abort_flag = &misc->abort;
-
-  const int jb = static_cast<int>(blockIdx.x) / BH;   // heaviest key blocks first
-  const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int k0 = jb * BM;
   const int n_qb = (N + BQ - 1) / BQ;
-  const int i_first = causal ? jb : 0;
-  const int n_steps = n_qb - i_first;
-  const int n_halves = 2 * n_steps;
+  const int n_items = n_qb * BH;
 
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
@@ -144,9 +169,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarPReady + t), 4);
       mbar_init(bar(kBarDQFull + t), 1);
       mbar_init(bar(kBarTmemFree + t), 4);
+      mbar_init(bar(kBarItemFull + t), 1);
+      mbar_init(bar(kBarItemEmpty + t), kItemConsumers);
     }
     mbar_init(bar(kBarKVDone), 1);
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarEpiDone), 8);
     misc->abort = 0;
     fence_barrier_init();
   }
@@ -164,6 +192,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+  // Consumer side of the item ring: waits for entry k and frees it (one
+  // arrival per warp, or the lone MMA thread).
+  auto fetch_item = [&](int k, int &w, bool whole_warp) -> bool {
+    const int slot = k & 1;
+    if (!mbar_wait(bar(kBarItemFull + slot), (k >> 1) & 1, abort_flag)) return false;
+    w = *reinterpret_cast<volatile int *>(&misc->item[slot]);
+    if (whole_warp) __syncwarp();
+    if (!whole_warp || (threadIdx.x & 31) == 0) mbar_arrive(bar(kBarItemEmpty + slot));
+    return true;
+  };
+
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLoad));
     if (warp == 0 && elect_one()) {
@@ -172,40 +211,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(bar(kBarKV), 2 * kTile);
-      for (int b = 0; b < 2; ++b) {
-        tma_load_3d(s_base + kOffK + b * kKeyBox, &tm_k, b * 64, k0, bh, bar(kBarKV));
-        tma_load_3d(s_base + kOffV + b * kKeyBox, &tm_v, b * 64, k0, bh, bar(kBarKV));
-      }
-      int nq = 0, ndo = 0;
+      int nq = 0, ndo = 0, nkv = 0;   // halves (and K/V pairs) issued so far
       bool ok = true;
-      for (int h = 0; h < n_halves && ok; ++h) {
-        const int slot = h % kSlots, use = h / kSlots;
-        const int qb = i_first + (h >> 1);
-        const int qrow = qb * BQ + (h & 1) * BH_;
-        if (!(ok = mbar_wait(bar(kBarQEmpty + slot), (use & 1) ^ 1, abort_flag))) break;
-        mbar_arrive_expect_tx(bar(kBarQFull + slot), kHalf + kVecBytes);
-        for (int b = 0; b < 2; ++b)
-          tma_load_3d(s_base + kOffQ + slot * kHalf + b * kHalfBox, &tm_q, b * 64, qrow, bh,
-                      bar(kBarQFull + slot));
-        const float *vsrc = vecs + (static_cast<int64_t>(bh) * n_qb + qb) * (2 * BQ) + (h & 1) * BH_;
-        bulk_load(s_base + kOffVec + slot * kVecBytes, vsrc, BH_ * 4, bar(kBarQFull + slot));
-        bulk_load(s_base + kOffVec + slot * kVecBytes + BH_ * 4, vsrc + BQ, BH_ * 4,
-                  bar(kBarQFull + slot));
-        nq = h + 1;
-        if (!(ok = mbar_wait(bar(kBarDOEmpty + slot), (use & 1) ^ 1, abort_flag))) break;
-        mbar_arrive_expect_tx(bar(kBarDOFull + slot), kHalf);
-        for (int b = 0; b < 2; ++b)
-          tma_load_3d(s_base + kOffDO + slot * kHalf + b * kHalfBox, &tm_do, b * 64, qrow, bh,
-                      bar(kBarDOFull + slot));
-        ndo = h + 1;
+      for (int k = 0; ok; ++k) {
+        const int islot = k & 1;
+        if (!(ok = mbar_wait(bar(kBarItemEmpty + islot), ((k >> 1) & 1) ^ 1, abort_flag))) break;
+        const int w = atomicAdd(sched, 1);
+        misc->item[islot] = w;
+        mbar_arrive(bar(kBarItemFull + islot));
+        if (w >= n_items) break;
+        BwdItem it;
+        it.decode(w, BH, n_qb, causal);
+        const int h_base = nq;
+        // Q / dO half h of the item (with its [LSE2 | D] vectors on QFull).
+        auto load_half = [&](int h) -> bool {
+          const int g = h_base + h, slot = g % kSlots, use = g / kSlots;
+          const int qb = it.i_first + (h >> 1);
+          const int qrow = qb * BQ + (h & 1) * BH_;
+          if (!mbar_wait(bar(kBarQEmpty + slot), (use & 1) ^ 1, abort_flag)) return false;
+          mbar_arrive_expect_tx(bar(kBarQFull + slot), kHalf + kVecBytes);
+          for (int b = 0; b < 2; ++b)
+            tma_load_3d(s_base + kOffQ + slot * kHalf + b * kHalfBox, &tm_q, b * 64, qrow, it.bh,
+                        bar(kBarQFull + slot));
+          const float *vsrc =
+              vecs + (static_cast<int64_t>(it.bh) * n_qb + qb) * (2 * BQ) + (h & 1) * BH_;
+          bulk_load(s_base + kOffVec + slot * kVecBytes, vsrc, BH_ * 4, bar(kBarQFull + slot));
+          bulk_load(s_base + kOffVec + slot * kVecBytes + BH_ * 4, vsrc + BQ, BH_ * 4,
+                    bar(kBarQFull + slot));
+          nq = g + 1;
+          if (!mbar_wait(bar(kBarDOEmpty + slot), (use & 1) ^ 1, abort_flag)) return false;
+          mbar_arrive_expect_tx(bar(kBarDOFull + slot), kHalf);
+          for (int b = 0; b < 2; ++b)
+            tma_load_3d(s_base + kOffDO + slot * kHalf + b * kHalfBox, &tm_do, b * 64, qrow, it.bh,
+                        bar(kBarDOFull + slot));
+          ndo = g + 1;
+          return true;
+        };
+        // The first two halves as soon as ring slots free up; K and V once
+        // the previous item's last MMA has read them.
+        for (int h = 0; h < 2 && h < it.n_halves && ok; ++h) ok = load_half(h);
+        if (!ok) break;
+        if (k > 0 && !(ok = mbar_wait(bar(kBarKVDone), (k - 1) & 1, abort_flag))) break;
+        mbar_arrive_expect_tx(bar(kBarKV), 2 * kTile);
+        for (int b = 0; b < 2; ++b) {
+          tma_load_3d(s_base + kOffK + b * kKeyBox, &tm_k, b * 64, it.k0, it.bh, bar(kBarKV));
+          tma_load_3d(s_base + kOffV + b * kKeyBox, &tm_v, b * 64, it.k0, it.bh, bar(kBarKV));
+        }
+        nkv = k + 1;
+        for (int h = 2; h < it.n_halves && ok; ++h) ok = load_half(h);
       }
       if (!ok) {
-        drain_wait(bar(kBarKV), 0);
-        for (int h = (nq > kSlots ? nq - kSlots : 0); h < nq; ++h)
-          drain_wait(bar(kBarQFull + h % kSlots), (h / kSlots) & 1);
-        for (int h = (ndo > kSlots ? ndo - kSlots : 0); h < ndo; ++h)
-          drain_wait(bar(kBarDOFull + h % kSlots), (h / kSlots) & 1);
+        if (nkv > 0) drain_wait(bar(kBarKV), (nkv - 1) & 1);
+        for (int g = (nq > kSlots ? nq - kSlots : 0); g < nq; ++g)
+          drain_wait(bar(kBarQFull + g % kSlots), (g / kSlots) & 1);
+        for (int g = (ndo > kSlots ? ndo - kSlots : 0); g < ndo; ++g)
+          drain_wait(bar(kBarDOFull + g % kSlots), (g / kSlots) & 1);
       }
     } else if (warp == 1 && elect_one()) {
       // ---------------------------------------------------------- MMA issuer
@@ -223,10 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t do_kmaj = sdesc_lo(s_base + kOffDO, 16);
       const uint32_t do_mn = sdesc_lo(s_base + kOffDO, kHalfBox);
       const uint32_t ds_mn = sdesc_lo(s_base + kOffDS, kDSBytes); // dS^T as B
-      // S_t^T = K Q_t^T and dP_t^T = V dO_t^T of half h into R_t.
-      auto issue_sdp = [&](int h) {
+      // S_t^T = K Q_t^T and dP_t^T = V dO_t^T of ring half g into R_{h & 1}.
+      auto issue_sdp = [&](int h, int g) {
         const uint32_t R = tmem + 128u * (h & 1);
-        const uint32_t so = static_cast<uint32_t>((h % kSlots) * kHalf) >> 4;
+        const uint32_t so = static_cast<uint32_t>((g % kSlots) * kHalf) >> 4;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ok_ = static_cast<uint32_t>((kk >> 2) * kKeyBox + (kk & 3) * 32) >> 4;
@@ -236,49 +296,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar(kBarSFull + (h & 1)));
       };
-      bool ok = mbar_wait(bar(kBarKV), 0, abort_flag);
-      for (int h = 0; h < 2 && h < n_halves && ok; ++h) {
-        if (!(ok = mbar_wait(bar(kBarQFull + h), 0, abort_flag))) break;
-        if (!(ok = mbar_wait(bar(kBarDOFull + h), 0, abort_flag))) break;
-        tc_fence_after();
-        issue_sdp(h);
-      }
-      for (int h = 0; h < n_halves && ok; ++h) {
-        const int t = h & 1, i = h >> 1, slot = h % kSlots;
-        const uint32_t R = tmem + 128u * t;
-        if (!(ok = mbar_wait(bar(kBarPReady + t), i & 1, abort_flag))) break;
-        tc_fence_after();
-        // dQ_t'^T = K^T dS_t^T: M = d, N = 64 queries, K = 128 keys.
-        const uint32_t dso = static_cast<uint32_t>(t * kDSBytes) >> 4;
-#pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk) {
-          const uint32_t off = static_cast<uint32_t>(kk * 2048) >> 4;
-          mma_ss_lo(R + 64, k_mn + off, ds_mn + dso + off, idesc_q, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(kBarDQFull + t));
-        // dV += P_t^T dO_t, dK += dS_t^T Q_t (A operands from TMEM); K = 64
-        // queries.
-        const uint32_t so = static_cast<uint32_t>(slot * kHalf) >> 4;
-#pragma unroll
-        for (int kk = 0; kk < BH_ / 16; ++kk) {
-          const uint32_t ob = so + (static_cast<uint32_t>(kk * 2048) >> 4);
-          const uint32_t acc = (h > 0 || kk > 0) ? 1u : 0u;
-          mma_ts_lo(tmem + 256, R + kk * 8, do_mn + ob, idesc_g, acc);
-          mma_ts_lo(tmem + 256 + D, R + 32 + kk * 8, q_mn + ob, idesc_g, acc);
-        }
-        mma_commit(bar(kBarQEmpty + slot));
-        mma_commit(bar(kBarDOEmpty + slot));
-        const int h2 = h + 2;
-        if (h2 < n_halves) {
-          const int s2 = h2 % kSlots;
-          if (!(ok = mbar_wait(bar(kBarTmemFree + t), i & 1, abort_flag))) break;
-          if (!(ok = mbar_wait(bar(kBarQFull + s2), (h2 / kSlots) & 1, abort_flag))) break;
-          if (!(ok = mbar_wait(bar(kBarDOFull + s2), (h2 / kSlots) & 1, abort_flag))) break;
+      bool ok = true;
+      int g0 = 0;       // ring halves of the earlier items
+      int steps = 0;    // steps (per sub-tile) of the earlier items
+      for (int k = 0; ok; ++k) {
+        int w;
+        if (!(ok = fetch_item(k, w, false)) || w >= n_items) break;
+        BwdItem it;
+        it.decode(w, BH, n_qb, causal);
+        if (!(ok = mbar_wait(bar(kBarKV), k & 1, abort_flag))) break;
+        // The item's first S_t, dP_t: R_t must have been read out (the dQ'_t
+        // of the previous item's last step).
+        for (int h = 0; h < 2 && h < it.n_halves && ok; ++h) {
+          const int g = g0 + h;
+          if (steps > 0 && !(ok = mbar_wait(bar(kBarTmemFree + h), (steps - 1) & 1, abort_flag)))
+            break;
+          if (!(ok = mbar_wait(bar(kBarQFull + g % kSlots), (g / kSlots) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(bar(kBarDOFull + g % kSlots), (g / kSlots) & 1, abort_flag))) break;
           tc_fence_after();
-          issue_sdp(h2);
+          issue_sdp(h, g);
         }
+        for (int h = 0; h < it.n_halves && ok; ++h) {
+          const int t = h & 1, st = steps + (h >> 1), g = g0 + h, slot = g % kSlots;
+          const uint32_t R = tmem + 128u * t;
+          if (!(ok = mbar_wait(bar(kBarPReady + t), st & 1, abort_flag))) break;
+          tc_fence_after();
+          // dQ_t'^T = K^T dS_t^T: M = d, N = 64 queries, K = 128 keys.
+          const uint32_t dso = static_cast<uint32_t>(t * kDSBytes) >> 4;
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk) {
+            const uint32_t off = static_cast<uint32_t>(kk * 2048) >> 4;
+            mma_ss_lo(R + 64, k_mn + off, ds_mn + dso + off, idesc_q, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(kBarDQFull + t));
+          // The previous item's dV, dK must have left TMEM before the first
+          // product of this one overwrites them.
+          if (h == 0 && k > 0) {
+            if (!(ok = mbar_wait(bar(kBarEpiDone), (k - 1) & 1, abort_flag))) break;
+            tc_fence_after();
+          }
+          // dV += P_t^T dO_t, dK += dS_t^T Q_t (A operands from TMEM); K = 64
+          // queries.
+          const uint32_t so = static_cast<uint32_t>(slot * kHalf) >> 4;
+#pragma unroll
+          for (int kk = 0; kk < BH_ / 16; ++kk) {
+            const uint32_t ob = so + (static_cast<uint32_t>(kk * 2048) >> 4);
+            const uint32_t acc = (h > 0 || kk > 0) ? 1u : 0u;
+            mma_ts_lo(tmem + 256, R + kk * 8, do_mn + ob, idesc_g, acc);
+            mma_ts_lo(tmem + 256 + D, R + 32 + kk * 8, q_mn + ob, idesc_g, acc);
+          }
+          mma_commit(bar(kBarQEmpty + slot));
+          mma_commit(bar(kBarDOEmpty + slot));
+          const int h2 = h + 2;
+          if (h2 < it.n_halves) {
+            const int g2 = g0 + h2;
+            if (!(ok = mbar_wait(bar(kBarTmemFree + t), st & 1, abort_flag))) break;
+            if (!(ok = mbar_wait(bar(kBarQFull + g2 % kSlots), (g2 / kSlots) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait(bar(kBarDOFull + g2 % kSlots), (g2 / kSlots) & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_sdp(h2, g2);
+          }
+        }
+        if (ok) mma_commit(bar(kBarKVDone));
+        g0 += it.n_halves;
+        steps += it.n_steps;
       }
-      if (ok) mma_commit(bar(kBarKVDone));
       mma_commit(bar(kBarDrain));
       drain_wait(bar(kBarDrain), 0);
     }
@@ -291,50 +373,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;        // key row of S^T, dP^T; d row of dQ'^T
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t R = tmem + lane_off + 128u * t;
-    const int key = k0 + r;
     const uint64_t c2 = f2(scale * kLog2e, scale * kLog2e);
     uint8_t *ds_buf = smem + kOffDS + t * kDSBytes;
+    // This warp's quarter of the dS^T buffer: staging of its dQ' boxes and
+    // of its dV / dK rows.
+    uint8_t *stg = ds_buf + quarter * 4096;
+    const uint32_t stg_u32 = s_base + kOffDS + t * kDSBytes + quarter * 4096;
     bool ok = true;
-    for (int i = 0; i < n_steps && ok; ++i) {
-      const int h = 2 * i + t, slot = h % kSlots;
-      const int q0 = (i_first + i) * BQ + t * BH_;   // first query of the sub-tile
-      if (!(ok = wait_warp(bar(kBarSFull + t), i & 1, abort_flag))) break;
-      // [LSE2 | D] of the sub-tile came with Q_t on QFull, which S_t needed.
-      if (!(ok = wait_warp(bar(kBarQFull + slot), (h / kSlots) & 1, abort_flag))) break;
-      tc_fence_after();
-      const float *vec = reinterpret_cast<const float *>(smem + kOffVec + slot * kVecBytes);
-      // Masking is needed only where a key of this warp is past N or, on the
-      // diagonal block, later than a query (warp-uniform).
-      const bool diag = causal && (q0 < k0 + BM) && (q0 + BH_ > k0);
-      const bool masked = diag || (k0 + quarter * 32 + 31 >= N);
-      if (masked)
-        bwd_tile::chunks<true>(R, vec, ds_buf, r, key, q0, N, diag, c2);
-      else
-        bwd_tile::chunks<false>(R, vec, ds_buf, r, key, q0, N, diag, c2);
-      tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPReady + t));
+    int g0 = 0, steps = 0;
+    for (int k = 0; ok; ++k) {
+      int w;
+      if (!(ok = fetch_item(k, w, true)) || w >= n_items) break;
+      BwdItem it;
+      it.decode(w, BH, n_qb, causal);
+      const int key = it.k0 + r;
+      for (int i = 0; i < it.n_steps && ok; ++i) {
+        const int h = 2 * i + t, st = steps + i, g = g0 + h, slot = g % kSlots;
+        const int q0 = (it.i_first + i) * BQ + t * BH_;   // first query of the sub-tile
+        if (!(ok = wait_warp(bar(kBarSFull + t), st & 1, abort_flag))) break;
+        // [LSE2 | D] of the sub-tile came with Q_t on QFull, which S_t needed.
+        if (!(ok = wait_warp(bar(kBarQFull + slot), (g / kSlots) & 1, abort_flag))) break;
+        tc_fence_after();
+        const float *vec = reinterpret_cast<const float *>(smem + kOffVec + slot * kVecBytes);
+        // Masking is needed only where a key of this warp is past N or, on the
+        // diagonal block, later than a query (warp-uniform).
+        const bool diag = causal && (q0 < it.k0 + BM) && (q0 + BH_ > it.k0);
+        const bool masked = diag || (it.k0 + quarter * 32 + 31 >= N);
+        if (masked)
+          bwd_tile::chunks<true>(R, vec, ds_buf, r, key, q0, N, diag, c2);
+        else
+          bwd_tile::chunks<false>(R, vec, ds_buf, r, key, q0, N, diag, c2);
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarPReady + t));
 
-      // dQ_t'^T row d = r: 64 query columns, read out, then R_t is released.
-      if (!(ok = wait_warp(bar(kBarDQFull + t), i & 1, abort_flag))) break;
-      tc_fence_after();
-      uint32_t g0[32], g1[32];
-      tmem_ld32(R + 64, g0);
-      tmem_ld32(R + 96, g1);
-      tmem_wait_ld(g0);
-      tmem_wait_ld(g1);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarTmemFree + t));
-      // Add into the row-major accumulator with TMA reduces: this warp's
-      // quarter of the dS^T buffer (its own key rows, free now that dQ'^T,
-      // which read it, is complete) stages one 32-query x 32-d box at a time
-      // as [query][d] fp32 rows with the 128-byte swizzle.
-      {
-        uint8_t *stg = ds_buf + quarter * 4096;
-        const uint32_t stg_u32 = s_base + kOffDS + t * kDSBytes + quarter * 4096;
+        // dQ_t'^T row d = r: 64 query columns, read out, then R_t is released.
+        if (!(ok = wait_warp(bar(kBarDQFull + t), st & 1, abort_flag))) break;
+        tc_fence_after();
+        uint32_t g0v[32], g1v[32];
+        tmem_ld32(R + 64, g0v);
+        tmem_ld32(R + 96, g1v);
+        tmem_wait_ld(g0v);
+        tmem_wait_ld(g1v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarTmemFree + t));
+        // Add into the row-major accumulator with TMA reduces: this warp's
+        // quarter of the dS^T buffer (its own key rows, free now that dQ'^T,
+        // which read it, is complete) stages one 32-query x 32-d box at a time
+        // as [query][d] fp32 rows with the 128-byte swizzle.
 #pragma unroll
         for (int bx = 0; bx < 2; ++bx) {
           if (bx == 1) {
@@ -344,11 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int qq = 0; qq < 32; ++qq)
             *reinterpret_cast<uint32_t *>(stg + qq * 128 + ((((lane >> 2) ^ (qq & 7))) << 4) +
-                                          (lane & 3) * 4) = bx ? g1[qq] : g0[qq];
+                                          (lane & 3) * 4) = bx ? g1v[qq] : g0v[qq];
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add_3d(&tm_dq, stg_u32, 32 * quarter, q0 + 32 * bx, bh);
+            tma_reduce_add_3d(&tm_dq, stg_u32, 32 * quarter, q0 + 32 * bx, it.bh);
             bulk_commit();
           }
         }
@@ -356,50 +445,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
       }
-    }
+      if (!ok) break;
 
-    // Epilogue: group 0 writes dV_j, group 1 dK_j = scale * (dS^T Q), as bf16
-    // rows (rows >= N are not stored).
-    if (ok) ok = wait_warp(bar(kBarKVDone), 0, abort_flag);
-    if (ok) {
+      // Epilogue: group 0 writes dV_j, group 1 dK_j = scale * (dS^T Q), as
+      // bf16 rows (rows >= N are not stored).  Both 64-column halves are
+      // read out of TMEM first, so the MMA warp may start the next item's
+      // products into them while the rows are stored.
+      if (!(ok = wait_warp(bar(kBarKVDone), k & 1, abort_flag))) break;
       tc_fence_after();
-      __nv_bfloat16 *base = (t ? dk : dv) + static_cast<int64_t>(bh) * N * D;
+      __nv_bfloat16 *base = (t ? dk : dv) + static_cast<int64_t>(it.bh) * N * D;
       const float mul = t ? scale : 1.f;
       const uint32_t col = t ? 256u + D : 256u;
-      // The rows leave through shared memory (the Q ring is idle now: every
-      // MMA that read it has completed), 64 columns at a time: each warp packs
-      // its 32 rows into 4 KB (16-byte chunks swizzled by the row) and reads
-      // them back so that eight lanes store one row's 128 contiguous bytes.
-      uint8_t *stg = smem + kOffQ + (t * 4 + quarter) * 4096;
-      const int key_w = key - lane;   // this warp's first key row
-#pragma unroll 1
-      for (int h = 0; h < D / 64; ++h) {
-        uint32_t v[2][32];
-        tmem_ld32(tmem + lane_off + col + 64 * h, v[0]);
-        tmem_ld32(tmem + lane_off + col + 64 * h + 32, v[1]);
-        tmem_wait_ld(v[0]);
-        tmem_wait_ld(v[1]);
+      uint32_t v[4][32];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t *c8 = &v[k >> 2][(k & 3) * 8];
+      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + col + 32 * c, v[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_wait_ld(v[c]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarEpiDone));
+      // The rows leave through this warp's staging quarter, 64 columns at a
+      // time: the warp packs its 32 rows into 4 KB (16-byte chunks swizzled by
+      // the row) and reads them back so that eight lanes store one row's 128
+      // contiguous bytes.
+      const int key_w = key - lane;   // this warp's first key row
+#pragma unroll
+      for (int hh = 0; hh < D / 64; ++hh) {
+#pragma unroll
+        for (int kq = 0; kq < 8; ++kq) {
+          const uint32_t *c8 = &v[2 * hh + (kq >> 2)][(kq & 3) * 8];
           uint4 x;
           x.x = pack_bf16x2(__uint_as_float(c8[0]) * mul, __uint_as_float(c8[1]) * mul);
           x.y = pack_bf16x2(__uint_as_float(c8[2]) * mul, __uint_as_float(c8[3]) * mul);
           x.z = pack_bf16x2(__uint_as_float(c8[4]) * mul, __uint_as_float(c8[5]) * mul);
           x.w = pack_bf16x2(__uint_as_float(c8[6]) * mul, __uint_as_float(c8[7]) * mul);
-          *reinterpret_cast<uint4 *>(stg + lane * 128 + ((k ^ (lane & 7)) * 16)) = x;
+          *reinterpret_cast<uint4 *>(stg + lane * 128 + ((kq ^ (lane & 7)) * 16)) = x;
         }
         __syncwarp();
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int rr = (lane >> 3) + 4 * k, ch = lane & 7;
+        for (int kq = 0; kq < 8; ++kq) {
+          const int rr = (lane >> 3) + 4 * kq, ch = lane & 7;
           const uint4 x = *reinterpret_cast<const uint4 *>(stg + rr * 128 + ((ch ^ (rr & 7)) * 16));
           if (key_w + rr < N)
-            *reinterpret_cast<uint4 *>(base + static_cast<int64_t>(key_w + rr) * D + 64 * h +
+            *reinterpret_cast<uint4 *>(base + static_cast<int64_t>(key_w + rr) * D + 64 * hh +
                                        ch * 8) = x;
         }
         __syncwarp();
       }
+      g0 += it.n_halves;
+      steps += it.n_steps;
     }
   }
 
@@ -410,7 +504,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (threadIdx.x == 0 && misc->abort) atomicExch(dev_status, kDevTimeout);
+  if (threadIdx.x == 0) {
+    if (misc->abort) atomicExch(dev_status, kDevTimeout);
+    // The last CTA to finish puts the launch's work counters back to zero.
+    __threadfence();
+    if (atomicAdd(sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      sched[0] = 0;
+      sched[1] = 0;
+      __threadfence();
+    }
+  }
 }
 
 }  // namespace
@@ -419,14 +522,19 @@ cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
                                  const CUtensorMap &tv, const CUtensorMap &tdo64,
                                  const CUtensorMap &tdq,
                                  const float *vecs, void *dk, void *dv, int BH,
-                                 int N, float scale, int causal, int *dev_status,
+                                 int N, float scale, int causal, int *sched, int *dev_status,
                                  cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(bwd_pipe_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
+  int dev = 0, n_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
   const int n_qb = (N + BQ - 1) / BQ;
+  const long long n_items = static_cast<long long>(n_qb) * BH;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_qb * BH);
+  cfg.gridDim = dim3(static_cast<unsigned>(n_items < n_sm ? n_items : n_sm));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
@@ -437,7 +545,7 @@ cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, bwd_pipe_kernel, tq64, tk, tv, tdo64, tdq, vecs,
                             reinterpret_cast<__nv_bfloat16 *>(dk),
-                            reinterpret_cast<__nv_bfloat16 *>(dv), N, BH, scale, causal,
+                            reinterpret_cast<__nv_bfloat16 *>(dv), N, BH, scale, causal, sched,
                             dev_status);
 }
 

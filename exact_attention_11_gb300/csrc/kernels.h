@@ -80,15 +80,16 @@ cudaError_t launch_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             const CUtensorMap &tdo, const CUtensorMap &tdq, const void *o,
                             const void *dout, const float *lse, void *dq, void *dk, void *dv,
                             int BH, int N, int d, float scale, int causal, float *ws,
-                            int *dev_status, cudaStream_t stream);
+                            int *sched, int *dev_status, cudaStream_t stream);
 
 // The d = 128 main kernel (bwd_bf16_d128.cu); vecs = the [-LSE2 | -D]
-// blocks, tdq = the fp32 map of the row-major dQ accumulator (TMA reduces).
+// blocks, tdq = the fp32 map of the row-major dQ accumulator (TMA reduces);
+// sched = a pair of work counters kept at zero (persistent CTAs).
 cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
                                  const CUtensorMap &tv, const CUtensorMap &tdo64,
                                  const CUtensorMap &tdq, const float *vecs, void *dk, void *dv,
                                  int BH,
-                                 int N, float scale, int causal, int *dev_status,
+                                 int N, float scale, int causal, int *sched, int *dev_status,
                                  cudaStream_t stream);
 
 // The d = 64 main kernel (bwd_bf16_d64.cu); tdq = the accumulator's fp32 map
