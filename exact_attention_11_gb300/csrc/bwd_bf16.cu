@@ -124,7 +124,7 @@ cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     e = launch_bwd_main_d128(tq, tk, tv, tdo, tdq, vecs, dk, dv, BH, N, scale, causal, sched,
                              dev_status, stream);
   else
-    e = launch_bwd_main_d64(tq, tk, tv, tdo, tdq, vecs, dk, dv, BH, N, scale, causal,
+    e = launch_bwd_main_d64(tq, tk, tv, tdo, tdq, vecs, dk, dv, BH, N, scale, causal, sched,
                             dev_status, stream);
   if (e != cudaSuccess) return e;
   const int64_t n8 = rows * D / 8;

@@ -93,12 +93,12 @@ cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
                                  cudaStream_t stream);
 
 // The d = 64 main kernel (bwd_bf16_d64.cu); tdq = the accumulator's fp32 map
-// (its dQ' tiles are added with TMA reduces).
+// (its dQ' tiles are added with TMA reduces); sched as for d = 128.
 cudaError_t launch_bwd_main_d64(const CUtensorMap &tq64, const CUtensorMap &tk,
                                 const CUtensorMap &tv, const CUtensorMap &tdo64,
                                 const CUtensorMap &tdq, const float *vecs, void *dk, void *dv,
-                                int BH, int N, float scale, int causal, int *dev_status,
-                                cudaStream_t stream);
+                                int BH, int N, float scale, int causal, int *sched,
+                                int *dev_status, cudaStream_t stream);
 
 int decode_max_parts(int max_num_blocks_per_seq);
 // Grouped key/value heads (decode_gqa.cu): group = num_heads / num_kv_heads
