@@ -95,6 +95,44 @@ def test_backward_full_size_all_heads(d):
         _check_heads(q, k, v, do, grads, every[i:i + 8], d, True)
 
 
+@pytest.mark.parametrize("d,causal", [(128, False), (64, False), (128, True), (64, True)])
+def test_backward_several_items_per_cta(d, causal):
+    """4 x 16 x 1024: 512 (key block, head) items on at most one CTA per SM, so
+    each persistent CTA takes several in turn (items of different heads and
+    lengths back to back); 12 heads, from both ends of the item order, are
+    checked against the oracle."""
+    B, H, N = 4, 16, 1024
+    (q, k, v, do), grads = _run(B, H, N, d, causal, seed=11 + d)
+    heads = [(0, 0), (0, 1), (0, 15), (1, 3), (1, 8), (2, 0), (2, 9), (2, 14), (3, 2), (3, 7),
+             (3, 14), (3, 15)]
+    _check_heads(q, k, v, do, grads, heads, d, causal)
+
+
+def test_backward_two_streams_at_once():
+    """Two backward calls in flight at once on two streams (separate work
+    counters and workspaces), with no wait between the launches; both match
+    the oracle."""
+    cases = [(1, 3, 700, 128, True, 21), (2, 2, 900, 64, False, 22)]
+    prepared = []
+    for B, H, N, d, causal, seed in cases:
+        q, k, v = (t.to(DEV) for t in inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=seed))
+        do = inputs.grad_output(B, H, N, d, torch.bfloat16, seed=seed).to(DEV)
+        o, lse = fa.forward(q, k, v, causal=causal)
+        prepared.append((q, k, v, do, o, lse, d, causal))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for (q, k, v, do, o, lse, d, causal), st in zip(prepared, streams):
+        with torch.cuda.stream(st):
+            outs.append(fa.backward(q, k, v, o, lse, do, causal=causal))
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    for (q, k, v, do, o, lse, d, causal), grads in zip(prepared, outs):
+        ref = oracle.attention_backward(q.cpu(), k.cpu(), v.cpu(), do.cpu(), d ** -0.5, causal)
+        for name, got, want in zip(("dQ", "dK", "dV"), grads, ref):
+            _compare(got.float().cpu().numpy(), want, name)
+
+
 def test_backward_writes_stay_inside_outputs():
     B, H, N, d = 1, 3, 333, 128
     q, k, v = (t.to(DEV) for t in inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=9))
