@@ -32,8 +32,8 @@
  * cudaFreeAsync), so a larger problem never synchronises the device; a call
  * being captured into a CUDA graph cannot grow them and returns
  * FA_ERR_UNSUPPORTED instead, so run one call of the largest size before
- * capturing.  The forward kernels and the tensor-core grouped decode take a
- * pair of work counters per launch: eager launches rotate through 64 pairs,
+ * capturing.  The forward kernels, the backward's main kernel and the
+ * tensor-core grouped decode take a pair of work counters per launch: eager launches rotate through 64 pairs,
  * launches captured into a graph through 64 others that a graph keeps for
  * every replay; so at most 64 eager calls may be in flight on a device at
  * once, and a graph must not run concurrently with itself.
