@@ -196,8 +196,8 @@ def fa_release() -> None:
 
 
 def fa_debug_inject_fault(mode: int) -> int:
-    """Test hook: arm (1) or disarm (0) a lost-copy fault in the next forward
-    launch on the current device (see fattn.h)."""
+    """Test hook: arm a lost-copy fault in the next forward (1) or backward
+    (2) launch on the current device, or disarm (0) (see fattn.h)."""
     return _check("fa_debug_inject_fault", load().fa_debug_inject_fault(mode))
 
 

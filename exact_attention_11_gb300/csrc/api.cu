@@ -35,7 +35,7 @@ struct DeviceState {
   const void *kv_maps_k = nullptr, *kv_maps_v = nullptr;
   int kv_maps_hk = 0;
   bool kv_maps_valid = false;
-  int inject_fault = 0;           // fa_debug_inject_fault: armed for the next forward
+  int inject_fault = 0;           // fa_debug_inject_fault: 1 next forward, 2 next backward
   int checked = 0;                // 1: sm_103 verified, -1: unsupported
 };
 
@@ -316,8 +316,8 @@ int forward16(const void *q, const void *k, const void *v, void *o, float *lse, 
     if ((rc = get_encoder()) != FA_OK) return rc;
     DeviceState &st = g_dev[dev];
     sched = sched_slot(st, reinterpret_cast<cudaStream_t>(stream));
-    fault_cta = st.inject_fault ? 0 : -1;
-    st.inject_fault = 0;
+    fault_cta = st.inject_fault == 1 ? 0 : -1;
+    if (st.inject_fault == 1) st.inject_fault = 0;
     if (mask != nullptr) {
       const size_t need = fattn::mask_summary_bytes(mask_heads, N);
       if ((rc = grow_on_stream(&st.mask_ws, &st.mask_ws_bytes, need,
@@ -475,7 +475,7 @@ int fa_backward(const void *q, const void *k, const void *v, const void *o, cons
   if (workspace_bytes < fattn::bwd_workspace_bytes(BH, N, d)) return FA_ERR_INVALID_ARG;
   // The preparation kernel runs 16 padded rows per block of its 1-D grid.
   if ((long long)BH * ((N + 127) / 128) * 8 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-  int dev = 0;
+  int dev = 0, fault_cta = -1;
   int *sched = nullptr;
   CUtensorMap tq, tk, tv, tdo, tdq;
   {
@@ -483,6 +483,10 @@ int fa_backward(const void *q, const void *k, const void *v, const void *o, cons
     if ((rc = current_device(&dev)) != FA_OK) return rc;
     if ((rc = get_encoder()) != FA_OK) return rc;
     sched = sched_slot(g_dev[dev], reinterpret_cast<cudaStream_t>(stream));
+    if (g_dev[dev].inject_fault == 2) {
+      fault_cta = 0;
+      g_dev[dev].inject_fault = 0;
+    }
   }
   const int qdo_rows = fattn::bwd_qdo_box_rows(d);
   if ((rc = encode_qkv_map(&tq, q, BH, N, d, qdo_rows)) != FA_OK) return rc;
@@ -494,7 +498,7 @@ int fa_backward(const void *q, const void *k, const void *v, const void *o, cons
                                             N, d,
                                             scale, causal ? 1 : 0,
                                             reinterpret_cast<float *>(workspace), sched,
-                                            g_dev[dev].status,
+                                            fault_cta, g_dev[dev].status,
                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -599,7 +603,7 @@ int fa_decode_gqa_select(int impl) {
 }
 
 int fa_debug_inject_fault(int mode) {
-  if (mode != 0 && mode != 1) return FA_ERR_INVALID_ARG;
+  if (mode != 0 && mode != 1 && mode != 2) return FA_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0, rc;
   if ((rc = current_device(&dev)) != FA_OK) return rc;

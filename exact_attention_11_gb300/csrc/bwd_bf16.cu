@@ -106,8 +106,8 @@ template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const CUtensorMap &tdo, const CUtensorMap &tdq, const void *o,
                          const void *dout, const float *lse, void *dq, void *dk, void *dv, int BH,
-                         int N, float scale, int causal, float *ws, int *sched, int *dev_status,
-                         cudaStream_t stream) {
+                         int N, float scale, int causal, float *ws, int *sched, int fault_cta,
+                         int *dev_status, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(BH) * N;
   const int n_qb = (N + BQ - 1) / BQ;
   const int64_t padded = static_cast<int64_t>(BH) * n_qb * BQ;
@@ -122,10 +122,10 @@ cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   // Q and dO maps have 64-row boxes (the main kernels' 64-query sub-tiles).
   if constexpr (D == 128)
     e = launch_bwd_main_d128(tq, tk, tv, tdo, tdq, vecs, dk, dv, BH, N, scale, causal, sched,
-                             dev_status, stream);
+                             fault_cta, dev_status, stream);
   else
     e = launch_bwd_main_d64(tq, tk, tv, tdo, tdq, vecs, dk, dv, BH, N, scale, causal, sched,
-                            dev_status, stream);
+                            fault_cta, dev_status, stream);
   if (e != cudaSuccess) return e;
   const int64_t n8 = rows * D / 8;
   cudaLaunchConfig_t cfg = {};
@@ -153,12 +153,12 @@ cudaError_t launch_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             const CUtensorMap &tdo, const CUtensorMap &tdq, const void *o,
                             const void *dout, const float *lse, void *dq, void *dk, void *dv,
                             int BH, int N, int d, float scale, int causal, float *ws,
-                            int *sched, int *dev_status, cudaStream_t stream) {
+                            int *sched, int fault_cta, int *dev_status, cudaStream_t stream) {
   if (d == 64)
     return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, o, dout, lse, dq, dk, dv, BH, N, scale, causal,
-                            ws, sched, dev_status, stream);
+                            ws, sched, fault_cta, dev_status, stream);
   return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, o, dout, lse, dq, dk, dv, BH, N, scale, causal,
-                           ws, sched, dev_status, stream);
+                           ws, sched, fault_cta, dev_status, stream);
 }
 
 }  // namespace fattn

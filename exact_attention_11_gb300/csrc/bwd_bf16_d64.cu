@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_do,
                       const __grid_constant__ CUtensorMap tm_dq, const float *__restrict__ vecs,
                       __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int N,
-                      int BH, float scale, int causal, int *__restrict__ sched,
+                      int BH, float scale, int causal, int *__restrict__ sched, int fault_cta,
                       int *__restrict__ dev_status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t s_base = smem_u32(smem);
@@ -249,6 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the previous item's last MMA has read them.
         for (int h = 0; h < 2 && h < it.n_halves && ok; ++h) ok = load_half(h);
         if (!ok) break;
+        if (static_cast<int>(blockIdx.x) == fault_cta) {
+          // Failure-path test: stop here, as if the K and V copies were lost;
+          // the MMA warp's bounded wait for them runs out.
+          ok = false;
+          break;
+        }
         if (k > 0 && !(ok = mbar_wait(bar(kBarKVDone), (k - 1) & 1, abort_flag))) break;
         mbar_arrive_expect_tx(bar(kBarKV), 2 * kTile);
         tma_load_3d(s_base + kOffK, &tm_k, 0, it.k0, it.bh, bar(kBarKV));
@@ -525,7 +531,7 @@ cudaError_t launch_bwd_main_d64(const CUtensorMap &tq64, const CUtensorMap &tk,
                                 const CUtensorMap &tv, const CUtensorMap &tdo64,
                                 const CUtensorMap &tdq, const float *vecs, void *dk, void *dv,
                                 int BH, int N, float scale, int causal, int *sched,
-                                int *dev_status, cudaStream_t stream) {
+                                int fault_cta, int *dev_status, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(bwd_pipe64_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -548,7 +554,7 @@ cudaError_t launch_bwd_main_d64(const CUtensorMap &tq64, const CUtensorMap &tk,
   return cudaLaunchKernelEx(&cfg, bwd_pipe64_kernel, tq64, tk, tv, tdo64, tdq, vecs,
                             reinterpret_cast<__nv_bfloat16 *>(dk),
                             reinterpret_cast<__nv_bfloat16 *>(dv), N, BH, scale, causal, sched,
-                            dev_status);
+                            fault_cta, dev_status);
 }
 
 }  // namespace fattn

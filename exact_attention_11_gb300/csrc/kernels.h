@@ -80,7 +80,7 @@ cudaError_t launch_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             const CUtensorMap &tdo, const CUtensorMap &tdq, const void *o,
                             const void *dout, const float *lse, void *dq, void *dk, void *dv,
                             int BH, int N, int d, float scale, int causal, float *ws,
-                            int *sched, int *dev_status, cudaStream_t stream);
+                            int *sched, int fault_cta, int *dev_status, cudaStream_t stream);
 
 // The d = 128 main kernel (bwd_bf16_d128.cu); vecs = the [-LSE2 | -D]
 // blocks, tdq = the fp32 map of the row-major dQ accumulator (TMA reduces);
@@ -89,8 +89,8 @@ cudaError_t launch_bwd_main_d128(const CUtensorMap &tq64, const CUtensorMap &tk,
                                  const CUtensorMap &tv, const CUtensorMap &tdo64,
                                  const CUtensorMap &tdq, const float *vecs, void *dk, void *dv,
                                  int BH,
-                                 int N, float scale, int causal, int *sched, int *dev_status,
-                                 cudaStream_t stream);
+                                 int N, float scale, int causal, int *sched, int fault_cta,
+                                 int *dev_status, cudaStream_t stream);
 
 // The d = 64 main kernel (bwd_bf16_d64.cu); tdq = the accumulator's fp32 map
 // (its dQ' tiles are added with TMA reduces); sched as for d = 128.
@@ -98,7 +98,7 @@ cudaError_t launch_bwd_main_d64(const CUtensorMap &tq64, const CUtensorMap &tk,
                                 const CUtensorMap &tv, const CUtensorMap &tdo64,
                                 const CUtensorMap &tdq, const float *vecs, void *dk, void *dv,
                                 int BH, int N, float scale, int causal, int *sched,
-                                int *dev_status, cudaStream_t stream);
+                                int fault_cta, int *dev_status, cudaStream_t stream);
 
 int decode_max_parts(int max_num_blocks_per_seq);
 // Grouped key/value heads (decode_gqa.cu): group = num_heads / num_kv_heads

@@ -366,8 +366,10 @@ int fa_paged_decode_noalloc(const void *q, const void *k_cache, const void *v_ca
  * missing key tile then runs out (after about 2 s), the CTA unwinds (in-flight
  * copies and MMAs drained, tensor memory freed) and fa_device_status()
  * returns FA_ERR_TIMEOUT.  That launch's output is incomplete; the CUDA
- * context and the library stay usable.  mode 0 disarms.  Returns FA_OK, or
- * FA_ERR_INVALID_ARG for another mode, or FA_ERR_NO_DEVICE.
+ * context and the library stay usable.  mode 2 does the same to the next
+ * fa_backward: its main kernel's first CTA loses the K and V copies of its
+ * first work item.  mode 0 disarms.  Returns FA_OK, or FA_ERR_INVALID_ARG
+ * for another mode, or FA_ERR_NO_DEVICE.
  */
 int fa_debug_inject_fault(int mode);
 
