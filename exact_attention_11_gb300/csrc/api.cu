@@ -341,14 +341,15 @@ int forward16(const void *q, const void *k, const void *v, void *o, float *lse, 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t *flags = nullptr;
   const int2 *ranges = nullptr;
+  const uint4 *bits = nullptr;
   if (mask != nullptr &&
       (rc = cuda_status(fattn::launch_mask_summary(mask, static_cast<int64_t>(mask_bh_stride), N,
-                                                   mask_heads, mask_ws, &flags, &ranges, s))) !=
-          FA_OK)
+                                                   mask_heads, mask_ws, &flags, &ranges, &bits,
+                                                   s))) != FA_OK)
     return rc;
   return cuda_status(launch_fwd_bf16(tq, tk, tv, o, lse, BH, N, d, scale, causal ? 1 : 0, sched,
                                      g_dev[dev].status, fault_cta, s, f16, mask,
-                                     static_cast<int64_t>(mask_bh_stride), ranges, flags));
+                                     static_cast<int64_t>(mask_bh_stride), ranges, flags, bits));
 }
 }  // namespace
 

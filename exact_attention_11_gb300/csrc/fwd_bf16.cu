@@ -188,7 +188,9 @@ struct ItemDecoder {
 // mask_ranges / mask_flags: the per-tile summary of mask_tiles.cu: per item
 // the key tiles its rows can see (the others are skipped), per 128 x 128
 // block a flag (0: nothing visible, 1: partly, 2: everything; a fully
-// visible tile reads no mask bytes).
+// visible tile reads no mask bytes), and mask_bits per row of each block its
+// 128 visibility bits, which a partly visible tile reads in place of the
+// row's 128 mask bytes.
 // FP8: E4M3 inputs (tm_v then maps V^T, [BH][d][Npad]); q_scale and k_scale
 // hold one dequantization scale per 128-row block of each head (n_sblk per
 // head), v_scale one per head.  The output is bf16.
@@ -203,7 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        int64_t mask_bh_stride, const float *__restrict__ q_scale,
                        const float *__restrict__ k_scale, const float *__restrict__ v_scale,
                        int n_sblk, const int2 *__restrict__ mask_ranges,
-                       const uint8_t *__restrict__ mask_flags) {
+                       const uint8_t *__restrict__ mask_flags,
+                       const uint4 *__restrict__ mask_bits) {
   using C = Cfg<D, FP8>;
   using SC = SoftmaxCfg<FP8>;
   static_assert(!FP8 || (D == 128 && !F16 && !MASK), "the FP8 variant is d = 128, unmasked");
@@ -528,9 +531,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // sequence end has no rows to keep: treat it as seeing nothing).
       const int n_t = (N + BM - 1) / BM;
       const int qt = q0 / BM + t;
-      const uint8_t *flag_row =
-          MASK ? mask_flags + (static_cast<int64_t>(mask_bh_stride ? bh : 0) * n_t + qt) * n_t
-               : nullptr;
+      const int64_t blk_row = (static_cast<int64_t>(mask_bh_stride ? bh : 0) * n_t + qt) * n_t;
+      const uint8_t *flag_row = MASK ? mask_flags + blk_row : nullptr;
+      const uint4 *bits_row = MASK ? mask_bits + blk_row * BM + r_local : nullptr;
       // FP8: the scores are raw code products; this tile's Q block scale (a
       // tile past the last block has no rows to keep) times each key tile's
       // scale turns them into scale * q.k.
@@ -540,27 +543,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (qblk < n_sblk) q_fac *= q_scale[static_cast<int64_t>(bh) * n_sblk + qblk];
       }
       float m = -INFINITY, l = 0.f;
+      // MASK: the block flag of key tile j + 1 is fetched one tile ahead (a
+      // tile past the sequence end sees nothing), so that at tile j only the
+      // row's 128 visibility bits, for a partly visible block, wait on a load;
+      // they are fetched before the wait for the scores.  Holding the bits
+      // themselves a tile ahead costs the softmax warps registers they spill.
+      int flag_nx = (MASK && n_mine > 0 && qt < n_t) ? flag_row[kv0] : 0;
       for (int j = 0; j < n_mine; ++j, ++sc) {
         const float c_tile =
             FP8 ? q_fac * k_scale[static_cast<int64_t>(bh) * n_sblk + j] : scale_log2;
-        // MASK: this row's 128 mask bytes for key tile j, fetched before the
-        // wait for the scores (chunks past N read as "not visible").
-        uint4 mk[8];
+        uint4 mk = make_uint4(0u, 0u, 0u, 0u);   // keys past N are not visible
         int flag = 1;
         if (MASK) {
-          flag = qt < n_t ? flag_row[kv0 + j] : 0;
-          if (flag == 1) {
-            const int kb0 = (kv0 + j) * BN;
-            const uint8_t *mr = mask + static_cast<int64_t>(bh) * mask_bh_stride +
-                                static_cast<int64_t>(min(row, N - 1)) * N + kb0;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              mk[c] = (kb0 + 16 * c < N) ? *reinterpret_cast<const uint4 *>(mr + 16 * c)
-                                         : make_uint4(0u, 0u, 0u, 0u);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) mk[c] = make_uint4(0u, 0u, 0u, 0u);   // nothing visible
-          }
+          flag = flag_nx;
+          if (flag == 1) mk = bits_row[static_cast<int64_t>(kv0 + j) * BM];
+          if (j + 1 < n_mine && qt < n_t) flag_nx = flag_row[kv0 + j + 1];
         }
         if (!(ok = mbar_wait(bar(kBarSFull + t), sc & 1, abort_flag))) break;
         tc_fence_after();
@@ -574,8 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (flag != 2) {   // a fully visible tile needs no mask
 #pragma unroll
             for (int c = 0; c < BN; ++c) {
-              const uint32_t w = (&mk[c >> 4].x)[(c >> 2) & 3];
-              if (((w >> (8 * (c & 3))) & 0xffu) == 0u) S_(c) = __float_as_uint(-INFINITY);
+              const uint32_t w = (&mk.x)[c >> 5];
+              if (((w >> (c & 31)) & 1u) == 0u) S_(c) = __float_as_uint(-INFINITY);
             }
           }
         } else if (j == n_mine - 1) {
@@ -759,7 +756,8 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
                      int *dev_status, int fault_cta, cudaStream_t stream, const uint8_t *mask,
                      int64_t mask_bh_stride, const float *q_scale = nullptr,
                      const float *k_scale = nullptr, const float *v_scale = nullptr,
-                     const int2 *mask_ranges = nullptr, const uint8_t *mask_flags = nullptr) {
+                     const int2 *mask_ranges = nullptr, const uint8_t *mask_flags = nullptr,
+                     const uint4 *mask_bits = nullptr) {
   using C = Cfg<D, FP8>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -796,7 +794,7 @@ cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
   return cudaLaunchKernelEx(&cfg, fwd_bf16_tc_kernel<D, F16, MASK, FP8>, tq, tk, tv,
                             reinterpret_cast<uint16_t *>(o), lse, N, BH, n_qblocks, scale_log2,
                             causal, sched, dev_status, fault_cta, mask, mask_bh_stride, q_scale,
-                            k_scale, v_scale, n_sblk, mask_ranges, mask_flags);
+                            k_scale, v_scale, n_sblk, mask_ranges, mask_flags, mask_bits);
 }
 
 }  // namespace
@@ -805,10 +803,11 @@ cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             void *o, float *lse, int BH, int N, int d, float scale, int causal,
                             int *sched, int *dev_status, int fault_cta, cudaStream_t stream,
                             bool f16, const uint8_t *mask, int64_t mask_bh_stride,
-                            const int2 *mask_ranges, const uint8_t *mask_flags) {
+                            const int2 *mask_ranges, const uint8_t *mask_flags,
+                            const uint4 *mask_bits) {
 #define FATTN_FWD_ARGS \
   tq, tk, tv, o, lse, BH, N, scale, causal, sched, dev_status, fault_cta, stream, mask, \
-      mask_bh_stride, nullptr, nullptr, nullptr, mask_ranges, mask_flags
+      mask_bh_stride, nullptr, nullptr, nullptr, mask_ranges, mask_flags, mask_bits
   if (mask != nullptr) {
     if (f16) return cudaErrorInvalidValue;   // masks are served for bf16 only
     return d == 64 ? launch_d<64, false, true>(FATTN_FWD_ARGS)

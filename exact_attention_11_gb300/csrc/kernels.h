@@ -26,24 +26,26 @@ constexpr int kFwdSchedSlots = 64;
 // failure-path test); -1 in normal use.
 // f16 selects fp16 Q, K, V, O (tensor maps of CU_TENSOR_MAP_DATA_TYPE_FLOAT16).
 // mask (bf16 only, causal 0, N a multiple of 16): uint8, key j visible to row i
-// of head bh iff mask[bh * mask_bh_stride + i * N + j] != 0; mask_ranges and
-// mask_flags: its tile summary from launch_mask_summary.
+// of head bh iff mask[bh * mask_bh_stride + i * N + j] != 0; mask_ranges,
+// mask_flags and mask_bits: its tile summary from launch_mask_summary.
 cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             void *o, float *lse, int BH, int N, int d, float scale, int causal,
                             int *sched, int *dev_status, int fault_cta, cudaStream_t stream,
                             bool f16 = false, const uint8_t *mask = nullptr,
                             int64_t mask_bh_stride = 0, const int2 *mask_ranges = nullptr,
-                            const uint8_t *mask_flags = nullptr);
+                            const uint8_t *mask_flags = nullptr, const uint4 *mask_bits = nullptr);
 
 // Tile summary of a boolean mask (mask_tiles.cu) for mask_heads heads (1 when
 // the mask is shared): per 128 x 128 block a flag (0 nothing visible, 1
 // partly, 2 everything), per pair of query tiles the key tiles to process
-// (int2 {kv0 | n_a << 16, n_b}, see mask_tiles.cu).  ws: mask_summary_bytes(mask_heads, N) bytes of device
-// memory; *flags and *ranges point into it.
+// (int2 {kv0 | n_a << 16, n_b}, see mask_tiles.cu), per row of each block its
+// 128 visibility bits (16 bytes).  ws: mask_summary_bytes(mask_heads, N)
+// bytes of 16-byte aligned device memory; *flags, *ranges and *bits point
+// into it.
 size_t mask_summary_bytes(int mask_heads, int N);
 cudaError_t launch_mask_summary(const uint8_t *mask, int64_t bh_stride, int N, int mask_heads,
                                 void *ws, uint8_t **flags, const int2 **ranges,
-                                cudaStream_t stream);
+                                const uint4 **bits, cudaStream_t stream);
 
 // Head dimension 256 (fwd_d256.cu), bf16 or (f16) fp16: tq and tk as for
 // launch_fwd_bf16 (64 x 128 x 1 boxes), tv with 64 x 64 x 1 boxes.

@@ -111,7 +111,9 @@ int fa_forward_f16(const void *q, const void *k, const void *v, void *o, float *
  * 16 (else FA_ERR_ALIGNMENT).  A row with no visible key gets o = 0 and
  * lse = -inf.  Each call first summarises the mask per 128 x 128 block (one
  * read of the mask): key tiles that none of a query block's rows can see are
- * skipped, and fully visible blocks are not read again.  The summary lives
+ * skipped, fully visible blocks are not read again, and a partly visible
+ * block is read back as 16 bytes of visibility bits per row (N * N / 8 bytes
+ * per mask head in all) instead of its 128 mask bytes.  The summary lives
  * in a library-owned buffer grown on demand in stream order; two masked
  * calls must not overlap on the GPU (order them on one stream or with an
  * event).  d is 64 or 128.  Other arguments, layouts and errors as for
