@@ -1,6 +1,7 @@
 // mask_tiles.cu -- a per-tile summary of a boolean attention mask, so that
 // the masked forward skips key tiles no query row of a work item can see and
-// reads mask bytes only for tiles that are partly visible.
+// reads visibility only for tiles that are partly visible, as 16 bytes of
+// bits per row instead of the row's 128 mask bytes.
 //
 // flags[mh][qt][kt] (uint8) for each 128 x 128 block of mask head mh (one head
 // when the mask is shared): 0 = no visible key, 2 = every key visible (and
