@@ -95,8 +95,15 @@ struct Cfg {
   static constexpr int kBar = kV0 + kStages * kTileBytes;
   // Epilogue staging: per softmax warp (2 tiles x 4) its 32 rows x 64 columns
   // of bf16 output, 4 KB.
-  static constexpr int kStage = kBar + 512;
-  static constexpr int kBytes = kStage + 8 * 4096;
+  // FP8: P leaves the scores' TMEM columns for shared memory, two buffers
+  // per query tile of 128 rows x 128 codes in the 128-byte-swizzle K-major
+  // layout (the layout of Q), so that Q K^T(j+1) may overwrite the scores as
+  // soon as the softmax has loaded S(j), without waiting for P V(j).  A
+  // tile's output staging is its first P buffer (free during its epilogue).
+  static constexpr int kStage = kBar + (FP8 ? 1024 : 512);
+  static constexpr int kP = kStage;                  // FP8: 4 x 16 KB
+  static constexpr int kPBuf = BM * BN;              // 16 KB
+  static constexpr int kBytes = kStage + (FP8 ? 4 * kPBuf : 8 * 4096);
   static constexpr int kAlloc = kBytes + 1024;      // slack for 1 KB alignment
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;
@@ -136,8 +143,24 @@ enum : int {
   kBarKEmpty = 20,
   kBarVFull = 24,
   kBarVEmpty = 28,
-  kNumBars = 34
+  kBarSFree = 34,      // FP8, +tile: the softmax has loaded S(j) (4 warps)
+  kBarPVDone = 36,     // FP8, +2 * tile + P buffer: P V(j) has completed
+  kBarPReady1 = 40,    // FP8: kBarPReady's halves for P buffer 1
+  kNumBars = 44
 };
+// The PReady barrier of half h of P(n) of tile t.  FP8: one set per P
+// buffer, since there the softmax may finish P(n + 1) (its scores were
+// computed ahead) before the MMA warp has waited for P(n); a set sees the
+// tiles n, n + 2, ... and the softmax cannot reach n + 2 before P V(n) has
+// been issued.  The phase parity of the wait follows.
+template <bool FP8>
+__device__ __forceinline__ int pready_slot(int t, int h, int n) {
+  return ((FP8 && (n & 1)) ? kBarPReady1 : kBarPReady) + 2 * t + h;
+}
+template <bool FP8>
+__device__ __forceinline__ uint32_t pready_parity(int n) {
+  return static_cast<uint32_t>((FP8 ? n >> 1 : n) & 1);
+}
 // Arrivals that free an item-ring slot: the MMA thread plus every warp of the
 // two softmax warpgroups.
 constexpr int kItemConsumers = 1 + 4 + 4;
@@ -147,6 +170,7 @@ struct SmemMisc {
   int abort;
   int item[2];
 };
+static_assert(8 * kNumBars + sizeof(SmemMisc) <= 512, "barrier area");
 
 // Waits with a time limit for the phase of parity `ph` of an mbarrier; used
 // on the unwind paths.
@@ -251,6 +275,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarPReady + 2 * t), 4);      // one arrival per softmax warp
       mbar_init(bar(kBarPReady + 2 * t + 1), 4);
       mbar_init(bar(kBarODone + t), 1);
+      mbar_init(bar(kBarSFree + t), 4);
+      mbar_init(bar(kBarPVDone + 2 * t), 1);
+      mbar_init(bar(kBarPVDone + 2 * t + 1), 1);
+      mbar_init(bar(kBarPReady1 + 2 * t), 4);
+      mbar_init(bar(kBarPReady1 + 2 * t + 1), 4);
     }
     mbar_init(bar(kBarDrain), 1);
     for (int k = 0; k < 2; ++k) {
@@ -412,97 +441,195 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto wait_p = [&](int t, int h, int cnt) {
-        return mbar_wait(bar(kBarPReady + 2 * t + h), cnt & 1, abort_flag);
+        return mbar_wait(bar(pready_slot<FP8>(t, h, cnt)), pready_parity<FP8>(cnt), abort_flag);
       };
       auto wait_k = [&](int kvi) {
         return mbar_wait(bar(kBarKFull + kvi % S), (kvi / S) & 1, abort_flag);
       };
-      int it = 0, kv = 0, cnt_a = 0, cnt_b = 0;
+      int it = 0, kv = 0;
       bool ok = true;
-      // The next item's QK_A(0) is issued during this item's last step, before
-      // the wait for tile B's last P, so that tile A's softmax of the next item
-      // overlaps tile B's tail instead of following it.
-      int w = 0;
-      bool a0_issued = false;
-      ok = fetch_item(0, w, false);
-      for (int k = 0; ok && w < n_items; ++k) {
-        int q0, bh, n_a, n_b, kv0;
-        sch.decode(w, q0, bh, n_a, n_b, kv0);
-        if (!a0_issued) {
-          if (!(ok = mbar_wait(bar(kBarQFullA), it & 1, abort_flag) && wait_k(kv))) break;
+      if constexpr (FP8) {
+        // P in shared memory: Q K^T(j+1) of a tile is issued as soon as its
+        // softmax has loaded S(j) (SFree) and K(j+1) has landed, ahead of
+        // P V(j), so the next scores are ready when the softmax finishes P(j).
+        // Each commit covers every earlier MMA of this thread, so SFull(j+1)
+        // still certifies P V(j-1) (the P buffer the softmax fills next);
+        // P V(j) signals PVDone for the one thing that needs it, a rescale of O.
+        const uint32_t dp = sdesc_lo(s_base + C::kP, 16);
+        int qk_n[2] = {0, 0}, pv_n[2] = {0, 0};   // Q K^T and P V issued, per tile
+        auto qk_free = [&](int t, int kvi) -> bool {
+          if (qk_n[t] > 0 && !mbar_wait(bar(kBarSFree + t), (qk_n[t] - 1) & 1, abort_flag))
+            return false;
           tc_fence_after();
-          qk(0, kv);
-          if (n_a == 1) mma_commit(bar(kBarQEmptyA));
-        }
-        a0_issued = false;
-        if (!(ok = mbar_wait(bar(kBarQFullB), it & 1, abort_flag) && wait_k(kv))) break;
-        tc_fence_after();
-        qk(1, kv);
-        mma_commit(bar(kBarKEmpty + kv % S));
-        if (n_b == 1) mma_commit(bar(kBarQEmptyB));
-        int w_next = n_items;
-        bool fetched = false;
-        for (int j = 0; j < n_b; ++j) {
-          const int kvj = kv + j;
-          const int st = kvj % S;
-          if (!(ok = mbar_wait(bar(kBarVFull + st), (kvj / S) & 1, abort_flag))) break;
-          bool k_next_ready = false;
-          if (j < n_a) {
-            if (!(ok = wait_p(0, 0, cnt_a))) break;
+          qk(t, kvi);
+          ++qk_n[t];
+          return true;
+        };
+        auto pv_smem = [&](int t, int kvi, bool first) -> bool {
+          const int n = pv_n[t];
+          const uint32_t a = dp + (((t * 2 + (n & 1)) * C::kPBuf) >> 4);
+          const uint32_t b = dv + (((kvi % S) * C::kTileBytes) >> 4);
+          const uint32_t o_col = tmem + (t ? C::kColO1 : C::kColO0);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (!wait_p(t, h, n)) return false;
             tc_fence_after();
-            pv(0, kvj, j == 0, 0);
-            if (!(ok = wait_p(0, 1, cnt_a))) break;
-            tc_fence_after();
-            pv(0, kvj, j == 0, 1);
-            ++cnt_a;
-            if (j == n_a - 1) mma_commit(bar(kBarODone + 0));
+#pragma unroll
+            for (int kk = 2 * h; kk < 2 * h + 2; ++kk)
+              mma_f8_ss_lo(o_col, a + kk * 2, b + kk * 2, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(kBarPVDone + 2 * t + (n & 1)));
+          ++pv_n[t];
+          return true;
+        };
+        int w = 0;
+        bool a0_issued = false;
+        ok = fetch_item(0, w, false);
+        for (int k = 0; ok && w < n_items; ++k) {
+          int q0, bh, n_a, n_b, kv0;
+          sch.decode(w, q0, bh, n_a, n_b, kv0);
+          if (!a0_issued) {
+            if (!(ok = mbar_wait(bar(kBarQFullA), it & 1, abort_flag) && wait_k(kv) &&
+                       qk_free(0, kv)))
+              break;
+            if (n_a == 1) mma_commit(bar(kBarQEmptyA));
+          }
+          a0_issued = false;
+          if (!(ok = mbar_wait(bar(kBarQFullB), it & 1, abort_flag) && wait_k(kv) &&
+                     qk_free(1, kv)))
+            break;
+          mma_commit(bar(kBarKEmpty + kv % S));
+          if (n_b == 1) mma_commit(bar(kBarQEmptyB));
+          int w_next = n_items;
+          bool fetched = false;
+          for (int j = 0; j < n_b; ++j) {
+            const int kvj = kv + j;
+            const int st = kvj % S;
             if (j + 1 < n_a) {
-              if (!(ok = wait_k(kvj + 1))) break;
-              k_next_ready = true;
-              tc_fence_after();
-              qk(0, kvj + 1);
+              if (!(ok = wait_k(kvj + 1) && qk_free(0, kvj + 1))) break;
               if (j + 2 == n_a) mma_commit(bar(kBarQEmptyA));  // last QK_A of the item
             }
+            if (!(ok = mbar_wait(bar(kBarVFull + st), (kvj / S) & 1, abort_flag))) break;
+            if (j < n_a) {
+              if (!(ok = pv_smem(0, kvj, j == 0))) break;
+              if (j == n_a - 1) mma_commit(bar(kBarODone + 0));
+            }
+            if (j == n_b - 1) {
+              // The next item's tile A, once S_A has been read.
+              if (!(ok = fetch_item(k + 1, w_next, false))) break;
+              fetched = true;
+              if (w_next < n_items) {
+                int nq0, nbh, nn_a, nn_b, nkv0;
+                sch.decode(w_next, nq0, nbh, nn_a, nn_b, nkv0);
+                if (!(ok = mbar_wait(bar(kBarQFullA), (it + 1) & 1, abort_flag) &&
+                           wait_k(kv + n_b) && qk_free(0, kv + n_b)))
+                  break;
+                if (nn_a == 1) mma_commit(bar(kBarQEmptyA));
+                a0_issued = true;
+              }
+            }
+            if (j + 1 < n_b) {
+              if (!(ok = wait_k(kvj + 1) && qk_free(1, kvj + 1))) break;
+              mma_commit(bar(kBarKEmpty + (kvj + 1) % S));
+              if (j + 2 == n_b) mma_commit(bar(kBarQEmptyB));  // last QK_B of the item
+            }
+            if (!(ok = pv_smem(1, kvj, j == 0))) break;
+            mma_commit(bar(kBarVEmpty + st));
+            if (j == n_b - 1) mma_commit(bar(kBarODone + 1));
           }
-          if (j == n_b - 1) {
-            // S_A is free (its last PV was issued above or at an earlier step):
-            // start the next item's tile A now.
-            if (!(ok = fetch_item(k + 1, w_next, false))) break;
-            fetched = true;
-            if (w_next < n_items) {
-              int nq0, nbh, nn_a, nn_b, nkv0;
-              sch.decode(w_next, nq0, nbh, nn_a, nn_b, nkv0);
-              if (!(ok = mbar_wait(bar(kBarQFullA), (it + 1) & 1, abort_flag) &&
-                         wait_k(kv + n_b)))
-                break;
+          if (!ok) break;
+          kv += n_b;
+          ++it;
+          if (!fetched && !(ok = fetch_item(k + 1, w_next, false))) break;
+          w = w_next;
+        }
+      } else {
+        int cnt_a = 0, cnt_b = 0;
+        // The next item's QK_A(0) is issued during this item's last step, before
+        // the wait for tile B's last P, so that tile A's softmax of the next item
+        // overlaps tile B's tail instead of following it.
+        int w = 0;
+        bool a0_issued = false;
+        ok = fetch_item(0, w, false);
+        for (int k = 0; ok && w < n_items; ++k) {
+          int q0, bh, n_a, n_b, kv0;
+          sch.decode(w, q0, bh, n_a, n_b, kv0);
+          if (!a0_issued) {
+            if (!(ok = mbar_wait(bar(kBarQFullA), it & 1, abort_flag) && wait_k(kv))) break;
+            tc_fence_after();
+            qk(0, kv);
+            if (n_a == 1) mma_commit(bar(kBarQEmptyA));
+          }
+          a0_issued = false;
+          if (!(ok = mbar_wait(bar(kBarQFullB), it & 1, abort_flag) && wait_k(kv))) break;
+          tc_fence_after();
+          qk(1, kv);
+          mma_commit(bar(kBarKEmpty + kv % S));
+          if (n_b == 1) mma_commit(bar(kBarQEmptyB));
+          int w_next = n_items;
+          bool fetched = false;
+          for (int j = 0; j < n_b; ++j) {
+            const int kvj = kv + j;
+            const int st = kvj % S;
+            if (!(ok = mbar_wait(bar(kBarVFull + st), (kvj / S) & 1, abort_flag))) break;
+            bool k_next_ready = false;
+            if (j < n_a) {
+              if (!(ok = wait_p(0, 0, cnt_a))) break;
               tc_fence_after();
-              qk(0, kv + n_b);
-              if (nn_a == 1) mma_commit(bar(kBarQEmptyA));
-              a0_issued = true;
+              pv(0, kvj, j == 0, 0);
+              if (!(ok = wait_p(0, 1, cnt_a))) break;
+              tc_fence_after();
+              pv(0, kvj, j == 0, 1);
+              ++cnt_a;
+              if (j == n_a - 1) mma_commit(bar(kBarODone + 0));
+              if (j + 1 < n_a) {
+                if (!(ok = wait_k(kvj + 1))) break;
+                k_next_ready = true;
+                tc_fence_after();
+                qk(0, kvj + 1);
+                if (j + 2 == n_a) mma_commit(bar(kBarQEmptyA));  // last QK_A of the item
+              }
+            }
+            if (j == n_b - 1) {
+              // S_A is free (its last PV was issued above or at an earlier step):
+              // start the next item's tile A now.
+              if (!(ok = fetch_item(k + 1, w_next, false))) break;
+              fetched = true;
+              if (w_next < n_items) {
+                int nq0, nbh, nn_a, nn_b, nkv0;
+                sch.decode(w_next, nq0, nbh, nn_a, nn_b, nkv0);
+                if (!(ok = mbar_wait(bar(kBarQFullA), (it + 1) & 1, abort_flag) &&
+                           wait_k(kv + n_b)))
+                  break;
+                tc_fence_after();
+                qk(0, kv + n_b);
+                if (nn_a == 1) mma_commit(bar(kBarQEmptyA));
+                a0_issued = true;
+              }
+            }
+            if (!(ok = wait_p(1, 0, cnt_b))) break;
+            tc_fence_after();
+            pv(1, kvj, j == 0, 0);
+            if (!(ok = wait_p(1, 1, cnt_b))) break;
+            tc_fence_after();
+            pv(1, kvj, j == 0, 1);
+            ++cnt_b;
+            mma_commit(bar(kBarVEmpty + st));
+            if (j == n_b - 1) mma_commit(bar(kBarODone + 1));
+            if (j + 1 < n_b) {
+              if (!k_next_ready && !(ok = wait_k(kvj + 1))) break;
+              tc_fence_after();
+              qk(1, kvj + 1);
+              mma_commit(bar(kBarKEmpty + (kvj + 1) % S));
+              if (j + 2 == n_b) mma_commit(bar(kBarQEmptyB));  // last QK_B of the item
             }
           }
-          if (!(ok = wait_p(1, 0, cnt_b))) break;
-          tc_fence_after();
-          pv(1, kvj, j == 0, 0);
-          if (!(ok = wait_p(1, 1, cnt_b))) break;
-          tc_fence_after();
-          pv(1, kvj, j == 0, 1);
-          ++cnt_b;
-          mma_commit(bar(kBarVEmpty + st));
-          if (j == n_b - 1) mma_commit(bar(kBarODone + 1));
-          if (j + 1 < n_b) {
-            if (!k_next_ready && !(ok = wait_k(kvj + 1))) break;
-            tc_fence_after();
-            qk(1, kvj + 1);
-            mma_commit(bar(kBarKEmpty + (kvj + 1) % S));
-            if (j + 2 == n_b) mma_commit(bar(kBarQEmptyB));  // last QK_B of the item
-          }
+          if (!ok) break;
+          kv += n_b;
+          ++it;
+          if (!fetched && !(ok = fetch_item(k + 1, w_next, false))) break;
+          w = w_next;
         }
-        if (!ok) break;
-        kv += n_b;
-        ++it;
-        if (!fetched && !(ok = fetch_item(k + 1, w_next, false))) break;
-        w = w_next;
       }
       // Drain: every MMA issued above has completed once this phase does.
       mma_commit(bar(kBarDrain));
@@ -566,6 +693,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + c * 32, sv[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_wait_ld(sv[c]);
+        if (FP8) {
+          // The scores are in registers: the MMA warp may overwrite S_T with
+          // the next tile's (P goes to shared memory).
+          tc_fence_before();
+          __syncwarp();
+          if ((threadIdx.x & 31) == 0) mbar_arrive(bar(kBarSFree + t));
+        }
 #define S_(c) sv[(c) >> 5][(c) & 31]
         if (MASK) {
           if (flag != 2) {   // a fully visible tile needs no mask
@@ -598,8 +732,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = tmax;
         }
         // PV_T(j-1) was issued before QK_T(j), so O_T is complete: rescale it
-        // before the first half of P lets PV_T(j) accumulate into it.
+        // before the first half of P lets PV_T(j) accumulate into it.  (FP8:
+        // QK_T(j) goes first, so wait for PV_T(j-1) itself.)
         if (j > 0 && __any_sync(~0u, alpha != 1.f)) {
+          if (FP8) {
+            const int pv = sc - 1;
+            if (!(ok = mbar_wait(bar(kBarPVDone + 2 * t + (pv & 1)), (pv >> 1) & 1, abort_flag)))
+              break;
+            tc_fence_after();
+          }
           const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -643,12 +784,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               pk[(c & 1) * 8 + (e >> 2)] = pack_e4m3x4(p.x, p.y, r.x, r.y);
             }
             if (c & 1) {
-              // Keys 0-63 (then 64-127) of P are in TMEM: let PV_T use them.
-              tmem_st16(s_tmem + (c >> 1) * 16, pk);
-              tmem_wait_st();
+              // Keys 0-63 (then 64-127) of P, 16-byte chunks 4(c >> 1) .. +3
+              // of this row of P buffer sc & 1 (128-byte swizzle: chunk ^ row
+              // % 8), are in shared memory: let PV_T use them.  (The buffer
+              // was last read by PV_T(sc - 2), complete before S_T(sc).)
+              uint8_t *prow = smem + C::kP + (t * 2 + (sc & 1)) * C::kPBuf +
+                              (r_local >> 3) * 1024 + (r_local & 7) * 128;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int ch = 4 * (c >> 1) + q;
+                *reinterpret_cast<uint4 *>(prow + ((ch ^ (r_local & 7)) << 4)) =
+                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+              }
+              fence_proxy_async_smem();
+              tmem_wait_st();   // a rescale of O_T above has landed
               tc_fence_before();
               __syncwarp();
-              if ((threadIdx.x & 31) == 0) mbar_arrive(bar(kBarPReady + 2 * t + (c >> 1)));
+              if ((threadIdx.x & 31) == 0) mbar_arrive(bar(pready_slot<FP8>(t, c >> 1, sc)));
             }
           }
         } else {
@@ -689,7 +841,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // row so that neither side has bank conflicts) and reads it back so that
       // eight lanes store one row's 128 contiguous bytes: 4 lines per store
       // instruction instead of 32.
-      uint8_t *stg = smem + C::kStage + (t * 4 + quarter) * 4096;
+      uint8_t *stg = smem +
+                     (FP8 ? C::kP + t * 2 * C::kPBuf + quarter * 4096
+                          : C::kStage + (t * 4 + quarter) * 4096);
       const int lane = threadIdx.x & 31;
       const int row_w = row - lane;   // this warp's first row
 #pragma unroll

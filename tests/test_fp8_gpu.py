@@ -177,6 +177,27 @@ def test_fp8_forward_benchmark_shape_full():
     _check_forward(q, k, v, True)
 
 
+def test_fp8_forward_many_launches_after_l2_flush():
+    """The benchmark's shape launched 4000 times, each after a write that
+    evicts L2 (so the key and value tiles arrive late and the softmax warps
+    run ahead of the MMA warp): no wait runs out, and every output is
+    bit-identical to the first (the kernel is deterministic)."""
+    B, H, N, d = 2, 16, 4096, 128
+    q, k, v = inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=3)
+    x = _quantize(q, k, v)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=DEV)
+    first, _ = fa.forward_fp8(x, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    for i in range(4000):
+        flush.zero_()
+        o, _ = fa.forward_fp8(x, causal=True)
+        if i % 500 == 499:
+            torch.cuda.synchronize()
+            assert fa.fa_device_status() == 0, f"a wait ran out by launch {i}"
+            assert torch.equal(o, first)
+
+
 def test_fp8_distance_from_bf16_is_the_quantization_error():
     """The FP8 output differs from the bf16 forward of the same inputs by about
     what quantizing the inputs alone explains: the rms of (FP8 - bf16) on the
