@@ -41,6 +41,9 @@
 // While a softmax warpgroup writes one item's output, the tensor core already
 // computes the next item's first S tiles; the next PV_T cannot start before
 // those warps have read O_T, because it waits for their first P_T.
+// The E4M3 instantiation instead keeps P_T in shared memory (two buffers per
+// tile) and issues QK_T(j+1) as soon as the softmax has loaded S_T(j), ahead
+// of PV_T(j): there the softmax waits for PV_T(j) only before a rescale.
 //
 // Rescaling the TMEM-resident output is skipped while the row max has grown
 // by at most 8 (log2 units) since the value in use: exponentials are taken
@@ -422,23 +425,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar(kBarSFull + t));
       };
-      // Half h of O_T += P_T V: keys 64h .. 64h+63 of the tile.
+      // Half h of O_T += P_T V with P_T in TMEM over S_T (16-bit kernels):
+      // keys 64h .. 64h+63 of the tile.
       auto pv = [&](int t, int kvi, bool first, int h) {
         const uint32_t b = dv + (((kvi % S) * C::kTileBytes) >> 4);
         const uint32_t s_col = tmem + (t ? C::kColS1 : C::kColS0);
         const uint32_t o_col = tmem + (t ? C::kColO1 : C::kColO0);
-        if (FP8) {
-          // P_T holds four codes per TMEM column: 32 keys = 8 columns.
 #pragma unroll
-          for (int kk = 2 * h; kk < 2 * h + 2; ++kk)
-            mma_f8_ts_lo(o_col, s_col + kk * 8, b + kk * 2, idesc_pv,
-                         (!first || kk > 0) ? 1u : 0u);
-        } else {
-#pragma unroll
-          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
-            mma_ts_lo(o_col, s_col + kk * 8, b + ((kk * 2048) >> 4), idesc_pv,
-                      (!first || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+          mma_ts_lo(o_col, s_col + kk * 8, b + ((kk * 2048) >> 4), idesc_pv,
+                    (!first || kk > 0) ? 1u : 0u);
       };
       auto wait_p = [&](int t, int h, int cnt) {
         return mbar_wait(bar(pready_slot<FP8>(t, h, cnt)), pready_parity<FP8>(cnt), abort_flag);

@@ -29,18 +29,6 @@ __device__ __forceinline__ void mma_f8_ss_lo(uint32_t d_tmem, uint32_t a_lo, uin
       : "memory");
 }
 
-// D (+)= A B with A in TMEM: row i of A is TMEM lane i, four E4M3 values per
-// 32-bit column, the lowest byte first; K = 32 spans 8 columns.
-__device__ __forceinline__ void mma_f8_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
-                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .b64 db;\n .reg .pred p;\n mov.b64 db, {%2, %5};\n"
-      " setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSdescHi1024)
-      : "memory");
-}
-
 // Four fp32 values -> four E4M3 codes in one word (x0 in the lowest byte),
 // each rounded to nearest even and saturated to +-448.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
