@@ -718,7 +718,8 @@ def gpu_arm(args):
                                  "fp32 FMA rate from SM count and maximum clock", "alu",
                                  "fwd_f32_kernel<64>",
                                  "fa_forward_fp32 fp32 B=1 H=1 N=64 d=64 non-causal (timed in "
-                                 "groups of launches: one launch is a few microseconds)")
+                                 "groups of launches: one launch is a few microseconds)",
+                                 recorded_traffic("fwd_f32_kernel<64>"))
         res["fwd_f32"]["roofline"]["note"] = ("exact fp32 FMAs on the CUDA cores; one 64-row "
                                               "head is two small CTAs, so the figure is launch "
                                               "latency, not a use of the device")
@@ -736,7 +737,8 @@ def gpu_arm(args):
         res["fwd_long"] = leg_out("fwd_long", fwd_flops(**FWD_LONG), 1e12, "TFLOP/s", peak_t,
                                   tensor_kind, "tensor", "fwd_bf16_tc_kernel<128>",
                                   "fa_forward bf16 B=1 H=8 N=16384 d=128 causal, inputs "
-                                  "N(0,1)*0.5")
+                                  "N(0,1)*0.5",
+                                  recorded_traffic("fwd_bf16_tc_kernel<128> 1x8x16384"))
     if "decode" in legs:
         res["decode"] = leg_out("decode", dec_bytes, 1e9, "GB/s", peak_h, hbm_kind, "hbm",
                                 "paged_decode_kernel",
