@@ -32,7 +32,8 @@ Printed JSON line (rank 0), in this order:
                  host<->device copies inside the timed region (copy-in, compute
                  and copy-out of consecutive steps overlap on three streams)
   cpu_baseline   the float64 CPU oracle on the host cores, on bounded samples
---impl reference times that oracle alone (the reference arm of this build).
+--impl reference times that oracle alone, as the comparison arm: the same
+metric and workload, computed by the float64 CPU implementation.
 --only LEG[,LEG] runs only the named legs (no main loop, e2e, CPU baseline or
 hashing), allocating only their workloads: the entry used for profiling.
 Multi-GPU (torchrun): each rank runs an independent replica (weak scaling).
