@@ -164,3 +164,49 @@ def test_decode_workspace_cannot_grow_during_capture():
             g.capture_end()
     assert err is not None and err.status == -2   # FA_ERR_UNSUPPORTED
     torch.cuda.synchronize()
+
+
+def test_forwards_and_backward_in_one_cuda_graph():
+    """The bf16 forward, the masked forward (mask summary and forward, chained
+    by dependent launches), the E4M3 forward and the backward captured into
+    one CUDA graph replay to the eager results: bit for bit, except dQ, whose
+    fp32 sums over key blocks may add in another order (as between two eager
+    calls).  Each captured launch keeps its own work-counter slot."""
+    B, H, N, d = 1, 4, 640, 128
+    q, k, v = (t.to(DEV) for t in inputs.forward_inputs(B, H, N, d, torch.bfloat16, seed=71))
+    do = inputs.grad_output(B, H, N, d, torch.bfloat16, seed=71).to(DEV)
+    g = torch.Generator().manual_seed(71)
+    mask = (torch.rand((N, N), generator=g) < 0.5).to(torch.uint8).to(DEV)
+    x = fa.quantize_fp8(q, k, v)
+    ws = torch.empty((fa.fa_backward_workspace_bytes(B, H, N, d),), dtype=torch.uint8,
+                     device=DEV)
+    o, om, o8 = (torch.empty_like(q) for _ in range(3))
+    lse, lm, l8 = (torch.empty((B, H, N), dtype=torch.float32, device=DEV) for _ in range(3))
+
+    def work():
+        fa.forward(q, k, v, causal=True, out=o, lse=lse)
+        fa.forward_masked(q, k, v, mask, out=om, lse=lm)
+        fa.forward_fp8(x, causal=True, out=o8, lse=l8)
+        return fa.backward(q, k, v, o, lse, do, causal=True, workspace=ws)
+
+    eager_grads = work()   # also sizes the library's mask summary buffer
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (o, lse, om, lm, o8, l8)]
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            grads = work()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for t in (o, lse, om, lm, o8, l8) + tuple(grads):
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert fa.fa_device_status() == 0
+        for got, want in zip((o, lse, om, lm, o8, l8), eager):
+            assert torch.equal(got, want)
+        assert torch.equal(grads[1], eager_grads[1]) and torch.equal(grads[2], eager_grads[2])
+        dq, dq0 = grads[0].float(), eager_grads[0].float()
+        assert (dq - dq0).abs().max().item() <= 2 ** -7 * dq0.abs().max().item()
