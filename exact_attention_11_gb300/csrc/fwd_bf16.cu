@@ -199,9 +199,11 @@ struct ItemDecoder {
     kv0 = 0;
     if (ranges != nullptr) {
       const int2 r = ranges[static_cast<int64_t>(mask_shared ? 0 : bh) * n_qblocks + qb];
-      kv0 = r.x & 0xffff;
-      n_a = r.x >> 16;
-      n_b = r.y;
+      // Clamped into the sequence's key tiles, so that no summary can make
+      // the item address tiles, flags or bits outside their buffers.
+      kv0 = min(r.x & 0xffff, n_kv_total - 1);
+      n_b = max(1, min(r.y, n_kv_total - kv0));
+      n_a = max(1, min(r.x >> 16, n_b));
       return;
     }
     n_a = causal ? min(2 * qb + 1, n_kv_total) : n_kv_total;
