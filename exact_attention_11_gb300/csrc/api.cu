@@ -436,7 +436,7 @@ int fa_forward_fp8(const void *q8, const void *k8, const void *vt8, const float 
   if (d != 128) return FA_ERR_UNSUPPORTED;
   const int BH = B * H;
   if (BH == 0 || N == 0) return FA_OK;
-  int dev = 0;
+  int dev = 0, fault_cta = -1;
   int *sched = nullptr;
   CUtensorMap tq, tk, tvt;
   {
@@ -445,13 +445,15 @@ int fa_forward_fp8(const void *q8, const void *k8, const void *vt8, const float 
     if ((rc = get_encoder()) != FA_OK) return rc;
     DeviceState &st = g_dev[dev];
     sched = sched_slot(st, reinterpret_cast<cudaStream_t>(stream));
+    fault_cta = st.inject_fault == 1 ? 0 : -1;
+    if (st.inject_fault == 1) st.inject_fault = 0;
   }
   if ((rc = encode_e4m3_map(&tq, q8, BH, N, d)) != FA_OK) return rc;
   if ((rc = encode_e4m3_map(&tk, k8, BH, N, d)) != FA_OK) return rc;
   if ((rc = encode_e4m3_map(&tvt, vt8, BH, d, (int)fp8_vt_stride(N))) != FA_OK) return rc;
   return cuda_status(fattn::launch_fwd_fp8(tq, tk, tvt, q_scale, k_scale, v_scale, o, lse, BH, N,
                                            scale, causal ? 1 : 0, sched, g_dev[dev].status,
-                                           reinterpret_cast<cudaStream_t>(stream)));
+                                           fault_cta, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 unsigned long long fa_backward_workspace_bytes(int B, int H, int N, int d) {

@@ -976,10 +976,10 @@ cudaError_t launch_fwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const 
 cudaError_t launch_fwd_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tvt,
                            const float *q_scale, const float *k_scale, const float *v_scale,
                            void *o, float *lse, int BH, int N, float scale, int causal,
-                           int *sched, int *dev_status, cudaStream_t stream) {
+                           int *sched, int *dev_status, int fault_cta, cudaStream_t stream) {
   return launch_d<128, false, false, true>(tq, tk, tvt, o, lse, BH, N, scale, causal, sched,
-                                           dev_status, -1, stream, nullptr, 0, q_scale, k_scale,
-                                           v_scale);
+                                           dev_status, fault_cta, stream, nullptr, 0, q_scale,
+                                           k_scale, v_scale);
 }
 
 }  // namespace fattn

@@ -56,11 +56,12 @@ cudaError_t launch_fwd_d256(const CUtensorMap &tq, const CUtensorMap &tk, const 
 // FP8 forward (fwd_bf16.cu, d = 128): tq, tk are E4M3 maps {128, N, B*H}
 // with 128 x 128 x 1 boxes, tvt the E4M3 map {Npad, 128, B*H} of V^T, same
 // boxes; all with the 128-byte swizzle.  q_scale, k_scale: one fp32 per
-// 128-row block of each head; v_scale: one per head.  o is bf16.
+// 128-row block of each head; v_scale: one per head.  o is bf16.  fault_cta
+// as for launch_fwd_bf16.
 cudaError_t launch_fwd_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tvt,
                            const float *q_scale, const float *k_scale, const float *v_scale,
                            void *o, float *lse, int BH, int N, float scale, int causal,
-                           int *sched, int *dev_status, cudaStream_t stream);
+                           int *sched, int *dev_status, int fault_cta, cudaStream_t stream);
 
 // FP8 block quantization (fp8_quant.cu, d = 128); v_amax: the workspace of
 // fp8_quant_workspace_bytes(BH, N) bytes; signs: 128 fp32 +-1 values or null.

@@ -362,9 +362,10 @@ int fa_paged_decode_noalloc(const void *q, const void *k_cache, const void *v_ca
 /*
  * fa_debug_inject_fault -- test hook for the device-side failure path.
  *
- * mode 1 arms the current device: the next fa_forward launched on it makes
- * its first CTA's TMA producer stop after loading that CTA's first query
- * tiles, as if a copy had been lost.  The MMA warp's bounded wait for the
+ * mode 1 arms the current device: the next tensor-core forward launched on
+ * it (fa_forward, fa_forward_f16, fa_forward_masked or fa_forward_fp8, for
+ * head dimension 64 or 128) makes its first CTA's TMA producer stop after
+ * loading that CTA's first query tiles, as if a copy had been lost.  The MMA warp's bounded wait for the
  * missing key tile then runs out (after about 2 s), the CTA unwinds (in-flight
  * copies and MMAs drained, tensor memory freed) and fa_device_status()
  * returns FA_ERR_TIMEOUT.  That launch's output is incomplete; the CUDA

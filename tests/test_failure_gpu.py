@@ -1,7 +1,8 @@
 """Device-side failure detection without a GPU fault.
 
-fa_debug_inject_fault(1) makes one CTA of the next forward lose its key-tile
-copies (its producer stops after the query tiles); mode 2 does the same to
+fa_debug_inject_fault(1) makes one CTA of the next forward (bf16, fp16,
+masked or E4M3) lose its key-tile copies (its producer stops after the query
+tiles); mode 2 does the same to
 the next backward (its K and V copies).  The MMA warp's bounded
 wait for them runs out after about 2 s, the CTA unwinds, and the host reads
 FA_ERR_TIMEOUT from fa_device_status().  Nothing traps, faults or hangs: the
@@ -40,6 +41,31 @@ def test_lost_copy_times_out_and_context_survives():
     ro, rl = oracle.attention_forward(q, k, v, 128 ** -0.5, True)
     assert np.abs(o.float().cpu().numpy() - ro).max() <= 2e-2
     assert np.abs(lse.cpu().numpy() - rl).max() <= 1e-2
+
+
+def test_fp8_forward_lost_copy_times_out_and_context_survives():
+    """The same failure path in the E4M3 forward, which keeps P in shared
+    memory with its own MMA issue order and barriers: mode 1 arms it too;
+    the wait runs out, every role unwinds, and the next call gives the same
+    bits as a clean call before the fault."""
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in inputs.forward_inputs(1, 4, 640, 128, torch.bfloat16, seed=33))
+    x = fa.quantize_fp8(q, k, v)
+    clean, clean_lse = fa.forward_fp8(x, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    fa.fa_debug_inject_fault(1)
+    t0 = time.perf_counter()
+    fa.forward_fp8(x, causal=True)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert fa.fa_device_status() == -5          # FA_ERR_TIMEOUT, reported once
+    assert fa.fa_device_status() == 0
+    assert 1.0 < waited < 30.0
+    o, lse = fa.forward_fp8(x, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    assert torch.equal(o, clean) and torch.equal(lse, clean_lse)
 
 
 @pytest.mark.parametrize("d", [128, 64])
